@@ -1,0 +1,205 @@
+"""ctypes binding of libfa (include/fa.h): argument marshalling only.
+
+The functions named like the C entry points take the same arguments in the
+same order; pointer arguments may be ints (device addresses) or torch tensors
+(their ``data_ptr()``), ``stream`` may be an int, a ``torch.cuda.Stream`` or
+None (the current torch stream). They return the fa_status code as an int.
+
+The tensor-level helpers ``forward``, ``backward`` and ``decode`` allocate the
+outputs with torch, call the C entry point and raise :class:`FAError` on any
+status other than FA_OK. Every step of the computation runs in the library's
+CUDA kernels; there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
+FA_F32, FA_F16, FA_BF16 = 0, 1, 2
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
+
+# every symbol include/fa.h declares
+EXPORTS = (
+    "fa_fwd",
+    "fa_bwd",
+    "fa_bwd_workspace_bytes",
+    "fa_decode",
+    "fa_decode_workspace_bytes",
+    "fa_last_status",
+    "fa_status_string",
+    "fa_last_error_message",
+    "fa_set_wait_budget_ns",
+)
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = lib().fa_last_error_message().decode(errors="replace")
+        name = lib().fa_status_string(status).decode(errors="replace")
+        super().__init__(f"{where}: {name}: {msg}")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built (there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m exact_attention_gb300.build` "
+                           "(there is no fallback implementation)")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i, f, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int
+    L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    L.fa_fwd.restype = st
+    L.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, i, vp]
+    L.fa_bwd.restype = st
+    L.fa_decode.argtypes = [vp] * 5 + [i, i, i, i, f, i, i, vp]
+    L.fa_decode.restype = st
+    L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
+    L.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
+    L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_last_status.argtypes = [vp]
+    L.fa_last_status.restype = st
+    L.fa_status_string.argtypes = [st]
+    L.fa_status_string.restype = ctypes.c_char_p
+    L.fa_last_error_message.argtypes = []
+    L.fa_last_error_message.restype = ctypes.c_char_p
+    L.fa_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
+    L.fa_set_wait_budget_ns.restype = st
+    _lib = L
+    return L
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+# ------------------------------------------------------- C entry points
+def fa_fwd(Q, K, V, O, LSE, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
+    return lib().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, M, N, D, float(scale), int(causal),
+                        int(dtype), _stream(stream))
+
+
+def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
+    return lib().fa_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+                        _ptr(delta_ws), B, H, M, N, D, float(scale), int(causal), int(dtype), _stream(stream))
+
+
+def fa_decode(q, Kcache, Vcache, O, partial_ws, B, H, N, D, scale, n_splits, dtype, stream=None) -> int:
+    return lib().fa_decode(_ptr(q), _ptr(Kcache), _ptr(Vcache), _ptr(O), _ptr(partial_ws), B, H, N, D,
+                           float(scale), int(n_splits), int(dtype), _stream(stream))
+
+
+def fa_decode_workspace_bytes(B, H, D, n_splits) -> int:
+    return lib().fa_decode_workspace_bytes(B, H, D, n_splits)
+
+
+def fa_bwd_workspace_bytes(B, H, M) -> int:
+    return lib().fa_bwd_workspace_bytes(B, H, M)
+
+
+def fa_last_status(stream=None) -> int:
+    return lib().fa_last_status(_stream(stream))
+
+
+def fa_status_string(status: int) -> str:
+    return lib().fa_status_string(status).decode()
+
+
+def fa_last_error_message() -> str:
+    return lib().fa_last_error_message().decode(errors="replace")
+
+
+def fa_set_wait_budget_ns(ns: int) -> int:
+    return lib().fa_set_wait_budget_ns(int(ns))
+
+
+# ------------------------------------------------------- tensor helpers
+def fa_dtype(t) -> int:
+    import torch
+    m = {torch.float32: FA_F32, torch.float16: FA_F16, torch.bfloat16: FA_BF16}
+    if t.dtype not in m:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+def _check(status: int, where: str):
+    if status != FA_OK:
+        raise FAError(status, where)
+
+
+def _dims4(t, name):
+    if t.dim() != 4 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous 4-D CUDA tensor [B, H, rows, D]")
+    return t.shape
+
+
+def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, stream=None):
+    """O, LSE = attention(q [B,H,M,D], k/v [B,H,N,D]); LSE is float32 [B,H,M]."""
+    import torch
+    B, H, M, D = _dims4(q, "q")
+    N = _dims4(k, "k")[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    _check(fa_fwd(q, k, v, out, lse, B, H, M, N, D, scale, causal, fa_dtype(q), stream), "fa_fwd")
+    return out, lse
+
+
+def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=None):
+    """dQ, dK, dV of sum(do * o); also returns the delta workspace (rowsum(dO o O))."""
+    import torch
+    B, H, M, D = _dims4(q, "q")
+    N = _dims4(k, "k")[2]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    _check(fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, B, H, M, N, D, scale, causal, fa_dtype(q), stream),
+           "fa_bwd")
+    return dq, dk, dv, ws
+
+
+def decode(q, k_cache, v_cache, scale: float, n_splits: int, out=None, workspace=None, stream=None):
+    """O [B,H,1,D] for one query row per (batch, head); returns (O, partial workspace)."""
+    import torch
+    B, H, one, D = _dims4(q, "q")
+    if one != 1:
+        raise ValueError("decode takes one query row per (batch, head)")
+    N = _dims4(k_cache, "k_cache")[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        nbytes = fa_decode_workspace_bytes(B, H, D, n_splits)
+        workspace = torch.empty((max(nbytes, 4) // 4,), dtype=torch.float32, device=q.device)
+    _check(fa_decode(q, k_cache, v_cache, out, workspace, B, H, N, D, scale, n_splits, fa_dtype(q), stream),
+           "fa_decode")
+    return out, workspace
+
+
+def split_workspace(ws, B: int, H: int, D: int, n_splits: int):
+    """Views (O_s [B*H, n_splits, D], m_s [B*H, n_splits], l_s [B*H, n_splits]) of a decode workspace."""
+    BH = B * H
+    o = ws[: BH * n_splits * D].view(BH, n_splits, D)
+    m = ws[BH * n_splits * D: BH * n_splits * (D + 1)].view(BH, n_splits)
+    l_ = ws[BH * n_splits * (D + 1): BH * n_splits * (D + 2)].view(BH, n_splits)
+    return o, m, l_

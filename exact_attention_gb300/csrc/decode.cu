@@ -1,0 +1,387 @@
+// Flash decoding: one query row per (batch, head) against a long KV cache.
+//
+// Follows "Flash decoding" (linear algebra for programmers, part 4),
+// "Overview of the algorithm": the keys are split into n_splits chunks; the
+// split kernel runs the online softmax over one chunk and writes the
+// unnormalised partial (O_s, m_s, l_s); the combine kernel rescales every
+// partial by e^{m_s - m_g} and divides once by l_g.
+//
+// GB300 design (not the page's): the split kernel is HBM-bound (one FMA per
+// byte), so each CTA streams its chunk of K and V through a 3-stage ring of
+// shared-memory buffers filled by bulk TMA copies (cp.async.bulk, one producer
+// warp, L2 evict-first), and 4 compute warps read 16-byte vectors from it.
+// A "row unit" of D*size/16 lanes owns one key at a time; each unit carries
+// its own (m, l, acc) online-softmax state in registers, and the units of the
+// CTA are merged with the (m, l) monoid at the end ("Flash Attention" notes,
+// "Deriving the online softmax").
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kDecWarps = 4;                      // compute warps
+constexpr int kDecThreads = (kDecWarps + 1) * 32;  // + one producer warp
+constexpr int kDecStages = 3;
+constexpr int kDecStageBytes = 16384;              // K + V bytes per stage
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int DT>
+struct Elem;
+template <>
+struct Elem<kF32> {
+  using T = float;
+  static constexpr int kSize = 4;
+  __device__ static void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x);
+    f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z);
+    f[3] = __uint_as_float(u.w);
+  }
+  __device__ static T from_f32(float x) { return x; }
+};
+template <>
+struct Elem<kF16> {
+  using T = __half;
+  static constexpr int kSize = 2;
+  __device__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      float2 t = __half22float2(h);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ static T from_f32(float x) { return __float2half_rn(x); }
+};
+template <>
+struct Elem<kBF16> {
+  using T = __nv_bfloat16;
+  static constexpr int kSize = 2;
+  __device__ static void unpack(const uint4& u, float* f) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+  __device__ static T from_f32(float x) { return __float2bfloat16_rn(x); }
+};
+
+template <int D, int DT>
+struct DecCfg {
+  static constexpr int kES = Elem<DT>::kSize;
+  static constexpr int kRow = D * kES;             // bytes per key row
+  static constexpr int kLPK = kRow / 16;           // lanes per key (one 16-byte vector each)
+  static constexpr int kKPW = 32 / kLPK;           // keys per warp in parallel
+  static constexpr int kEPL = 16 / kES;            // elements per lane
+  static constexpr int kNU = kDecWarps * kKPW;     // row units per CTA
+  static constexpr int kTK = kDecStageBytes / (2 * kRow);  // keys per stage
+  static constexpr int kG = kTK / kNU;             // keys per row unit per stage
+  static_assert(kLPK >= 1 && kLPK <= 32 && kG >= 1, "decode tiling");
+};
+
+struct DecSmemHdr {
+  unsigned long long full[kDecStages];
+  unsigned long long empty[kDecStages];
+  int abort_flag;
+};
+
+template <int D, int DT>
+__global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typename Elem<DT>::T* __restrict__ q,
+                                                                   const typename Elem<DT>::T* __restrict__ K,
+                                                                   const typename Elem<DT>::T* __restrict__ V,
+                                                                   float* __restrict__ ws, int BH, int N,
+                                                                   int n_splits, float scale_log2,
+                                                                   DevStatus* status,
+                                                                   unsigned long long budget_ns) {
+  using C = DecCfg<D, DT>;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  DecSmemHdr* hdr = reinterpret_cast<DecSmemHdr*>(smem_raw);
+  uint8_t* ring = smem_raw + 128;  // stage st: K at ring + st*kDecStageBytes, V right after K
+  float* red = reinterpret_cast<float*>(ring + kDecStages * kDecStageBytes);  // merge scratch
+
+  const int split = blockIdx.x;
+  const int bh = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  const int chunk = (N + n_splits - 1) / n_splits;
+  const int n_start = min(split * chunk, N);
+  const int n_end = min(n_start + chunk, N);
+  const int nkeys = n_end - n_start;
+  const int nstage = (nkeys + C::kTK - 1) / C::kTK;
+
+  float* ws_O = ws + (static_cast<size_t>(bh) * n_splits + split) * D;
+  float* ws_m = ws + static_cast<size_t>(BH) * n_splits * D + static_cast<size_t>(bh) * n_splits + split;
+  float* ws_l = ws_m + static_cast<size_t>(BH) * n_splits;
+
+  if (nkeys <= 0) {  // empty split: the identity of the merge
+    for (int d = threadIdx.x; d < D; d += blockDim.x) ws_O[d] = 0.f;
+    if (threadIdx.x == 0) {
+      *ws_m = -INFINITY;
+      *ws_l = 0.f;
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kDecStages; ++s) {
+      ptx::mbar_init(ptx::smem_u32(&hdr->full[s]), 1);
+      ptx::mbar_init(ptx::smem_u32(&hdr->empty[s]), kDecWarps);
+    }
+    hdr->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernDecodeSplit};
+
+  const size_t head_off = static_cast<size_t>(bh) * N * D;
+
+  if (warp == kDecWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      const uint64_t pol = ptx::policy_evict_first();
+      const char* kb = reinterpret_cast<const char*>(K + head_off);
+      const char* vb = reinterpret_cast<const char*>(V + head_off);
+      int issued = 0;
+      for (int it = 0; it < nstage; ++it) {
+        const int st = it % kDecStages;
+        const uint32_t ph = static_cast<uint32_t>(it / kDecStages) & 1u;
+        if (!ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ph ^ 1u, wc, 1)) break;
+        const int k0 = n_start + it * C::kTK;
+        const int nk = min(C::kTK, n_end - k0);
+        const uint32_t bytes = static_cast<uint32_t>(nk) * C::kRow;
+        const uint32_t full = ptx::smem_u32(&hdr->full[st]);
+        ptx::mbar_arrive_expect_tx(full, 2u * bytes);
+        uint8_t* sk = ring + st * kDecStageBytes;
+        ptx::bulk_load(ptx::smem_u32(sk), kb + static_cast<size_t>(k0) * C::kRow, bytes, full, pol);
+        ptx::bulk_load(ptx::smem_u32(sk + kDecStageBytes / 2), vb + static_cast<size_t>(k0) * C::kRow, bytes, full,
+                       pol);
+        issued = it + 1;
+      }
+      if (hdr->abort_flag) {  // let copies already in flight land before the CTA exits
+        for (int it = max(0, issued - kDecStages); it < issued; ++it)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[it % kDecStages]),
+                               static_cast<uint32_t>(it / kDecStages) & 1u, 100000000ull);
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int ru = warp * C::kKPW + lane / C::kLPK;  // row unit
+  const int sl = lane % C::kLPK;                   // 16-byte slot within the key row
+  float qv[C::kEPL];
+  {
+    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(q + static_cast<size_t>(bh) * D) +
+                                                    sl * 16);
+    Elem<DT>::unpack(u, qv);
+#pragma unroll
+    for (int e = 0; e < C::kEPL; ++e) qv[e] *= scale_log2;  // scores come out in log2 units
+  }
+  float m = -INFINITY, l = 0.f;
+  float acc[C::kEPL];
+#pragma unroll
+  for (int e = 0; e < C::kEPL; ++e) acc[e] = 0.f;
+
+  for (int it = 0; it < nstage; ++it) {
+    const int st = it % kDecStages;
+    const uint32_t ph = static_cast<uint32_t>(it / kDecStages) & 1u;
+    if (!ptx::mbar_wait(ptx::smem_u32(&hdr->full[st]), ph, wc, 2)) break;
+    const int nk = min(C::kTK, n_end - (n_start + it * C::kTK));
+    const uint8_t* sk = ring + st * kDecStageBytes;
+    const uint8_t* sv = sk + kDecStageBytes / 2;
+
+    float s[C::kG];
+#pragma unroll
+    for (int g = 0; g < C::kG; ++g) {
+      const int kk = ru + g * C::kNU;
+      float part = 0.f;
+      if (kk < nk) {
+        float kf[C::kEPL];
+        Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sk + kk * C::kRow + sl * 16), kf);
+#pragma unroll
+        for (int e = 0; e < C::kEPL; ++e) part = fmaf(qv[e], kf[e], part);
+      }
+#pragma unroll
+      for (int o = C::kLPK / 2; o >= 1; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+      s[g] = kk < nk ? part : -INFINITY;
+    }
+    float mb = s[0];
+#pragma unroll
+    for (int g = 1; g < C::kG; ++g) mb = fmaxf(mb, s[g]);
+    const float m_new = fmaxf(m, mb);
+    const float m_safe = m_new == -INFINITY ? 0.f : m_new;
+    const float corr = ptx::ex2(m - m_safe);
+    float p[C::kG];
+    float ps = 0.f;
+#pragma unroll
+    for (int g = 0; g < C::kG; ++g) {
+      p[g] = ptx::ex2(s[g] - m_safe);
+      ps += p[g];
+    }
+    l = fmaf(l, corr, ps);
+    m = m_new;
+#pragma unroll
+    for (int e = 0; e < C::kEPL; ++e) acc[e] *= corr;
+#pragma unroll
+    for (int g = 0; g < C::kG; ++g) {
+      const int kk = ru + g * C::kNU;
+      if (kk < nk) {
+        float vf[C::kEPL];
+        Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sv + kk * C::kRow + sl * 16), vf);
+#pragma unroll
+        for (int e = 0; e < C::kEPL; ++e) acc[e] = fmaf(p[g], vf[e], acc[e]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->empty[st]));
+  }
+
+  // Merge the row units of this CTA: (m, l) monoid, then write the partial.
+  float* red_m = red;                 // [kNU]
+  float* red_l = red + C::kNU;        // [kNU]
+  float* red_acc = red + 2 * C::kNU;  // [kNU][D]
+  if (sl == 0) {
+    red_m[ru] = m;
+    red_l[ru] = l;
+  }
+#pragma unroll
+  for (int e = 0; e < C::kEPL; ++e) red_acc[ru * D + sl * C::kEPL + e] = acc[e];
+  asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
+  if (hdr->abort_flag) return;
+
+  float mg = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < C::kNU; ++u) mg = fmaxf(mg, red_m[u]);
+  const float mg_safe = mg == -INFINITY ? 0.f : mg;
+  for (int d = threadIdx.x; d < D; d += kDecWarps * 32) {
+    float o = 0.f;
+#pragma unroll
+    for (int u = 0; u < C::kNU; ++u) o = fmaf(ptx::ex2(red_m[u] - mg_safe), red_acc[u * D + d], o);
+    ws_O[d] = o;
+  }
+  if (threadIdx.x == 0) {
+    float lg = 0.f;
+#pragma unroll
+    for (int u = 0; u < C::kNU; ++u) lg = fmaf(ptx::ex2(red_m[u] - mg_safe), red_l[u], lg);
+    *ws_m = mg * kLn2;  // natural-log units, as in the page's equations (-inf stays -inf)
+    *ws_l = lg;
+  }
+}
+
+constexpr int kCombThreads = 128;
+constexpr int kCombChunk = 1024;
+
+template <int D, int DT>
+__global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const float* __restrict__ ws,
+                                                                      typename Elem<DT>::T* __restrict__ O, int BH,
+                                                                      int n_splits) {
+  __shared__ float w[kCombChunk];
+  __shared__ float red[kCombThreads / 32];
+  __shared__ float s_mg, s_lg;
+  const int bh = blockIdx.x;
+  const float* Os = ws + static_cast<size_t>(bh) * n_splits * D;
+  const float* ms = ws + static_cast<size_t>(BH) * n_splits * D + static_cast<size_t>(bh) * n_splits;
+  const float* ls = ms + static_cast<size_t>(BH) * n_splits;
+  const int tid = threadIdx.x;
+
+  // PDL: wait until the split kernel's partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  float mx = -INFINITY;
+  for (int s = tid; s < n_splits; s += kCombThreads) mx = fmaxf(mx, ms[s]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  if ((tid & 31) == 0) red[tid >> 5] = mx;
+  __syncthreads();
+  if (tid == 0) {
+    float v = red[0];
+    for (int i = 1; i < kCombThreads / 32; ++i) v = fmaxf(v, red[i]);
+    s_mg = v;
+  }
+  __syncthreads();
+  const float mg = s_mg;
+
+  float lsum = 0.f, o = 0.f;
+  for (int c0 = 0; c0 < n_splits; c0 += kCombChunk) {
+    const int cn = min(kCombChunk, n_splits - c0);
+    for (int s = tid; s < cn; s += kCombThreads) {
+      const float ww = ptx::ex2((ms[c0 + s] - mg) * kLog2e);  // e^{m_s - m_g}; empty split -> 0
+      w[s] = ww;
+      lsum = fmaf(ww, ls[c0 + s], lsum);
+    }
+    __syncthreads();
+    if (tid < D)
+      for (int s = 0; s < cn; ++s) o = fmaf(w[s], Os[static_cast<size_t>(c0 + s) * D + tid], o);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, off);
+  if ((tid & 31) == 0) red[tid >> 5] = lsum;
+  __syncthreads();
+  if (tid == 0) {
+    float v = 0.f;
+    for (int i = 0; i < kCombThreads / 32; ++i) v += red[i];
+    s_lg = v;
+  }
+  __syncthreads();
+  if (tid < D) O[static_cast<size_t>(bh) * D + tid] = Elem<DT>::from_f32(o / s_lg);
+}
+
+template <int D, int DT>
+cudaError_t launch_decode_t(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N,
+                            float scale, int n_splits, const LaunchCtx& ctx) {
+  using C = DecCfg<D, DT>;
+  using T = typename Elem<DT>::T;
+  const size_t smem = 128 + kDecStages * kDecStageBytes + (2 * C::kNU + C::kNU * D) * sizeof(float);
+  auto kern = decode_split_kernel<D, DT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_splits, BH);
+  kern<<<grid, kDecThreads, smem, ctx.stream>>>(static_cast<const T*>(q), static_cast<const T*>(K),
+                                                static_cast<const T*>(V), ws, BH, N, n_splits, scale * kLog2e,
+                                                ctx.status, ctx.wait_budget_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(BH);
+  cfg.blockDim = dim3(kCombThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, DT>, static_cast<const float*>(ws), static_cast<T*>(O),
+                            BH, n_splits);
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N, int D,
+                          float scale, int n_splits, int dtype, const LaunchCtx& ctx) {
+  if (BH > 65535) return cudaErrorNotSupported;  // grid.y limit of the split kernel
+#define FA_DEC(DD, TT) \
+  if (D == DD && dtype == TT) return launch_decode_t<DD, TT>(q, K, V, O, ws, BH, N, scale, n_splits, ctx);
+  FA_DEC(64, kF32)
+  FA_DEC(64, kF16)
+  FA_DEC(64, kBF16)
+  FA_DEC(128, kF32)
+  FA_DEC(128, kF16)
+  FA_DEC(128, kBF16)
+#undef FA_DEC
+  return cudaErrorNotSupported;
+}
+
+}  // namespace fa

@@ -1,0 +1,304 @@
+// The C ABI of libfa: argument checks, per-device state, TMA descriptor
+// encoding and dispatch to the kernel launchers. See include/fa.h for the
+// contract of each entry point.
+#include <cudaTypedefs.h>
+
+#include <cinttypes>
+#include <climits>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/fa.h"
+#include "fa_internal.cuh"
+
+namespace fa {
+
+__device__ DevStatus g_status;  // one per device that loads the library
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevState {
+  bool ready = false;
+  int num_sms = 0;
+  DevStatus* status = nullptr;  // device address of g_status on this device
+};
+
+std::mutex g_mutex;
+DevState g_dev[kMaxDevices];
+unsigned long long g_wait_budget_ns = 0;  // 0 = not yet read from the environment
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+thread_local char t_msg[512] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_msg, sizeof(t_msg), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(FA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+unsigned long long wait_budget() {
+  if (g_wait_budget_ns == 0) {
+    unsigned long long v = 2000000000ull;
+    if (const char* e = std::getenv("FA_WAIT_BUDGET_NS")) {
+      unsigned long long x = std::strtoull(e, nullptr, 10);
+      if (x >= 1000ull) v = x;
+    }
+    g_wait_budget_ns = v;
+  }
+  return g_wait_budget_ns;
+}
+
+// Per-device set-up, done once with that device current: SM count and the
+// device address of the status word.
+fa_status device_state(DevState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DevState& st = g_dev[dev];
+  if (!st.ready) {
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    DevStatus zero{};
+    e = cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+    st.num_sms = sms;
+    st.status = static_cast<DevStatus*>(p);
+    st.ready = true;
+  }
+  wait_budget();
+  *out = &st;
+  return FA_OK;
+}
+
+fa_status make_ctx(LaunchCtx* ctx, void* stream) {
+  DevState* st = nullptr;
+  fa_status s = device_state(&st);
+  if (s != FA_OK) return s;
+  ctx->status = st->status;
+  ctx->num_sms = st->num_sms;
+  ctx->wait_budget_ns = wait_budget();
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  return FA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+fa_status check_dtype(int dtype) {
+  if (dtype != FA_F32 && dtype != FA_F16 && dtype != FA_BF16) return fail(FA_ERR_INVALID, "unknown dtype %d", dtype);
+  return FA_OK;
+}
+
+fa_status check_ptr(const void* p, const char* name) {
+  if (p == nullptr) return fail(FA_ERR_INVALID, "%s is NULL", name);
+  if (!aligned16(p)) return fail(FA_ERR_INVALID, "%s is not 16-byte aligned", name);
+  return FA_OK;
+}
+
+// Rejects element counts whose byte size or whose row index would overflow the
+// 32-bit row coordinates the kernels and TMA descriptors use.
+fa_status check_sizes(int B, int H, int M, int N, int D) {
+  if (B < 0 || H < 0 || M < 0 || N < 0 || D <= 0)
+    return fail(FA_ERR_INVALID, "negative or zero size (B=%d H=%d M=%d N=%d D=%d)", B, H, M, N, D);
+  const long long bh = static_cast<long long>(B) * H;
+  if (bh > INT_MAX) return fail(FA_ERR_INVALID, "B*H overflows int");
+  if (bh * static_cast<long long>(M > N ? M : N) > static_cast<long long>(INT_MAX))
+    return fail(FA_ERR_INVALID, "B*H*max(M,N) = %lld rows overflows int", bh * (M > N ? M : N));
+  if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension D=%d (supported: 64, 128)", D);
+  return FA_OK;
+}
+
+// The tensor-core paths fold scale into the exponent after taking the row
+// maximum of the raw scores, which needs scale > 0.
+fa_status check_scale(float scale, bool positive) {
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(FA_ERR_INVALID, "scale must be finite (got %g)", static_cast<double>(scale));
+  if (positive && !(scale > 0.f)) return fail(FA_ERR_INVALID, "scale must be > 0 (got %g)", static_cast<double>(scale));
+  return FA_OK;
+}
+
+#define FA_TRY(expr)                 \
+  do {                               \
+    fa_status _s = (expr);           \
+    if (_s != FA_OK) return _s;      \
+  } while (0)
+
+}  // namespace
+
+bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_rows) {
+  if (g_encode == nullptr) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q{};
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const size_t es = dtype_size(dtype);
+  CUtensorMapDataType t = dtype == kF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                          : dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {inner * es, inner * rows * es};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_status_string(fa_status s) {
+  switch (s) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID: return "FA_ERR_INVALID: invalid argument";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: unsupported configuration";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA: CUDA error";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up a bounded wait";
+  }
+  return "unknown fa_status";
+}
+
+const char* fa_last_error_message(void) { return t_msg; }
+
+fa_status fa_set_wait_budget_ns(unsigned long long ns) {
+  if (ns < 1000ull) return fail(FA_ERR_INVALID, "wait budget %llu ns is below 1000 ns", ns);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_wait_budget_ns = ns;
+  return FA_OK;
+}
+
+size_t fa_bwd_workspace_bytes(int B, int H, int M) {
+  if (B <= 0 || H <= 0 || M <= 0) return 0;
+  return static_cast<size_t>(B) * H * M * sizeof(float);
+}
+
+size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits) {
+  if (B <= 0 || H <= 0 || D <= 0 || n_splits <= 0) return 0;
+  return static_cast<size_t>(B) * H * n_splits * (D + 2) * sizeof(float);
+}
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int M, int N, int D,
+                 float scale, int causal, fa_dtype dtype, void* stream) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, M, N, D));
+  FA_TRY(check_scale(scale, true));
+  if (B * H == 0 || M == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  FA_TRY(check_ptr(Q, "Q"));
+  FA_TRY(check_ptr(K, "K"));
+  FA_TRY(check_ptr(V, "V"));
+  FA_TRY(check_ptr(O, "O"));
+  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return fail(FA_ERR_INVALID, "LSE misaligned");
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  cudaError_t e;
+  if (dtype == FA_F32)
+    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, ctx);
+  else
+    e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_fwd: configuration not supported");
+  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "fa_fwd: TMA descriptor rejected by the driver");
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
+  return FA_OK;
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                 void* dQ, void* dK, void* dV, float* delta_ws, int B, int H, int M, int N, int D, float scale,
+                 int causal, fa_dtype dtype, void* stream) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, M, N, D));
+  if (dtype == FA_F32) return fail(FA_ERR_UNSUPPORTED, "fa_bwd supports FA_F16 and FA_BF16");
+  FA_TRY(check_scale(scale, true));
+  if (B * H == 0 || M == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  FA_TRY(check_ptr(Q, "Q"));
+  FA_TRY(check_ptr(K, "K"));
+  FA_TRY(check_ptr(V, "V"));
+  FA_TRY(check_ptr(O, "O"));
+  FA_TRY(check_ptr(dO, "dO"));
+  FA_TRY(check_ptr(LSE, "LSE"));
+  FA_TRY(check_ptr(dQ, "dQ"));
+  FA_TRY(check_ptr(dK, "dK"));
+  FA_TRY(check_ptr(dV, "dV"));
+  FA_TRY(check_ptr(delta_ws, "delta_ws"));
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  cudaError_t e = launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, B * H, M, N, D, scale, causal != 0, dtype, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_bwd: configuration not supported");
+  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "fa_bwd: TMA descriptor rejected by the driver");
+  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
+  return FA_OK;
+}
+
+fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void* O, float* partial_ws, int B, int H,
+                    int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, 1, N, D));
+  FA_TRY(check_scale(scale, false));
+  if (B * H == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  if (n_splits < 1 || n_splits > N || n_splits > 65535)
+    return fail(FA_ERR_INVALID, "n_splits=%d outside [1, min(N=%d, 65535)]", n_splits, N);
+  if (B * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode: B*H=%d above 65535", B * H);
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(Kcache, "Kcache"));
+  FA_TRY(check_ptr(Vcache, "Vcache"));
+  FA_TRY(check_ptr(O, "O"));
+  FA_TRY(check_ptr(partial_ws, "partial_ws"));
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  cudaError_t e = launch_decode(q, Kcache, Vcache, O, partial_ws, B * H, N, D, scale, n_splits, dtype, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode: configuration not supported");
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode launch");
+  return FA_OK;
+}
+
+fa_status fa_last_status(void* stream) {
+  DevState* st = nullptr;
+  FA_TRY(device_state(&st));
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  DevStatus h{};
+  e = cudaMemcpy(&h, st->status, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the status word");
+  if (h.code == 0u) return FA_OK;
+  DevStatus zero{};
+  e = cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
+  static const char* names[] = {"?", "fwd", "fwd_f32", "bwd_delta", "bwd_dkdv", "bwd_dq", "decode_split",
+                                "decode_combine"};
+  const char* kn = h.kernel < 8 ? names[h.kernel] : "?";
+  if (h.code == kStatusTimeout)
+    return fail(FA_ERR_TIMEOUT, "kernel %s gave up wait site %u in block %u", kn, h.site, h.block);
+  return fail(FA_ERR_CUDA, "kernel %s reported status %u (site %u, block %u)", kn, h.code, h.site, h.block);
+}
+
+}  // extern "C"

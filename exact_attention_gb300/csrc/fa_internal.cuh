@@ -1,0 +1,64 @@
+// Declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fa {
+
+// Device-side status word, one per device. A kernel that gives up a bounded
+// wait writes its code here (first writer wins) and exits; fa_last_status()
+// reads and clears it after synchronising.
+struct DevStatus {
+  unsigned int code;    // 0 = ok, kStatusTimeout, ...
+  unsigned int kernel;  // KernelId of the first failing kernel
+  unsigned int site;    // which wait inside that kernel
+  unsigned int block;   // linear block index
+};
+constexpr unsigned int kStatusTimeout = 4u;  // matches FA_ERR_TIMEOUT
+
+enum KernelId : unsigned int {
+  kKernFwd = 1,
+  kKernFwdF32 = 2,
+  kKernBwdDelta = 3,
+  kKernBwdDkDv = 4,
+  kKernBwdDq = 5,
+  kKernDecodeSplit = 6,
+  kKernDecodeCombine = 7,
+};
+
+// Numeric storage types, same values as the C ABI's fa_dtype.
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+inline size_t dtype_size(int dt) { return dt == kF32 ? 4u : 2u; }
+
+// Per-launch context every kernel receives.
+struct LaunchCtx {
+  DevStatus* status;
+  unsigned long long wait_budget_ns;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+// ---- launchers (each returns a cudaError_t from the launch itself)
+cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N, int D,
+                          float scale, int n_splits, int dtype, const LaunchCtx& ctx);
+
+cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
+                            int D, float scale, bool causal, int dtype, const LaunchCtx& ctx);
+
+cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
+                           int D, float scale, bool causal, const LaunchCtx& ctx);
+
+cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                       void* dQ, void* dK, void* dV, float* delta, int BH, int M, int N, int D, float scale,
+                       bool causal, int dtype, const LaunchCtx& ctx);
+
+// Encodes a 3-D TMA tensor map over a contiguous [outer, rows, inner] tensor
+// (inner = head dimension) with a box of [box_inner, box_rows, 1] elements and
+// 128-byte swizzle. Returns false when the driver rejects it.
+bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace fa

@@ -82,13 +82,26 @@ def decode_head_kv(b: int, h: int, N: int, D: int, dtype: str, seed: int = 0):
     return k, v
 
 
+def iter_decode_heads(B: int, H: int, N: int, D: int, dtype: str, seed: int = 0, workers: int = 0):
+    """Yields (b, h, K_bh, V_bh) for every head, drawn on a thread pool (each head
+    has its own generator, so the values do not depend on the number of workers)."""
+    import concurrent.futures as cf
+    import os
+    heads = [(b, h) for b in range(B) for h in range(H)]
+    workers = workers or min(16, os.cpu_count() or 1)
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        futs = [ex.submit(decode_head_kv, b, h, N, D, dtype, seed) for b, h in heads]
+        for (b, h), f in zip(heads, futs):
+            k, v = f.result()
+            yield b, h, k, v
+
+
 def decode_inputs(B: int, H: int, N: int, D: int, dtype: str, seed: int = 0):
     """q [B,H,1,D] and the caches K/V [B,H,N,D], head by head from decode_head_kv."""
     q = decode_query(B, H, D, dtype, seed)
     st = {"f32": np.float32, "f16": np.float16, "bf16": np.uint16}[dtype]
     k = np.empty((B, H, N, D), dtype=st)
     v = np.empty((B, H, N, D), dtype=st)
-    for b in range(B):
-        for h in range(H):
-            k[b, h], v[b, h] = decode_head_kv(b, h, N, D, dtype, seed)
+    for b, h, kh, vh in iter_decode_heads(B, H, N, D, dtype, seed, workers=1 if B * H * N < (1 << 20) else 0):
+        k[b, h], v[b, h] = kh, vh
     return q, k, v

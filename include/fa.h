@@ -1,0 +1,147 @@
+/*
+ * libfa — exact attention on one GB300 GPU (sm_103a), C ABI.
+ *
+ *   O = softmax(scale * Q K^T) V
+ *
+ * computed FlashAttention-2 style: every CTA owns a block of query rows and
+ * walks the keys in blocks, carrying a running row maximum m, denominator l and
+ * unnormalised accumulator, so the score matrix never reaches device memory.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller, dense and
+ *   contiguous, 16-byte aligned. The library allocates no device memory.
+ * - Layout: Q, O, dO, dQ are [B, H, M, D]; K, V, dK, dV are [B, H, N, D]
+ *   (row-major, D fastest). LSE and delta are [B, H, M] float32.
+ * - dtype selects the storage type of Q/K/V/O/dO/dQ/dK/dV: FA_F16, FA_BF16 or
+ *   FA_F32. Softmax state and accumulation are float32 in every case; the f32
+ *   path contracts with three TF32 products (hi*hi + hi*lo + lo*hi).
+ * - D must be 64 or 128 (FA_ERR_UNSUPPORTED otherwise).
+ * - stream is a cudaStream_t (NULL = the legacy default stream). Calls are
+ *   asynchronous: the return value covers argument checks and the launch only.
+ *   Faults detected on the device (a bounded wait that ran out) are reported by
+ *   fa_last_status() after the caller synchronises.
+ * - Errors: FA_ERR_INVALID for bad arguments (null pointer, misaligned pointer,
+ *   non-positive sizes, index overflow); nothing is launched in that case.
+ *   fa_last_error_message() returns a one-line reason for the calling thread.
+ * - B*H == 0 or M == 0 is an empty problem: FA_OK, nothing launched.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_status {
+  FA_OK = 0,
+  FA_ERR_INVALID = 1,     /* bad argument, nothing launched */
+  FA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. D not in {64,128}) */
+  FA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  FA_ERR_TIMEOUT = 4      /* a kernel gave up a bounded wait (see fa_last_status) */
+} fa_status;
+
+typedef enum fa_dtype { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
+
+/*
+ * Forward pass (prefill).
+ *
+ * Follows "Flash attention, f32" (Phobos examples: the online-softmax loop
+ * over key blocks, "After the loop" normalisation) and "06: Fused attention"
+ * (attn_fwd: causal rule, stored log-sum-exp L = m + log l).
+ *
+ *   Q [B,H,M,D], K [B,H,N,D], V [B,H,N,D]  inputs, dtype
+ *   O [B,H,M,D]                            output, dtype (round to nearest even)
+ *   LSE [B,H,M] float32                    output, natural log of the row sum of
+ *                                          exp(scale*q.k); may be NULL
+ *   scale                                  multiplies Q K^T before the softmax;
+ *                                          must be finite and > 0
+ *   causal                                 nonzero: key j is visible to query i
+ *                                          iff j <= i (top-left aligned)
+ * M, N >= 1 (N == 0 is FA_ERR_INVALID). Any M, N: ragged tails are masked.
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int M, int N,
+                 int D, float scale, int causal, fa_dtype dtype, void* stream);
+
+/*
+ * Backward pass: gradients of sum(dO o O).
+ *
+ * Follows "06: Fused attention" (attn_bwd_delta, attn_bwd_dkdv, attn_bwd_dq)
+ * and the identity D_i = rowsum(dO o O), dS = P o (dP - D) from the "Flash
+ * Attention" notes ("IO complexity"). Three launches on `stream`: delta, then
+ * dK/dV (one CTA per key block walking the query blocks), then dQ (one CTA per
+ * query block walking the key blocks).
+ *
+ *   Q, K, V, O, dO   inputs (O from fa_fwd with the same arguments)
+ *   LSE              input, [B,H,M] float32 written by fa_fwd
+ *   dQ [B,H,M,D], dK [B,H,N,D], dV [B,H,N,D]   outputs, dtype
+ *   delta_ws         caller-owned scratch of fa_bwd_workspace_bytes(B,H,M)
+ *                    bytes; holds rowsum(dO o O) (float32 [B,H,M]) on return
+ * dtype must be FA_F16 or FA_BF16 (FA_ERR_UNSUPPORTED for FA_F32); scale as
+ * for fa_fwd (finite, > 0).
+ */
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                 void* dQ, void* dK, void* dV, float* delta_ws, int B, int H, int M, int N, int D, float scale,
+                 int causal, fa_dtype dtype, void* stream);
+
+/* Bytes of scratch fa_bwd needs: B*H*M float32. */
+size_t fa_bwd_workspace_bytes(int B, int H, int M);
+
+/*
+ * Decode (flash decoding): one query row per (batch, head) against a KV cache.
+ *
+ * Follows "Flash decoding" (linear algebra for programmers, part 4),
+ * "Overview of the algorithm": the keys are cut into n_splits chunks of
+ * ceil(N / n_splits) keys; each chunk s writes an UNNORMALISED partial
+ *   m_s = max_j x_j,  l_s = sum_j e^{x_j - m_s},  O_s = sum_j e^{x_j - m_s} V_j
+ * (x_j = scale * q . K_j, natural-log units), and a combine kernel merges them
+ * with one global 1/l_g.
+ *
+ *   q [B,H,1,D]                    input, dtype
+ *   Kcache, Vcache [B,H,N,D]       input, dtype
+ *   O [B,H,1,D]                    output, dtype
+ *   partial_ws                     caller-owned scratch of
+ *                                  fa_decode_workspace_bytes(B,H,D,n_splits)
+ *                                  bytes; on return it holds, float32,
+ *                                  O_s [B*H][n_splits][D], then m_s
+ *                                  [B*H][n_splits], then l_s [B*H][n_splits]
+ *                                  (an empty split has m_s = -inf, l_s = 0)
+ *   scale                          any finite value
+ *   n_splits                       1 <= n_splits <= min(N, 65535); B*H <= 65535
+ */
+fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void* O, float* partial_ws, int B,
+                    int H, int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream);
+
+/* Bytes of scratch fa_decode needs: B*H*n_splits*(D+2) float32. */
+size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status
+ * word. FA_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call
+ * (fa_last_error_message() names the kernel and the wait), FA_ERR_CUDA if the
+ * synchronisation itself failed, FA_OK otherwise. The status word is shared by
+ * all streams of a device.
+ */
+fa_status fa_last_status(void* stream);
+
+/* Static string for a status code. */
+const char* fa_status_string(fa_status s);
+
+/* One-line description of the last error on the calling host thread. */
+const char* fa_last_error_message(void);
+
+/*
+ * Bound, in nanoseconds, on every wait inside the kernels launched by this
+ * library after the call (default 2e9, i.e. 2 s; the environment variable
+ * FA_WAIT_BUDGET_NS overrides the default at first use). Values < 1000 are
+ * FA_ERR_INVALID.
+ */
+fa_status fa_set_wait_budget_ns(unsigned long long ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

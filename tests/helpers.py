@@ -1,0 +1,47 @@
+"""Test helpers: moving synth arrays to the GPU and comparing results with the oracle."""
+from __future__ import annotations
+
+import numpy as np
+
+from exact_attention_gb300 import synth
+
+TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
+
+# Tolerances stated for this method: max |GPU - oracle| on O, on the gradients and on LSE.
+TOL_O = {"f32": 1e-4, "f16": 2e-3, "bf16": 1e-2}
+TOL_GRAD = {"f16": 1e-2, "bf16": 5e-2}
+TOL_LSE = 1e-4
+REL_L2_F32 = 1e-5
+
+
+def to_device(a: np.ndarray, dtype: str):
+    import torch
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(a))
+    return t.cuda()
+
+
+def to_f64(t) -> np.ndarray:
+    import torch
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def errs(got: np.ndarray, ref: np.ndarray):
+    d = np.abs(got - ref)
+    rel_l2 = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+    return float(d.max()) if d.size else 0.0, rel_l2
+
+
+def assert_close(got, ref, atol: float, what: str, rel_l2: float | None = None):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    mx, rl = errs(got, ref)
+    assert mx <= atol, f"{what}: max abs err {mx:.3e} > {atol:.1e} (rel L2 {rl:.3e})"
+    if rel_l2 is not None:
+        assert rl <= rel_l2, f"{what}: rel L2 {rl:.3e} > {rel_l2:.1e} (max abs {mx:.3e})"
+    return mx, rl
+
+
+def f64(a, dtype):
+    return synth.to_f64(a, dtype)
