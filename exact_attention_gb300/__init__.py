@@ -20,6 +20,7 @@ from ._binding import (  # noqa: F401
     fa_bwd,
     fa_bwd_workspace_bytes,
     fa_decode,
+    fa_decode_static,
     fa_decode_workspace_bytes,
     fa_fwd,
     fa_last_error_message,

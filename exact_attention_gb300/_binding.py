@@ -28,6 +28,7 @@ EXPORTS = (
     "fa_bwd_workspace_bytes",
     "fa_decode",
     "fa_decode_workspace_bytes",
+    "fa_decode_static",
     "fa_last_status",
     "fa_status_string",
     "fa_last_error_message",
@@ -61,6 +62,8 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd.restype = st
     L.fa_decode.argtypes = [vp] * 5 + [i, i, i, i, f, i, i, vp]
     L.fa_decode.restype = st
+    L.fa_decode_static.argtypes = [vp] * 4 + [i, i, i, i, f, i, i, vp]
+    L.fa_decode_static.restype = st
     L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_decode_workspace_bytes.restype = ctypes.c_size_t
     L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
@@ -108,6 +111,12 @@ def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, B, H, M, N, D, scale, caus
 def fa_decode(q, Kcache, Vcache, O, partial_ws, B, H, N, D, scale, n_splits, dtype, stream=None) -> int:
     return lib().fa_decode(_ptr(q), _ptr(Kcache), _ptr(Vcache), _ptr(O), _ptr(partial_ws), B, H, N, D,
                            float(scale), int(n_splits), int(dtype), _stream(stream))
+
+
+def fa_decode_static(q, Kcache, Vcache, O, B, H, N, D, scale, n_splits, dtype, stream=None) -> int:
+    """Decode with the library's own fixed scratch (no workspace, no allocation); see include/fa.h."""
+    return lib().fa_decode_static(_ptr(q), _ptr(Kcache), _ptr(Vcache), _ptr(O), B, H, N, D, float(scale),
+                                  int(n_splits), int(dtype), _stream(stream))
 
 
 def fa_decode_workspace_bytes(B, H, D, n_splits) -> int:

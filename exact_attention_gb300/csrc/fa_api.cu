@@ -281,6 +281,80 @@ fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void*
   return FA_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode with scratch that the library owns.
+//
+// Some callers cannot allocate device memory when they need to decode: code
+// that runs under a caching or arena allocator that must not grow, a runtime
+// that accounts for every buffer itself, or a C caller that has no allocator
+// of its own at that point. fa_decode_static serves them: the split partials
+// live in g_decode_scratch, a fixed array in the library's device image that
+// every GPU loading the library holds until the process exits.
+namespace fa {
+namespace {
+
+constexpr size_t kStaticScratchFloats = static_cast<size_t>(4) << 20;  // 16 MiB of float32
+
+static __device__ __align__(256) float g_decode_scratch[kStaticScratchFloats];
+
+float* g_static_ptr[kMaxDevices] = {};
+
+// Once per device, with that device current: the device address of the array.
+// In host code the array's name only stands for it; the kernels must be given
+// this address instead.
+fa_status static_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
+    g_static_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_decode_static(const void* q, const void* Kcache, const void* Vcache, void* O, int B, int H, int N, int D,
+                           float scale, int n_splits, fa_dtype dtype, void* stream) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, 1, N, D));
+  FA_TRY(check_scale(scale, false));
+  if (B * H == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  if (n_splits < 1 || n_splits > N || n_splits > 65535)
+    return fail(FA_ERR_INVALID, "n_splits=%d outside [1, min(N=%d, 65535)]", n_splits, N);
+  if (B * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_static: B*H=%d above 65535", B * H);
+  const size_t need = static_cast<size_t>(B) * H * n_splits * (D + 2);
+  if (need > kStaticScratchFloats)
+    return fail(FA_ERR_INVALID,
+                "fa_decode_static: B*H*n_splits*(D+2) = %zu floats exceeds the library's fixed scratch of %zu "
+                "floats (16 MiB); use fewer splits or fa_decode with a caller workspace",
+                need, kStaticScratchFloats);
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(Kcache, "Kcache"));
+  FA_TRY(check_ptr(Vcache, "Vcache"));
+  FA_TRY(check_ptr(O, "O"));
+  float* ws = nullptr;
+  FA_TRY(static_scratch(&ws));
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  cudaError_t e = launch_decode(q, Kcache, Vcache, O, ws, B * H, N, D, scale, n_splits, dtype, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode_static: configuration not supported");
+  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_static launch");
+  return FA_OK;
+}
+
 fa_status fa_last_status(void* stream) {
   DevState* st = nullptr;
   FA_TRY(device_state(&st));

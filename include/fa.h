@@ -118,6 +118,31 @@ fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void*
 size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits);
 
 /*
+ * Decode that allocates nothing and needs no workspace argument.
+ *
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when they decode (a caching or arena allocator
+ * that must not grow, a runtime that accounts for every buffer itself, a C
+ * caller without an allocator at hand). Same arguments, layouts and result as
+ * fa_decode, minus partial_ws: the split partials go to a fixed 16 MiB float32
+ * array inside the library's device image, which every GPU that loads the
+ * library holds until the process exits.
+ *
+ * - Limit: B*H*n_splits*(D+2) <= 4,194,304 floats (e.g. B=8, H=32, D=128 with
+ *   up to 126 splits); larger requests return FA_ERR_INVALID, naming the limit,
+ *   and launch nothing.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture on the device.
+ * - Calls, cudaMalloc and cudaFree: none. The array is shared by every call on
+ *   a device and keeps the last call's partials. Nothing in it needs to start
+ *   at zero (each call writes every partial it reads), but calls that overlap
+ *   on the GPU (e.g. on two streams at once) race on it: serialise them.
+ */
+fa_status fa_decode_static(const void* q, const void* Kcache, const void* Vcache, void* O, int B, int H, int N,
+                           int D, float scale, int n_splits, fa_dtype dtype, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's status
  * word. FA_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call
  * (fa_last_error_message() names the kernel and the wait), FA_ERR_CUDA if the
