@@ -9,21 +9,34 @@
 //
 // GB300 layout of the work:
 //  * a CTA owns a pair of 128-row query tiles of one (batch, head) and runs
-//    persistently over such pairs (heaviest causal pairs first);
+//    persistently over such pairs (non-causal: the pairs of a head are adjacent
+//    so resident CTAs share that head's K/V in L2; causal: heaviest pairs first);
 //  * warp 8 issues TMA loads: both Q tiles once per pair, then K and V blocks
 //    of 128 keys into a ring of shared-memory stages (128-byte swizzle);
 //  * warp 9 (one thread) issues the MMAs: S_t = Q_t K^T into tensor memory,
 //    O_t += P_t V with P_t read from tensor memory;
 //  * warps 0-3 and 4-7 are the softmax of tile 0 and tile 1: each thread owns
-//    one query row (one TMEM lane), reads its 128 scores, updates (m, l),
-//    writes P as packed halves over the scores and, at the end of the pair,
-//    normalises O and stores O and LSE. The two tiles ping-pong so one tile's
-//    softmax overlaps the other tile's MMAs;
-//  * the accumulator is rescaled only when a row maximum grows by more than
-//    2^8 (in base-2 units); otherwise the stale maximum is kept, which leaves
-//    the result exact because O and l share it.
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D),
-// O1 [256+D, 256+2D).
+//    one query row (one TMEM lane). The two tiles ping-pong so one tile's
+//    softmax overlaps the other tile's MMAs.
+//
+// Softmax of one key block, per row. The running maximum is kept stale unless
+// the block's maximum exceeds it by more than 2^8 (base-2 units), the FA4
+// conditional rescale; O and l share the stale maximum so the result is exact.
+// Speculative single pass: the scores are read once, P = 2^(s*c - m) is formed
+// against the current maximum while the block maximum is tracked; only when
+// that maximum breaks the threshold (always on the first block) are the scores
+// read again with the new maximum and O rescaled in tensor memory. P stays in
+// registers until the decision, then is written as packed halves over the
+// scores' first 64 columns.
+//
+// O is divided by the sum of the half-rounded weights that multiplied V, so it
+// is a weighted mean of V rows; LSE uses the exact f32 sum. For D = 64 the
+// rounded sum comes from the MMA itself: V is extended by 16 columns of ones
+// (a constant shared-memory chunk), so O_t has 80 columns and column 64 holds
+// sum(P). For D = 128 tensor memory is full and the sum is formed in registers.
+//
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DO),
+// O1 [384,384+DO), DO = 80 (D = 64) or 128.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -37,7 +50,7 @@ constexpr int kBM = 128;        // query rows per tile
 constexpr int kBN = 128;        // keys per block
 constexpr int kChunk = 16384;   // one 128-row x 128-byte swizzled chunk
 // 10 warps: three share one SM sub-partition (16K registers), so a thread has
-// at most 168 registers; the softmax reads its scores in two passes to fit.
+// at most 168 registers.
 constexpr int kThreads = 320;   // 8 softmax warps + producer + MMA
 constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
@@ -51,7 +64,10 @@ struct FwdCfg {
   static constexpr int kTileBytes = kDC * kChunk;          // one Q tile / K block / V block
   static constexpr int kStages = D == 64 ? 4 : 2;          // K/V ring depth
   static constexpr int kQBuf = D == 64 ? 2 : 1;            // Q pair buffers
-  static constexpr int kSmemData = kQBuf * 2 * kTileBytes + kStages * 2 * kTileBytes;
+  static constexpr bool kOnesSum = D == 64;                // row sum from a ones block of V
+  static constexpr int kDO = kOnesSum ? D + 16 : D;        // O columns in tensor memory
+  static constexpr int kOnesOff = kQBuf * 2 * kTileBytes + kStages * 2 * kTileBytes;
+  static constexpr int kSmemData = kOnesOff + (kOnesSum ? kChunk : 0);
   static constexpr int kSmemBytes = 1024 + 1024 + kSmemData;  // header + alignment slack + data
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -72,9 +88,15 @@ struct TileInfo {
 template <bool CAUSAL>
 __device__ __forceinline__ TileInfo tile_info(int tile, int BH, int num_pairs, int nkb) {
   TileInfo ti;
-  const int pr = tile / BH;
-  ti.bh = tile - pr * BH;
-  const int pair = CAUSAL ? (num_pairs - 1 - pr) : pr;
+  int pair;
+  if (CAUSAL) {  // heads fastest, heaviest (last) pairs first
+    const int pr = tile / BH;
+    ti.bh = tile - pr * BH;
+    pair = num_pairs - 1 - pr;
+  } else {       // pairs of one head adjacent
+    ti.bh = tile / num_pairs;
+    pair = tile - ti.bh * num_pairs;
+  }
   ti.q0 = pair * 2 * kBM;
   if (CAUSAL) {
     ti.nb0 = min(nkb, ti.q0 / kBN + 1);
@@ -84,6 +106,61 @@ __device__ __forceinline__ TileInfo tile_info(int tile, int BH, int num_pairs, i
     ti.nb1 = nkb;
   }
   return ti;
+}
+
+// ---------------------------------------------------------------- softmax math
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ua, ub, uc, ud;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(ud) : "l"(ua), "l"(ub), "l"(uc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t ua, ub, ud;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+  asm("add.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Scores of keys past N, or past the query when causal, become -inf.
+template <bool CAUSAL>
+__device__ __forceinline__ void mask32(uint32_t* r, int key0, int N, int row) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int key = key0 + i;
+    if (key >= N || (CAUSAL && key > row)) r[i] = __float_as_uint(-INFINITY);
+  }
+}
+
+// P for 32 scores against the current maximum: packed halves into pk[16],
+// exact sum into se, rounded sum into sr (only when ROUNDED), and the raw
+// maximum into mx.
+template <bool BF16, bool ROUNDED>
+__device__ __forceinline__ void p_chunk(const uint32_t* r, float sl2, float neg_m, float& mx, float2& se, float2& sr,
+                                        uint32_t* pk) {
+  const float2 c2 = make_float2(sl2, sl2), m2 = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float2 s = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+    mx = fmax3(mx, s.x, s.y);
+    const float2 x = ffma2(s, c2, m2);
+    const float a = ptx::ex2(x.x), b = ptx::ex2(x.y);
+    se = fadd2(se, make_float2(a, b));
+    pk[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+    if (ROUNDED) sr = fadd2(sr, BF16 ? ptx::unpack_bf16x2(pk[i]) : ptx::unpack_f16x2(pk[i]));
+  }
 }
 
 template <int D, bool BF16, bool CAUSAL>
@@ -96,10 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   FwdHdr* hdr = reinterpret_cast<FwdHdr*>(smem_raw);
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
   const uint32_t data_u32 = (raw_u32 + 1024u + 1023u) & ~1023u;  // 1024-aligned for the swizzle atoms
-  // data layout: Q[qbuf][tile] then stages: K[stage], V[stage]
+  // data layout: Q[qbuf][tile], then stages (K, V), then the ones chunk (D = 64)
   auto q_addr = [&](int qb, int t) { return data_u32 + (qb * 2 + t) * C::kTileBytes; };
   auto k_addr = [&](int st) { return data_u32 + C::kQBuf * 2 * C::kTileBytes + st * 2 * C::kTileBytes; };
   auto v_addr = [&](int st) { return k_addr(st) + C::kTileBytes; };
+  const uint32_t ones_addr = data_u32 + C::kOnesOff;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -124,6 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     hdr->abort_flag = 0;
     ptx::fence_mbar_init();
   }
+  if (C::kOnesSum) {  // 16 KB of ones: the extra B columns whose products sum P
+    const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
+    uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (ones_addr - raw_u32));
+    for (int i = threadIdx.x; i < kChunk / 4; i += kThreads) ones[i] = one2;
+    ptx::fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
+  }
   if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
     ptx::tmem_relinquish();
@@ -138,6 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernFwd};
+
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -179,90 +264,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
+    // Lane 0 alone runs this role. One issuer serves both tiles in the order
+    // PV_{0,j-1}, QK_{0,j}, PV_{1,j-1}, QK_{1,j}: a tcgen05.mma issue blocks while the
+    // tensor pipe is busy, so each tile's group runs back to back (measured faster
+    // than one issuer per tile, whose MMAs interleave in the pipe, and than a
+    // warp-wide loop).
+    constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
+    constexpr uint32_t idesc_qk = ptx::idesc_f32acc(kBM, kBN, fmt, fmt, false, false);
+    constexpr uint32_t idesc_pv = ptx::idesc_f32acc(kBM, C::kDO, fmt, fmt, false, true);
     if (lane == 0) {
-      constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-      constexpr uint32_t idesc_qk = ptx::idesc_f32acc(kBM, kBN, fmt, fmt, false, false);
-      constexpr uint32_t idesc_pv = ptx::idesc_f32acc(kBM, D, fmt, fmt, false, true);
       uint32_t kv_it = 0;
       uint32_t p_ph[2] = {0u, 0u};
       int it = 0;
       bool ok = true;
-      auto issue_qk = [&](int t, int qb, int st) {
+      // descriptor of a byte offset from a descriptor: the start address field is addr >> 4
+      auto qk = [&](int t, int qb, int st) {
+        const uint64_t a0 = ptx::sdesc_sw128(q_addr(qb, t), 16, 1024);
+        const uint64_t b0 = ptx::sdesc_sw128(k_addr(st), 16, 1024);
         const uint32_t d = tmem + t * kBN;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kChunk + (ks & 3) * 32;
-          const uint64_t a = ptx::sdesc_sw128(q_addr(qb, t) + off, 16, 1024);
-          const uint64_t b = ptx::sdesc_sw128(k_addr(st) + off, 16, 1024);
-          ptx::mma_f16_ss(d, a, b, idesc_qk, ks > 0 ? 1u : 0u);
+          const uint64_t off = static_cast<uint64_t>(((ks >> 2) * kChunk + (ks & 3) * 32) >> 4);
+          ptx::mma_f16_ss(d, a0 + off, b0 + off, idesc_qk, ks > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int st, bool accumulate) {
-        const uint32_t d = tmem + 2 * kBN + t * D;
+      auto pv = [&](int t, int st, bool accumulate) {
+        // the second 64-column group of B is the next V chunk (D = 128) or the ones chunk (D = 64)
+        const uint32_t lbo = C::kOnesSum ? ones_addr - v_addr(st) : kChunk;
+        const uint64_t b0 = ptx::sdesc_sw128(v_addr(st), lbo, 1024);
+        const uint32_t d = tmem + 2 * kBN + t * 128;
         const uint32_t p = tmem + t * kBN;
 #pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint64_t b = ptx::sdesc_sw128(v_addr(st) + ks * 2048, kChunk, 1024);
-          ptx::mma_f16_ts(d, p + ks * 8, b, idesc_pv, (accumulate || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kBN / 16; ++ks)
+          ptx::mma_f16_ts(d, p + ks * 8, b0 + static_cast<uint64_t>((ks * 2048) >> 4), idesc_pv,
+                          (accumulate || ks > 0) ? 1u : 0u);
+      };
+      auto commit = [&](unsigned long long* bar) { ptx::tc_commit(ptx::smem_u32(bar)); };
+      auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+        return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
       };
       for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
         const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
         const int qb = it % C::kQBuf;
         const uint32_t qph = static_cast<uint32_t>(it / C::kQBuf) & 1u;
-        if (!ptx::mbar_wait(ptx::smem_u32(&hdr->q_full[qb]), qph, wc, 20)) break;
+        if (!wait(&hdr->q_full[qb], qph, 20)) break;
         ptx::tc_fence_after();
         const int nb = ti.nb1;
         for (int j = 0; j <= nb && ok; ++j) {
           const uint32_t cur = kv_it + j, prev = kv_it + j - 1;
           const int st = cur % C::kStages, pst = prev % C::kStages;
           if (j < nb) {
-            ok = ptx::mbar_wait(ptx::smem_u32(&hdr->k_full[st]), (cur / C::kStages) & 1u, wc, 21);
+            ok = wait(&hdr->k_full[st], (cur / C::kStages) & 1u, 21);
             if (!ok) break;
             ptx::tc_fence_after();
           }
           if (j >= 1 && j - 1 < ti.nb0) {
-            ok = ptx::mbar_wait(ptx::smem_u32(&hdr->p_full[0]), p_ph[0], wc, 22) &&
-                 ptx::mbar_wait(ptx::smem_u32(&hdr->v_full[pst]), (prev / C::kStages) & 1u, wc, 23);
+            ok = wait(&hdr->p_full[0], p_ph[0], 22) && wait(&hdr->v_full[pst], (prev / C::kStages) & 1u, 23);
             if (!ok) break;
             p_ph[0] ^= 1u;
             ptx::tc_fence_after();
-            issue_pv(0, pst, j - 1 > 0);
-            if (j - 1 == ti.nb0 - 1) ptx::tc_commit(ptx::smem_u32(&hdr->o_full[0]));
+            pv(0, pst, j - 1 > 0);
+            if (j - 1 == ti.nb0 - 1) commit(&hdr->o_full[0]);
           }
           if (j < ti.nb0) {
-            issue_qk(0, qb, st);
-            ptx::tc_commit(ptx::smem_u32(&hdr->s_full[0]));
+            qk(0, qb, st);
+            commit(&hdr->s_full[0]);
           }
           if (j >= 1) {
-            ok = ptx::mbar_wait(ptx::smem_u32(&hdr->p_full[1]), p_ph[1], wc, 24) &&
-                 ptx::mbar_wait(ptx::smem_u32(&hdr->v_full[pst]), (prev / C::kStages) & 1u, wc, 25);
+            ok = wait(&hdr->p_full[1], p_ph[1], 24) && wait(&hdr->v_full[pst], (prev / C::kStages) & 1u, 25);
             if (!ok) break;
             p_ph[1] ^= 1u;
             ptx::tc_fence_after();
-            issue_pv(1, pst, j - 1 > 0);
-            if (j - 1 == nb - 1) ptx::tc_commit(ptx::smem_u32(&hdr->o_full[1]));
-            ptx::tc_commit(ptx::smem_u32(&hdr->kv_empty[pst]));
+            pv(1, pst, j - 1 > 0);
+            if (j - 1 == nb - 1) commit(&hdr->o_full[1]);
+            commit(&hdr->kv_empty[pst]);
           }
           if (j < nb) {
-            issue_qk(1, qb, st);
-            ptx::tc_commit(ptx::smem_u32(&hdr->s_full[1]));
-            if (j == nb - 1) ptx::tc_commit(ptx::smem_u32(&hdr->q_empty[qb]));
+            qk(1, qb, st);
+            commit(&hdr->s_full[1]);
+            if (j == nb - 1) commit(&hdr->q_empty[qb]);
           }
         }
         kv_it += nb;
       }
-      // every MMA issued by this thread has completed once mma_done flips
-      ptx::tc_commit(ptx::smem_u32(&hdr->mma_done));
+      // every MMA issued by lane 0 has completed once mma_done flips
+      commit(&hdr->mma_done);
       ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
+    constexpr bool kRounded = !C::kOnesSum;  // rounded row sum formed in registers
     const int t = warp >> 2;          // which tile of the pair
     const int wq = warp & 3;          // TMEM lane quarter
     const uint32_t lane_sel = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_sel + t * kBN;
-    const uint32_t tO = tmem + lane_sel + 2 * kBN + t * D;
+    const uint32_t tO = tmem + lane_sel + 2 * kBN + t * 128;
     const uint32_t s_full = ptx::smem_u32(&hdr->s_full[t]);
     const uint32_t p_full = ptx::smem_u32(&hdr->p_full[t]);
     const uint32_t o_full = ptx::smem_u32(&hdr->o_full[t]);
@@ -273,8 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbt = t == 0 ? ti.nb0 : ti.nb1;
       const int row = ti.q0 + t * kBM + wq * 32 + lane;  // query index within the head
       float m2 = -INFINITY;  // running max of scale*log2(e)*s (possibly stale by < 2^8)
-      float l = 0.f;   // sum of the half-rounded weights fed to the MMA (normalises O)
-      float le = 0.f;  // sum of the exact f32 weights (gives LSE)
+      float l = 0.f;         // sum of the half-rounded weights (D = 128 only; D = 64 reads it from O)
+      float le = 0.f;        // sum of the exact f32 weights (gives LSE)
       for (int j = 0; j < nbt; ++j) {
         ok = ptx::mbar_wait(s_full, s_ph, wc, 30);
         __syncwarp();  // lanes may leave the poll at different times; reconverge for .aligned ops
@@ -283,41 +379,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tc_fence_after();
         const int kbase = j * kBN;
         const bool edge = (kbase + kBN > N) || (CAUSAL && kbase + kBN - 1 > ti.q0 + t * kBM);
-        // masked scores (keys past N, or past the query when causal) become -inf
-        auto mask = [&](uint32_t* r, int c0) {
-          if (edge) {
+
+        // -- speculative single pass against the current maximum
+        bool slow = (j == 0);
+        uint32_t pk[kBN / 2];
+        float2 se = make_float2(0.f, 0.f), sr = make_float2(0.f, 0.f);
+        if (!slow) {
+          float mx = -INFINITY;
+          const float neg_m = -m2;
+          uint32_t r[2][32];
+          ptx::tmem_ld32(tS, r[0]);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int key = kbase + c0 + i;
-              if (key >= N || (CAUSAL && key > row)) r[i] = __float_as_uint(-INFINITY);
+          for (int c = 0; c < 4; ++c) {
+            ptx::tmem_wait_ld32(r[c & 1]);
+            if (c < 3) ptx::tmem_ld32(tS + 32 * (c + 1), r[(c + 1) & 1]);
+            if (edge) mask32<CAUSAL>(r[c & 1], kbase + 32 * c, N, row);
+            p_chunk<BF16, kRounded>(r[c & 1], scale_log2, neg_m, mx, se, sr, pk + 16 * c);
+          }
+          slow = __any_sync(0xFFFFFFFFu, mx * scale_log2 > m2 + kRescaleThreshold);
+        }
+        if (slow) {
+          // -- block maximum first, then rescale O if the maximum moved, then P
+          float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBN; c += 32) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tS + c, r);
+            ptx::tmem_wait_ld32(r);
+            if (edge) mask32<CAUSAL>(r, kbase + c, N, row);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              mx0 = fmaxf(mx0, __uint_as_float(r[i]));
+              mx1 = fmaxf(mx1, __uint_as_float(r[i + 1]));
             }
           }
-        };
-        // pass 1: row maximum of the raw scores
-        float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBN; c += 32) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tS + c, r);
-          ptx::tmem_wait_ld32(r);
-          mask(r, c);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            mx0 = fmaxf(mx0, __uint_as_float(r[i]));
-            mx1 = fmaxf(mx1, __uint_as_float(r[i + 1]));
-          }
-        }
-        const float mb2 = fmaxf(mx0, mx1) * scale_log2;
-        const bool need = mb2 > m2 + kRescaleThreshold;
-        if (__any_sync(0xFFFFFFFFu, need)) {
-          const float m_new = fmaxf(m2, mb2);
+          const float m_new = fmaxf(m2, fmaxf(mx0, mx1) * scale_log2);
           const float corr = m_new == -INFINITY ? 1.f : ptx::ex2(m2 - m_new);
           l *= corr;
           le *= corr;
           if (j > 0) {  // O holds earlier blocks: rescale it (the previous PV has completed)
             uint32_t o[16];
 #pragma unroll
-            for (int c = 0; c < D; c += 16) {
+            for (int c = 0; c < C::kDO; c += 16) {
               ptx::tmem_ld16(tO + c, o);
               ptx::tmem_wait_ld16(o);
 #pragma unroll
@@ -326,39 +429,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           m2 = m_new;
-        }
-        // pass 2: P = 2^(s*scale*log2e - m), packed to halves over the first 64 columns.
-        // Half h reads score columns [64h, 64h+64) and writes P columns [32h, 32h+32),
-        // which were read before.
-        const float neg_m = m2 == -INFINITY ? 0.f : -m2;
-        float ps0 = 0.f, ps1 = 0.f, pe0 = 0.f, pe1 = 0.f;
+          const float neg_m = m2 == -INFINITY ? 0.f : -m2;
+          float mx_unused = -INFINITY;
+          se = make_float2(0.f, 0.f);
+          sr = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t r[64];
-          ptx::tmem_ld32(tS + 64 * h, r);
-          ptx::tmem_ld32(tS + 64 * h + 32, r + 32);
-          ptx::tmem_wait_ld32(r);
-          ptx::tmem_wait_ld32(r + 32);
-          mask(r, 64 * h);
-          mask(r + 32, 64 * h + 32);
-          uint32_t pk[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float a = ptx::ex2(fmaf(__uint_as_float(r[2 * i]), scale_log2, neg_m));
-            const float b = ptx::ex2(fmaf(__uint_as_float(r[2 * i + 1]), scale_log2, neg_m));
-            pe0 += a;
-            pe1 += b;
-            pk[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
-            // l sums the rounded weights the MMA multiplies V by, so O = sum(p V) / sum(p)
-            // is a weighted mean; with a dominant key its rounding error then cancels.
-            const float2 pr = BF16 ? ptx::unpack_bf16x2(pk[i]) : ptx::unpack_f16x2(pk[i]);
-            ps0 += pr.x;
-            ps1 += pr.y;
+          for (int c = 0; c < kBN; c += 32) {
+            uint32_t r[32];
+            ptx::tmem_ld32(tS + c, r);
+            ptx::tmem_wait_ld32(r);
+            if (edge) mask32<CAUSAL>(r, kbase + c, N, row);
+            p_chunk<BF16, kRounded>(r, scale_log2, neg_m, mx_unused, se, sr, pk + c / 2);
           }
-          ptx::tmem_st32(tS + 32 * h, pk);
         }
-        l += ps0 + ps1;
-        le += pe0 + pe1;
+        le += se.x + se.y;
+        if (kRounded) l += sr.x + sr.y;
+        // P over the scores' first 64 columns (all scores have been read)
+        ptx::tmem_st32(tS + 0, pk);
+        ptx::tmem_st32(tS + 32, pk + 32);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
@@ -371,6 +459,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       o_ph ^= 1u;
       ptx::tc_fence_after();
+      if (C::kOnesSum) {  // column D of O holds sum(P) accumulated by the MMA
+        uint32_t s1[16];
+        ptx::tmem_ld16(tO + D, s1);
+        ptx::tmem_wait_ld16(s1);
+        l = __uint_as_float(s1[0]);
+      }
       const float inv = 1.f / l;
       const bool valid = row < M;
       const size_t orow = (static_cast<size_t>(ti.bh) * M + (valid ? row : 0)) * D;

@@ -53,11 +53,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+
 // Every wait in this library is bounded: it gives up after `budget_ns` of
 // globaltimer time or a fixed number of polls, whichever comes first, or as
 // soon as another role of the CTA has raised the shared abort flag. On a
 // time-out it records (kernel, site) in the device status word and raises the
 // abort flag so that the rest of the CTA drains and exits.
+//
+// Waits use try_wait, which lets the SM suspend the polling thread: a hot
+// test_wait spin (or a nanosleep back-off) takes issue slots from the warps
+// sharing the SM sub-partition and measured slower in the forward kernel.
 struct WaitCtx {
   volatile int* abort_flag;  // shared memory, one per CTA
   DevStatus* status;         // global memory, one per device
@@ -79,8 +95,10 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
   constexpr uint32_t kMaxPolls = 1u << 28;
   for (uint32_t it = 0; it < kMaxPolls; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*w.abort_flag) return false;
-    if ((it & 31u) == 0u && globaltimer_ns() - t0 > w.budget_ns) break;
+    if ((it & 15u) == 0u) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.budget_ns) break;
+    }
   }
   raise_error(w, kStatusTimeout, site);
   return false;
@@ -261,6 +279,19 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 #undef FA_R8
 #undef FA_W8
 #undef FA_M8
+
+// Named barrier over `count` threads with an OR-reduction of `pred`: every
+// participant gets the same answer, so a group can agree to stop together.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "barrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0u;
+}
 
 // ------------------------------------------------------------ scalar math
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32).
