@@ -1,0 +1,79 @@
+"""Backward pass on the GPU against the fp64 oracle: dQ, dK, dV and the delta workspace."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import exact_attention_gb300 as fa
+from exact_attention_gb300 import synth
+
+from helpers import TOL_GRAD, assert_close, f64, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def run_bwd(B, H, M, N, D, dtype, causal, scale, seed=0, std=1.0):
+    q, k, v, do = synth.attention_inputs(B, H, M, N, D, dtype, seed=seed, std=std, with_dout=True)
+    qd, kd, vd, dod = (to_device(x, dtype) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, scale, causal)
+    dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    return (q, k, v, do), to_f64(o), (to_f64(dq), to_f64(dk), to_f64(dv)), to_f64(delta)
+
+
+def check(inputs, o_gpu, grads, delta, dtype, causal, scale, heads=None):
+    q, k, v, do = inputs
+    B, H = q.shape[:2]
+    heads = heads or [(b, h) for b in range(B) for h in range(H)]
+    worst = [0.0, 0.0, 0.0]
+    for b, h in heads:
+        ref = oracle.backward(f64(q[b, h], dtype), f64(k[b, h], dtype), f64(v[b, h], dtype), f64(do[b, h], dtype),
+                              scale, causal)
+        for n, (g, r) in enumerate(zip(grads, ref)):
+            mx, _ = assert_close(g[b, h], r, TOL_GRAD[dtype], f"{'dQ dK dV'.split()[n]}[{b},{h}] {dtype} "
+                                 f"causal={causal}")
+            worst[n] = max(worst[n], mx)
+        # delta is rowsum(dO o O) of the stored O (the tutorial's delta kernel)
+        dref = oracle.delta(o_gpu[b, h], f64(do[b, h], dtype))
+        assert_close(delta[b, h], dref, 1e-4 * max(1.0, float(np.max(np.abs(dref)))), f"delta[{b},{h}]")
+    return worst
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("std", [1.0, 0.5])
+def test_backward_tutorial_shape(causal, std):
+    """Z=1, H=2, N_CTX=1024, D=64, sm_scale 0.5, fp16, N(0,1) and N(0, 0.5^2)."""
+    inputs, o, grads, delta = run_bwd(1, 2, 1024, 1024, 64, "f16", causal, 0.5, seed=20, std=std)
+    check(inputs, o, grads, delta, "f16", causal, 0.5)
+
+
+SHAPES = [
+    (1, 1, 128, 128),
+    (1, 2, 256, 384),
+    (2, 1, 300, 200),
+    (1, 1, 129, 129),
+    (1, 1, 1, 1),
+    (1, 1, 77, 333),
+    (1, 1, 333, 77),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,M,N", SHAPES)
+def test_backward_matches_oracle(dtype, D, causal, B, H, M, N):
+    scale = 1.0 / math.sqrt(D)
+    inputs, o, grads, delta = run_bwd(B, H, M, N, D, dtype, causal, scale, seed=M * 7 + N)
+    check(inputs, o, grads, delta, dtype, causal, scale)
+
+
+def test_backward_gradient_identities():
+    """sum_j dK_j = 0 (rows of dS sum to zero) and sum_j dV_j = sum_i dO_i."""
+    inputs, o, (dq, dk, dv), _ = run_bwd(1, 2, 512, 512, 64, "f16", True, 0.125, seed=3)
+    do = f64(inputs[3], "f16")
+    assert np.max(np.abs(dk.sum(axis=2))) < 0.05
+    assert np.max(np.abs(dv.sum(axis=2) - do.sum(axis=2))) < 0.05
