@@ -111,3 +111,29 @@ def test_forward_closed_forms():
     assert_close(to_f64(out1), np.ones((B, H, M, D)), 1e-3, "V=1")
     outc, _ = fa.forward(qd, kd, vd, 0.125, True)
     assert_close(to_f64(outc)[:, :, 0], f64(v, "f16")[:, :, 0], 1e-3, "causal row 0")
+
+
+F32_SHAPES = [
+    # B, H, M, N
+    (1, 1, 256, 256),    # single head, 256 x 256 (seed 0)
+    (1, 1, 4096, 4096),  # single head, 4096 x 4096
+    (2, 3, 300, 200),
+    (1, 1, 1, 1),
+    (1, 2, 129, 777),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,M,N", F32_SHAPES)
+def test_forward_f32_matches_oracle(causal, B, H, M, N):
+    """f32 I/O (3xTF32 contraction): max abs <= 1e-4 and relative L2 <= 1e-5 against fp64."""
+    scale = 0.125
+    inputs, out, lse = run_fwd(B, H, M, N, 64, "f32", causal, scale, seed=0)
+    heads = [(0, 0)] if B * H * M * N > 10**7 else None
+    check_heads(inputs, out, lse, "f32", causal, scale, heads=heads, rel_l2=REL_L2_F32)
+
+
+def test_forward_f32_head_dim_128_is_unsupported():
+    import torch
+    q = torch.zeros((1, 1, 8, 128), dtype=torch.float32, device="cuda")
+    assert fa.fa_fwd(q, q, q, q, None, 1, 1, 8, 8, 128, 0.1, 0, fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
