@@ -119,9 +119,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU oracle
-def oracle_forward_sample(budget_s: float, max_heads: int = 48):
-    """Times the fp64 oracle forward on whole heads of the forward workload until
-    `budget_s` of work has run; returns (TFLOP/s, heads, seconds, threads)."""
+def oracle_forward_sample(budget_s: float, max_heads: int = 480):
+    """Times the fp64 oracle forward on whole heads of the forward workload (cycling
+    over four seeded heads, up to ten passes over its 48) until `budget_s` of work
+    has run; returns (TFLOP/s, heads, seconds, threads)."""
     import numpy as np
 
     import oracle
@@ -146,7 +147,7 @@ def oracle_decode_sample(budget_s: float):
     c = DEC
     q = synth.decode_query(1, 4, c["D"], c["dtype"], 0)
     heads, t_total, nbytes = 0, 0.0, 0.0
-    while t_total < budget_s and heads < 64:
+    while t_total < budget_s and heads < 256:
         kh, vh = synth.decode_head_kv(0, heads % 4, c["N"], c["D"], c["dtype"], 0)
         t0 = time.perf_counter()
         oracle.decode(synth.to_f64(q[0, heads % 4], c["dtype"]), synth.to_f64(kh, c["dtype"]),

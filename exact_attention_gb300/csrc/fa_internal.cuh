@@ -48,6 +48,9 @@ cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, 
 cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                             int D, float scale, bool causal, int dtype, const LaunchCtx& ctx);
 
+// head dimension 64 only (fp16 / bf16); called by launch_fwd_half
+cudaError_t launch_fwd_d64(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
+                           float scale, bool causal, int dtype, const LaunchCtx& ctx);
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                            int D, float scale, bool causal, const LaunchCtx& ctx);
 

@@ -1,0 +1,76 @@
+// Pieces shared by the half-precision forward kernels: the tile order over
+// (batch, head, query-tile pair) and packed f32 arithmetic for the softmax.
+#pragma once
+#include "fa_internal.cuh"
+
+namespace fa {
+namespace fwdc {
+
+constexpr int kBM = 128;  // query rows per tile
+constexpr int kBN = 128;  // keys per block
+
+struct TileInfo {
+  int bh, q0, nb0, nb1;
+};
+
+template <bool CAUSAL>
+__device__ __forceinline__ TileInfo tile_info(int tile, int BH, int num_pairs, int nkb) {
+  TileInfo ti;
+  int pair;
+  if (CAUSAL) {  // heads fastest, heaviest (last) pairs first
+    const int pr = tile / BH;
+    ti.bh = tile - pr * BH;
+    pair = num_pairs - 1 - pr;
+  } else {       // pairs of one head adjacent
+    ti.bh = tile / num_pairs;
+    pair = tile - ti.bh * num_pairs;
+  }
+  ti.q0 = pair * 2 * kBM;
+  if (CAUSAL) {
+    ti.nb0 = min(nkb, ti.q0 / kBN + 1);
+    ti.nb1 = min(nkb, (ti.q0 + kBM) / kBN + 1);
+  } else {
+    ti.nb0 = nkb;
+    ti.nb1 = nkb;
+  }
+  return ti;
+}
+
+// ---------------------------------------------------------------- softmax math
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  uint64_t ua, ub, uc, ud;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(ud) : "l"(ua), "l"(ub), "l"(uc));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
+  return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+  uint64_t ua, ub, ud;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
+  asm("add.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
+  float2 d;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Scores of keys past N, or past the query when causal, become -inf.
+template <bool CAUSAL>
+__device__ __forceinline__ void mask32(uint32_t* r, int key0, int N, int row) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int key = key0 + i;
+    if (key >= N || (CAUSAL && key > row)) r[i] = __float_as_uint(-INFINITY);
+  }
+}
+
+}  // namespace fwdc
+}  // namespace fa

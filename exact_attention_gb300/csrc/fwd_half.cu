@@ -41,13 +41,20 @@
 #include <cuda_fp16.h>
 
 #include "fa_internal.cuh"
+#include "fwd_common.cuh"
 #include "ptx.cuh"
 
 namespace fa {
 namespace {
 
-constexpr int kBM = 128;        // query rows per tile
-constexpr int kBN = 128;        // keys per block
+using fwdc::kBM;
+using fwdc::kBN;
+using fwdc::TileInfo;
+using fwdc::tile_info;
+using fwdc::ffma2;
+using fwdc::fadd2;
+using fwdc::fmax3;
+using fwdc::mask32;
 constexpr int kChunk = 16384;   // one 128-row x 128-byte swizzled chunk
 // 10 warps: three share one SM sub-partition (16K registers), so a thread has
 // at most 168 registers.
@@ -80,69 +87,6 @@ struct FwdHdr {
   uint32_t tmem_base;
   int abort_flag;
 };
-
-struct TileInfo {
-  int bh, q0, nb0, nb1;
-};
-
-template <bool CAUSAL>
-__device__ __forceinline__ TileInfo tile_info(int tile, int BH, int num_pairs, int nkb) {
-  TileInfo ti;
-  int pair;
-  if (CAUSAL) {  // heads fastest, heaviest (last) pairs first
-    const int pr = tile / BH;
-    ti.bh = tile - pr * BH;
-    pair = num_pairs - 1 - pr;
-  } else {       // pairs of one head adjacent
-    ti.bh = tile / num_pairs;
-    pair = tile - ti.bh * num_pairs;
-  }
-  ti.q0 = pair * 2 * kBM;
-  if (CAUSAL) {
-    ti.nb0 = min(nkb, ti.q0 / kBN + 1);
-    ti.nb1 = min(nkb, (ti.q0 + kBM) / kBN + 1);
-  } else {
-    ti.nb0 = nkb;
-    ti.nb1 = nkb;
-  }
-  return ti;
-}
-
-// ---------------------------------------------------------------- softmax math
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ua, ub, uc, ud;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(ud) : "l"(ua), "l"(ub), "l"(uc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
-  return d;
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-  uint64_t ua, ub, ud;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-  asm("add.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
-  return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// Scores of keys past N, or past the query when causal, become -inf.
-template <bool CAUSAL>
-__device__ __forceinline__ void mask32(uint32_t* r, int key0, int N, int row) {
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int key = key0 + i;
-    if (key >= N || (CAUSAL && key > row)) r[i] = __float_as_uint(-INFINITY);
-  }
-}
 
 // P for 32 scores against the current maximum: packed halves into pk[16],
 // exact sum into se, rounded sum into sr (only when ROUNDED), and the raw
@@ -516,7 +460,8 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 
 cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                             int D, float scale, bool causal, int dtype, const LaunchCtx& ctx) {
-  if (D != 64 && D != 128) return cudaErrorNotSupported;
+  if (D == 64) return launch_fwd_d64(Q, K, V, O, LSE, BH, M, N, scale, causal, dtype, ctx);
+  if (D != 128) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   if (!make_tmap_3d(&mq, Q, dtype, D, M, BH, 64, kBM) || !make_tmap_3d(&mk, K, dtype, D, N, BH, 64, kBN) ||
       !make_tmap_3d(&mv, V, dtype, D, N, BH, 64, kBN))
@@ -524,10 +469,6 @@ cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O
   const bool bf = dtype == kBF16;
 #define FA_L(DD, BB, CC) \
   if (D == DD && bf == BB && causal == CC) return launch_t<DD, BB, CC>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx);
-  FA_L(64, false, false)
-  FA_L(64, false, true)
-  FA_L(64, true, false)
-  FA_L(64, true, true)
   FA_L(128, false, false)
   FA_L(128, false, true)
   FA_L(128, true, false)

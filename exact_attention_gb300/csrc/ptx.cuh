@@ -319,6 +319,19 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t v) {
       : "r"(v));
   return r;
 }
+// s0 += low half, s1 += high half, each widened exactly to f32 (one mixed-precision add each)
+__device__ __forceinline__ void add_f16x2_to_f32(uint32_t v, float& s0, float& s1) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(v));
+}
+__device__ __forceinline__ void add_bf16x2_to_f32(uint32_t v, float& s0, float& s1) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(v));
+}
 __device__ __forceinline__ float2 unpack_bf16x2(uint32_t v) {
   return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
