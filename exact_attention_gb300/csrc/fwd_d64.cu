@@ -222,9 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         ok = kv_ready(0);
         if (ok) qk(0);
-        ok = ok && arrival_b();  // S_t(0) read
+        // S_t(0) read (only signalled when there is an S_t(1) to compute: with one block the
+        // next arrival would not depend on this thread, and a waiter two phases behind a
+        // barrier never sees its phase complete)
         if (ok && nb > 1) {
-          ok = kv_ready(1);
+          ok = arrival_b() && kv_ready(1);
           if (ok) qk(1);
         }
         for (int j = 0; j < nb && ok; ++j) {
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // previous block's second half of P is stored (waited at the end of that block)
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(sm_b);
+        if (lane == 0 && (j > 0 || nbt > 1)) ptx::mbar_arrive(sm_b);
 
         const int kbase = j * kBN;
         if ((kbase + kBN > N) || (CAUSAL && kbase + kBN - 1 > ti.q0 + t * kBM)) {
