@@ -399,7 +399,7 @@ def run_ours(args):
             "l2": "flushed (512 MB write) before the forward and the backward; decode cache 4.29 GB > L2",
         },
         "roofline": {
-            "kernel": "fwd_half_kernel<64,f16,noncausal>",
+            "kernel": "fwd_d64_kernel<f16,non-causal>",
             "bound": "tensor",
             "achieved": round(fwd_tflops / world, 2),
             "peak": peak_tf,
