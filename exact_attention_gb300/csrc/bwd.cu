@@ -350,18 +350,358 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   }
 }
 
-// --------------------------------------------------------------------------- dQ
-// TMEM: S [0,128) -> dS packed [0,64); dP [128,256); dQ [256, 256+D).
+// ------------------------------------------------------- overlapped dK/dV (D = 64) and dQ
+// Both keep the scores, dP, the packed MMA operands and the accumulators in
+// tensor memory side by side, so the next block's products are computed while
+// the compute warps work on this one. Eight compute warps: warp w owns TMEM lane
+// quarter w % 4 (one tile row per thread) and the half w / 4 of the streamed
+// block's 128 columns. Per block the compute warps signal twice: once the scores
+// are read and P is formed (dK/dV: P^T stored), once dP is read and dS stored.
+// The MMA thread issues the next block's scores at the first signal, and the next
+// dP and the gradient products at the second, so each barrier's next phase
+// depends on work its waiter does after the wait (no waiter falls two phases
+// behind).
+constexpr int kThreadsO = 320;  // compute 0-7, producer 8, MMA 9
+constexpr int kWarpProdO = 8;
+constexpr int kWarpMmaO = 9;
+constexpr int kStagesMax = 4;
+
+struct OvHdr {
+  unsigned long long fixed_full, fixed_empty;
+  unsigned long long full[kStagesMax], empty[kStagesMax];
+  unsigned long long s_full, dp_full;      // MMA -> compute
+  unsigned long long sig1, sig2;           // compute -> MMA (8 warps each)
+  unsigned long long free1, free2;         // MMA -> compute: packed operand regions read
+  unsigned long long acc_full, mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+  float nlse2[kStagesMax][kT];  // per streamed block: -LSE * log2(e) (dK/dV only)
+  float ndlt[kStagesMax][kT];   // per streamed block: -delta (dK/dV only)
+};
+constexpr uint32_t kOvHdrBytes = (sizeof(OvHdr) + 127u) & ~127u;
+
+template <int D>
+struct OvCfg {
+  static constexpr int kDC = D / 64;
+  static constexpr int kTileBytes = kDC * kChunkB;
+  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kData = 2 * kTileBytes + kStages * 2 * kTileBytes;
+  static constexpr int kSmem = 1024 + static_cast<int>(kOvHdrBytes) + kData;
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void ov_init(OvHdr* hdr, int stages, uint32_t full_count) {
+  ptx::mbar_init(ptx::smem_u32(&hdr->fixed_full), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->fixed_empty), 1);
+  for (int st = 0; st < stages; ++st) {
+    ptx::mbar_init(ptx::smem_u32(&hdr->full[st]), full_count);
+    ptx::mbar_init(ptx::smem_u32(&hdr->empty[st]), 1);
+  }
+  ptx::mbar_init(ptx::smem_u32(&hdr->s_full), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->dp_full), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->sig1), 8);
+  ptx::mbar_init(ptx::smem_u32(&hdr->sig2), 8);
+  ptx::mbar_init(ptx::smem_u32(&hdr->free1), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->free2), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->acc_full), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->mma_done), 1);
+  hdr->abort_flag = 0;
+  ptx::fence_mbar_init();
+}
+
+// dK / dV with D = 64. TMEM: S^T [0,128), dP^T [128,256), P^T packed [256,320),
+// dS^T packed [320,384), dV [384,448), dK [448,512).
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsO, 1)
+    bwd_dkdv64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                      const float* __restrict__ LSE, const float* __restrict__ delta, uint16_t* __restrict__ dK,
+                      uint16_t* __restrict__ dV, int BH, int M, int N, float scale, DevStatus* status,
+                      unsigned long long budget_ns) {
+  constexpr int D = 64;
+  using C = OvCfg<D>;
+  constexpr uint32_t cS = 0, cdP = 128, cP = 256, cdS = 320, cdV = 384, cdK = 448;
+  extern __shared__ uint8_t smem_raw[];
+  OvHdr* hdr = reinterpret_cast<OvHdr*>(smem_raw);
+  const uint32_t data = (ptx::smem_u32(smem_raw) + kOvHdrBytes + 1023u) & ~1023u;
+  const uint32_t sK = data, sV = data + C::kTileBytes;
+  auto sQ = [&](int st) { return data + 2 * C::kTileBytes + st * 2 * C::kTileBytes; };
+  auto sdO = [&](int st) { return sQ(st) + C::kTileBytes; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
+  const int items = BH * nkb;
+  const float sl2 = scale * kLog2eB;
+  auto item = [&](int w) {
+    BwdItem it;
+    it.bh = w / nkb;
+    it.r0 = (w - it.bh * nkb) * kT;
+    it.lo = CAUSAL ? min(it.r0 / kT, nqb) : 0;  // query blocks before the diagonal see no key here
+    it.hi = nqb;
+    return it;
+  };
+
+  if (threadIdx.x == 0) ov_init(hdr, C::kStages, 2);  // full: TMA bytes + LSE/delta staging
+  if (warp == kWarpMmaO) {
+    ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = hdr->tmem_base;
+  ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDkDv};
+
+  if (warp == kWarpProdO) {
+    // ------------------------------------------------------------ producer (whole warp)
+    uint32_t it_s = 0;
+    int n_item = 0;
+    bool ok = true;
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+      const BwdItem itm = item(w);
+      if (lane == 0) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10);
+        if (ok) {
+          const uint32_t ff = ptx::smem_u32(&hdr->fixed_full);
+          ptx::mbar_arrive_expect_tx(ff, 2 * C::kTileBytes);
+          ptx::tma_load_3d(sK, &tmK, ff, 0, itm.r0, itm.bh);
+          ptx::tma_load_3d(sV, &tmV, ff, 0, itm.r0, itm.bh);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      for (int i = itm.lo; i < itm.hi && ok; ++i, ++it_s) {
+        const int st = it_s % C::kStages;
+        if (lane == 0)
+          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / C::kStages) & 1u) ^ 1u, wc, 11);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        const uint32_t fb = ptx::smem_u32(&hdr->full[st]);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
+          ptx::tma_load_3d(sQ(st), &tmQ, fb, 0, i * kT, itm.bh);
+          ptx::tma_load_3d(sdO(st), &tmdO, fb, 0, i * kT, itm.bh);
+        }
+        // -LSE (base 2) and -delta of the block's queries; past M: P = 0, delta = 0
+        for (int q = lane; q < kT; q += 32) {
+          const int row = i * kT + q;
+          const bool in = row < M;
+          const size_t g = static_cast<size_t>(itm.bh) * M + (in ? row : 0);
+          hdr->nlse2[st][q] = in ? -LSE[g] * kLog2eB : -INFINITY;
+          hdr->ndlt[st][q] = in ? -delta[g] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(fb);
+      }
+    }
+    if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
+      for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
+        ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
+    }
+  } else if (warp == kWarpMmaO) {
+    // ------------------------------------------------------------ MMA issuer (lane 0)
+    if (lane == 0) {
+      constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
+      constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
+      constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
+      uint32_t it_s = 0, n1 = 0, n2 = 0;
+      int n_item = 0;
+      bool ok = true;
+      auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+        return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
+      };
+      auto commit = [&](unsigned long long* bar) { ptx::tc_commit(ptx::smem_u32(bar)); };
+      auto stage_ready = [&](uint32_t k) { return wait(&hdr->full[k % C::kStages], (k / C::kStages) & 1u, 21); };
+      auto qk = [&](uint32_t k) {  // S^T = K Q^T
+        const int st = k % C::kStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss(tmem + cS, kmajor_desc(sK, ks), kmajor_desc(sQ(st), ks), id_s, ks > 0);
+        commit(&hdr->s_full);
+      };
+      auto vdo = [&](uint32_t k) {  // dP^T = V dO^T
+        const int st = k % C::kStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
+        commit(&hdr->dp_full);
+      };
+      for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+        const BwdItem itm = item(w);
+        if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
+        if (itm.lo < itm.hi) {
+          ok = stage_ready(it_s);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          qk(it_s);
+          vdo(it_s);
+        }
+        for (int i = itm.lo; i < itm.hi; ++i, ++it_s) {
+          const int st = it_s % C::kStages;
+          const bool more = i + 1 < itm.hi;
+          const bool acc = i > itm.lo;
+          // S^T(i) read and P^T(i) stored
+          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+          if (ok && more) ok = stage_ready(it_s + 1);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (more) qk(it_s + 1);
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks)  // dV += P^T dO
+            ptx::mma_f16_ts(tmem + cdV, tmem + cP + ks * 8, mnmajor_desc(sdO(st), ks), id_g, (acc || ks > 0));
+          commit(&hdr->free1);
+          // dP^T(i) read and dS^T(i) stored
+          ok = wait(&hdr->sig2, (n2++) & 1u, 23);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (more) vdo(it_s + 1);
+#pragma unroll
+          for (int ks = 0; ks < kT / 16; ++ks)  // dK += dS^T Q
+            ptx::mma_f16_ts(tmem + cdK, tmem + cdS + ks * 8, mnmajor_desc(sQ(st), ks), id_g, (acc || ks > 0));
+          commit(&hdr->free2);
+          commit(&hdr->empty[st]);
+        }
+        if (!ok) break;
+        commit(&hdr->fixed_empty);
+        commit(&hdr->acc_full);
+      }
+      commit(&hdr->mma_done);
+      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps: one key row per thread
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's query columns [c0, c0 + 64)
+    uint32_t it_s = 0, nb = 0;  // blocks processed (all items): s_full/dp_full/free phases
+    int n_item = 0;
+    bool ok = true;
+    auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+      const bool r = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site));
+      ptx::tc_fence_after();
+      return r;
+    };
+    auto signal = [&](unsigned long long* bar) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
+    };
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+      const BwdItem itm = item(w);
+      const int key = itm.r0 + quarter * 32 + lane;
+      for (int i = itm.lo; i < itm.hi; ++i, ++it_s, ++nb) {
+        const int st = it_s % C::kStages;
+        // S^T(i) computed; the stage's -LSE/-delta were staged before its full barrier
+        ok = wait_all(&hdr->s_full, nb & 1u, 30) &&
+             wait_all(&hdr->full[st], (it_s / C::kStages) & 1u, 31);
+        if (!ok) break;
+        const float* nl = hdr->nlse2[st] + c0;
+        const float* nd = hdr->ndlt[st] + c0;
+        const int qb = i * kT + static_cast<int>(c0);  // first query of this warp's columns
+        const bool diag = CAUSAL && qb < key;          // some of these queries precede the key
+        float p[64];
+        {
+          uint32_t s[64];
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0, s);
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
+          ptx::tmem_wait_ld32(s);
+          ptx::tmem_wait_ld32(s + 32);
+          const float2 c2 = make_float2(sl2, sl2);
+#pragma unroll
+          for (int q = 0; q < 64; q += 2) {
+            const float2 nlq = *reinterpret_cast<const float2*>(nl + q);
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(s[q]), __uint_as_float(s[q + 1])), c2, nlq);
+            p[q] = ptx::ex2(x.x);
+            p[q + 1] = ptx::ex2(x.y);
+            if (diag) {  // key j is visible to query i iff j <= i
+              if (qb + q < key) p[q] = 0.f;
+              if (qb + q + 1 < key) p[q + 1] = 0.f;
+            }
+          }
+        }
+        // P^T(i-1) has been read by dV's MMA before P^T(i) overwrites it
+        if (nb > 0) {
+          ok = wait_all(&hdr->free1, (nb - 1u) & 1u, 32);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pk[k] = pack2<BF16>(p[c + 2 * k], p[c + 2 * k + 1]);
+          ptx::tmem_st16(tmem + lane_sel + cP + (c0 + c) / 2, pk);
+        }
+        ptx::tmem_wait_st();
+        signal(&hdr->sig1);
+        // dP^T(i) computed; dS^T = P^T o (dP^T - delta)
+        ok = wait_all(&hdr->dp_full, nb & 1u, 33);
+        if (ok && nb > 0) ok = wait_all(&hdr->free2, (nb - 1u) & 1u, 34);
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t dp[32];
+          ptx::tmem_ld32(tmem + lane_sel + cdP + c0 + c, dp);
+          ptx::tmem_wait_ld32(dp);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 ndq = *reinterpret_cast<const float2*>(nd + c + 2 * k);
+            const float2 t = ptx::fadd2(make_float2(__uint_as_float(dp[2 * k]), __uint_as_float(dp[2 * k + 1])), ndq);
+            const float2 ds = ptx::fmul2(make_float2(p[c + 2 * k], p[c + 2 * k + 1]), t);
+            pk[k] = pack2<BF16>(ds.x, ds.y);
+          }
+          ptx::tmem_st16(tmem + lane_sel + cdS + (c0 + c) / 2, pk);
+        }
+        ptx::tmem_wait_st();
+        signal(&hdr->sig2);
+      }
+      if (!ok) break;
+      // epilogue: this warp writes columns [32 * half, 32 * half + 32) of dV and scale * dK
+      ok = wait_all(&hdr->acc_full, n_item & 1, 35);
+      if (!ok) break;
+      const bool valid = key < N;
+      const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t a[32];
+        ptx::tmem_ld32(tmem + lane_sel + (part == 0 ? cdV : cdK) + 32 * half, a);
+        ptx::tmem_wait_ld32(a);
+        const float f = part == 0 ? 1.f : scale;
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          h[k] = none ? 0u : pack2<BF16>(__uint_as_float(a[2 * k]) * f, __uint_as_float(a[2 * k + 1]) * f);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>((part == 0 ? dV : dK) + g);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMmaO) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// dQ. TMEM: S [0,128), dP [128,256), dS packed [256,320), dQ [320, 320+D).
 template <int D, bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsB, 1)
+__global__ void __launch_bounds__(kThreadsO, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                   const float* __restrict__ LSE, const float* __restrict__ delta, uint16_t* __restrict__ dQ, int BH,
                   int M, int N, float scale, DevStatus* status, unsigned long long budget_ns) {
-  using C = BwdCfg<D>;
+  using C = OvCfg<D>;
+  constexpr uint32_t cS = 0, cdP = 128, cdS = 256, cdQ = 320;
+  constexpr int kDH = D / 2;  // dQ columns per warp half in the epilogue
   extern __shared__ uint8_t smem_raw[];
-  BwdHdr* hdr = reinterpret_cast<BwdHdr*>(smem_raw);
-  const uint32_t data = (ptx::smem_u32(smem_raw) + kHdrBytes + 1023u) & ~1023u;
+  OvHdr* hdr = reinterpret_cast<OvHdr*>(smem_raw);
+  const uint32_t data = (ptx::smem_u32(smem_raw) + kOvHdrBytes + 1023u) & ~1023u;
   const uint32_t sQ = data, sdO = data + C::kTileBytes;
   auto sK = [&](int st) { return data + 2 * C::kTileBytes + st * 2 * C::kTileBytes; };
   auto sV = [&](int st) { return sK(st) + C::kTileBytes; };
@@ -369,11 +709,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nqb;
   const float sl2 = scale * kLog2eB;
-
   auto item = [&](int w) {
     BwdItem it;
-    // causal: heaviest (last) query blocks first
-    const int qb_rev = w / BH;
+    const int qb_rev = w / BH;  // causal: heaviest (last) query blocks first
     it.bh = w - qb_rev * BH;
     const int qb = CAUSAL ? nqb - 1 - qb_rev : qb_rev;
     it.r0 = qb * kT;
@@ -382,21 +720,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     return it;
   };
 
-  if (threadIdx.x == 0) {
-    ptx::mbar_init(ptx::smem_u32(&hdr->fixed_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&hdr->fixed_empty), 1);
-    for (int s = 0; s < kStagesB; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&hdr->full[s]), 1);
-      ptx::mbar_init(ptx::smem_u32(&hdr->empty[s]), 1);
-    }
-    ptx::mbar_init(ptx::smem_u32(&hdr->s_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&hdr->p_full), 4);
-    ptx::mbar_init(ptx::smem_u32(&hdr->acc_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&hdr->mma_done), 1);
-    hdr->abort_flag = 0;
-    ptx::fence_mbar_init();
-  }
-  if (warp == kWarpMmaB) {
+  if (threadIdx.x == 0) ov_init(hdr, C::kStages, 1);
+  if (warp == kWarpMmaO) {
     ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
     ptx::tmem_relinquish();
   }
@@ -406,7 +731,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDq};
 
-  if (warp == kWarpProdB) {
+  if (warp == kWarpProdO) {
     if (lane == 0) {
       uint32_t it_s = 0;
       int n_item = 0;
@@ -421,8 +746,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           ptx::tma_load_3d(sdO + c * kChunkB, &tmdO, ff, c * 64, itm.r0, itm.bh);
         }
         for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
-          const int st = it_s % kStagesB;
-          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / kStagesB) & 1u) ^ 1u, wc, 11);
+          const int st = it_s % C::kStages;
+          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / C::kStages) & 1u) ^ 1u, wc, 11);
           if (!ok) break;
           const uint32_t fb = ptx::smem_u32(&hdr->full[st]);
           ptx::mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
@@ -432,112 +757,162 @@ __global__ void __launch_bounds__(kThreadsB, 1)
           }
         }
       }
+      if (hdr->abort_flag) {  // let issued copies land before shared memory is released
+        for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
+      }
     }
-  } else if (warp == kWarpMmaB) {
+  } else if (warp == kWarpMmaO) {
     if (lane == 0) {
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
       constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
-      uint32_t it_s = 0, p_ph = 0;
+      uint32_t it_s = 0, n1 = 0, n2 = 0;
       int n_item = 0;
       bool ok = true;
+      auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+        return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
+      };
+      auto commit = [&](unsigned long long* bar) { ptx::tc_commit(ptx::smem_u32(bar)); };
+      auto stage_ready = [&](uint32_t k) { return wait(&hdr->full[k % C::kStages], (k / C::kStages) & 1u, 21); };
+      auto qk = [&](uint32_t k) {  // S = Q K^T
+        const int st = k % C::kStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss(tmem + cS, kmajor_desc(sQ, ks), kmajor_desc(sK(st), ks), id_s, ks > 0);
+        commit(&hdr->s_full);
+      };
+      auto dov = [&](uint32_t k) {  // dP = dO V^T
+        const int st = k % C::kStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sdO, ks), kmajor_desc(sV(st), ks), id_s, ks > 0);
+        commit(&hdr->dp_full);
+      };
       for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
         const BwdItem itm = item(w);
-        if (!ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_full), n_item & 1, wc, 20)) break;
-        ptx::tc_fence_after();
+        if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
+        if (itm.lo < itm.hi) {
+          ok = stage_ready(it_s);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          qk(it_s);
+          dov(it_s);
+        }
         for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
-          const int st = it_s % kStagesB;
-          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->full[st]), (it_s / kStagesB) & 1u, wc, 21);
+          const int st = it_s % C::kStages;
+          const bool more = j + 1 < itm.hi;
+          // S(j) read
+          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+          if (ok && more) ok = stage_ready(it_s + 1);
           if (!ok) break;
           ptx::tc_fence_after();
-          // S = Q K^T and dP = dO V^T
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            ptx::mma_f16_ss(tmem + 0, kmajor_desc(sQ, ks), kmajor_desc(sK(st), ks), id_s, ks > 0);
-            ptx::mma_f16_ss(tmem + 128, kmajor_desc(sdO, ks), kmajor_desc(sV(st), ks), id_s, ks > 0);
-          }
-          ptx::tc_commit(ptx::smem_u32(&hdr->s_full));
-          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->p_full), p_ph, wc, 22);
+          if (more) qk(it_s + 1);
+          // dP(j) read and dS(j) stored
+          ok = wait(&hdr->sig2, (n2++) & 1u, 23);
           if (!ok) break;
-          p_ph ^= 1u;
           ptx::tc_fence_after();
-          // dQ += dS K
+          if (more) dov(it_s + 1);
 #pragma unroll
-          for (int ks = 0; ks < kT / 16; ++ks)
-            ptx::mma_f16_ts(tmem + 256, tmem + 0 + ks * 8, mnmajor_desc(sK(st), ks), id_g, (j > itm.lo || ks > 0));
-          ptx::tc_commit(ptx::smem_u32(&hdr->empty[st]));
+          for (int ks = 0; ks < kT / 16; ++ks)  // dQ += dS K
+            ptx::mma_f16_ts(tmem + cdQ, tmem + cdS + ks * 8, mnmajor_desc(sK(st), ks), id_g,
+                            (j > itm.lo || ks > 0));
+          commit(&hdr->free2);
+          commit(&hdr->empty[st]);
         }
         if (!ok) break;
-        ptx::tc_commit(ptx::smem_u32(&hdr->fixed_empty));
-        ptx::tc_commit(ptx::smem_u32(&hdr->acc_full));
+        commit(&hdr->fixed_empty);
+        commit(&hdr->acc_full);
       }
-      ptx::tc_commit(ptx::smem_u32(&hdr->mma_done));
+      commit(&hdr->mma_done);
       ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
     }
   } else {
     // ------------------------------------------------------------ compute warps: one query row per thread
-    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem + lane_sel, tdP = tmem + 128 + lane_sel, tdQ = tmem + 256 + lane_sel;
-    uint32_t s_ph = 0;
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's key columns [c0, c0 + 64)
+    uint32_t nb = 0;
     int n_item = 0;
     bool ok = true;
+    auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+      const bool r = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site));
+      ptx::tc_fence_after();
+      return r;
+    };
+    auto signal = [&](unsigned long long* bar) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
+    };
     for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
       const BwdItem itm = item(w);
-      const int row = itm.r0 + warp * 32 + lane;
+      const int row = itm.r0 + quarter * 32 + lane;
       const bool valid = row < M;
       const size_t g = static_cast<size_t>(itm.bh) * M + (valid ? row : 0);
-      const float lse2 = valid ? LSE[g] * kLog2eB : INFINITY;  // past M: P = 0
-      const float dlt = valid ? delta[g] : 0.f;
-      for (int j = itm.lo; j < itm.hi; ++j) {
-        ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(&hdr->s_full), s_ph, wc, 30));
+      const float nlse2 = valid ? -LSE[g] * kLog2eB : -INFINITY;  // past M: P = 0
+      const float ndlt = valid ? -delta[g] : 0.f;
+      for (int j = itm.lo; j < itm.hi; ++j, ++nb) {
+        ok = wait_all(&hdr->s_full, nb & 1u, 30);
         if (!ok) break;
-        s_ph ^= 1u;
-        ptx::tc_fence_after();
-        const int k0 = j * kT;
-        const bool edge = k0 + kT > N || (CAUSAL && k0 + kT - 1 > itm.r0);
-#pragma unroll
-        for (int c = 0; c < kT; c += 32) {
-          uint32_t s[32], dp[32];
-          ptx::tmem_ld32(tS + c, s);
-          ptx::tmem_ld32(tdP + c, dp);
+        const int kb = j * kT + static_cast<int>(c0);  // first key of this warp's columns
+        const bool edge = kb + 64 > N || (CAUSAL && kb + 63 > row);
+        float p[64];
+        {
+          uint32_t s[64];
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0, s);
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
           ptx::tmem_wait_ld32(s);
+          ptx::tmem_wait_ld32(s + 32);
+          const float2 c2 = make_float2(sl2, sl2), nl2 = make_float2(nlse2, nlse2);
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), c2, nl2);
+            p[k] = ptx::ex2(x.x);
+            p[k + 1] = ptx::ex2(x.y);
+            if (edge) {
+              if (kb + k >= N || (CAUSAL && kb + k > row)) p[k] = 0.f;
+              if (kb + k + 1 >= N || (CAUSAL && kb + k + 1 > row)) p[k + 1] = 0.f;
+            }
+          }
+        }
+        signal(&hdr->sig1);  // S(j) read: the next S may be computed
+        ok = wait_all(&hdr->dp_full, nb & 1u, 31);
+        if (ok && nb > 0) ok = wait_all(&hdr->free2, (nb - 1u) & 1u, 32);  // dS(j-1) read by dQ's MMA
+        if (!ok) break;
+        const float2 nd2 = make_float2(ndlt, ndlt);
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t dp[32];
+          ptx::tmem_ld32(tmem + lane_sel + cdP + c0 + c, dp);
           ptx::tmem_wait_ld32(dp);
-          uint32_t pd[16];
+          uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            float d2[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int key = k0 + c + 2 * k + h;
-              float p = ptx::ex2(fmaf(__uint_as_float(s[2 * k + h]), sl2, -lse2));
-              if (edge && (key >= N || (CAUSAL && key > row))) p = 0.f;
-              d2[h] = p * (__uint_as_float(dp[2 * k + h]) - dlt);
-            }
-            pd[k] = pack2<BF16>(d2[0], d2[1]);
+            const float2 t = ptx::fadd2(make_float2(__uint_as_float(dp[2 * k]), __uint_as_float(dp[2 * k + 1])), nd2);
+            const float2 ds = ptx::fmul2(make_float2(p[c + 2 * k], p[c + 2 * k + 1]), t);
+            pk[k] = pack2<BF16>(ds.x, ds.y);
           }
-          ptx::tmem_st16(tS + c / 2, pd);
+          ptx::tmem_st16(tmem + lane_sel + cdS + (c0 + c) / 2, pk);
         }
         ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->p_full));
+        signal(&hdr->sig2);
       }
       if (!ok) break;
-      ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(&hdr->acc_full), n_item & 1, wc, 31));
+      ok = wait_all(&hdr->acc_full, n_item & 1, 33);
       if (!ok) break;
-      ptx::tc_fence_after();
       const bool none = itm.lo >= itm.hi;
 #pragma unroll
-      for (int c = 0; c < D; c += 32) {
+      for (int c = 0; c < kDH; c += 32) {
         uint32_t a[32];
-        ptx::tmem_ld32(tdQ + c, a);
+        ptx::tmem_ld32(tmem + lane_sel + cdQ + kDH * half + c, a);
         ptx::tmem_wait_ld32(a);
         uint32_t h[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k)
           h[k] = none ? 0u : pack2<BF16>(__uint_as_float(a[2 * k]) * scale, __uint_as_float(a[2 * k + 1]) * scale);
         if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dQ + g * D + c);
+          uint4* d4 = reinterpret_cast<uint4*>(dQ + g * D + kDH * half + c);
 #pragma unroll
           for (int v = 0; v < 4; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
         }
@@ -548,7 +923,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMmaB) {
+  if (warp == kWarpMmaO) {
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -579,25 +954,35 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     return cudaErrorInvalidValue;
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   {
-    auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
     const long long items = static_cast<long long>(BH) * nkb;
     const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
-    kern<<<grid, kThreadsB, C::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dK),
-                                                   static_cast<uint16_t*>(dV), BH, M, N, scale, ctx.status,
-                                                   ctx.wait_budget_ns);
+    cudaError_t e;
+    if constexpr (D == 64) {  // tensor memory holds the overlapped layout
+      auto kern = bwd_dkdv64_kernel<BF16, CAUSAL>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, OvCfg<64>::kSmem);
+      if (e != cudaSuccess) return e;
+      kern<<<grid, kThreadsO, OvCfg<64>::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta,
+                                                               static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV),
+                                                               BH, M, N, scale, ctx.status, ctx.wait_budget_ns);
+    } else {
+      auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      if (e != cudaSuccess) return e;
+      kern<<<grid, kThreadsB, C::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dK),
+                                                     static_cast<uint16_t*>(dV), BH, M, N, scale, ctx.status,
+                                                     ctx.wait_budget_ns);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   {
     auto kern = bwd_dq_kernel<D, BF16, CAUSAL>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, OvCfg<D>::kSmem);
     if (e != cudaSuccess) return e;
     const long long items = static_cast<long long>(BH) * nqb;
     const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
-    kern<<<grid, kThreadsB, C::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dQ), BH, M,
-                                                   N, scale, ctx.status, ctx.wait_budget_ns);
+    kern<<<grid, kThreadsO, OvCfg<D>::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dQ),
+                                                            BH, M, N, scale, ctx.status, ctx.wait_budget_ns);
     return cudaGetLastError();
   }
 }

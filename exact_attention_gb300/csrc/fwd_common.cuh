@@ -2,6 +2,7 @@
 // (batch, head, query-tile pair) and packed f32 arithmetic for the softmax.
 #pragma once
 #include "fa_internal.cuh"
+#include "ptx.cuh"
 
 namespace fa {
 namespace fwdc {
@@ -36,31 +37,10 @@ __device__ __forceinline__ TileInfo tile_info(int tile, int BH, int num_pairs, i
   return ti;
 }
 
-// ---------------------------------------------------------------- softmax math
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  uint64_t ua, ub, uc, ud;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(uc) : "f"(c.x), "f"(c.y));
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(ud) : "l"(ua), "l"(ub), "l"(uc));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
-  return d;
-}
-__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
-  uint64_t ua, ub, ud;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ua) : "f"(a.x), "f"(a.y));
-  asm("mov.b64 %0, {%1, %2};" : "=l"(ub) : "f"(b.x), "f"(b.y));
-  asm("add.f32x2 %0, %1, %2;" : "=l"(ud) : "l"(ua), "l"(ub));
-  float2 d;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(ud));
-  return d;
-}
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
+// packed f32 arithmetic lives in ptx.cuh
+using ptx::fadd2;
+using ptx::ffma2;
+using ptx::fmax3;
 
 // Scores of keys past N, or past the query when causal, become -inf.
 template <bool CAUSAL>
