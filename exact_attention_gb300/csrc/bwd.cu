@@ -357,13 +357,17 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // quarter w % 4 (one tile row per thread) and the half w / 4 of the streamed
 // block's 128 columns. Per block the compute warps signal twice: once the scores
 // are read and P is formed (dK/dV: P^T stored), once dP is read and dS stored.
-// The MMA thread issues the next block's scores at the first signal, and the next
-// dP and the gradient products at the second, so each barrier's next phase
-// depends on work its waiter does after the wait (no waiter falls two phases
-// behind).
-constexpr int kThreadsO = 320;  // compute 0-7, producer 8, MMA 9
+// Two MMA-issuing threads share the work (a thread that has issued tcgen05 work
+// is slow to reach its next barrier operation, so one issuer left the tensor
+// pipe idle): warp 9 issues the next block's scores at the first signal and its
+// dP at the second; warp 10 issues the gradient products of this block at each
+// signal and releases the streamed stage (warp 9's products on it completed
+// before the compute warps read them). Each barrier's next phase depends on work
+// its waiters do after their wait, so no waiter falls two phases behind.
+constexpr int kThreadsO = 352;  // compute 0-7, producer 8, MMA issuers 9 (scores) and 10 (gradients)
 constexpr int kWarpProdO = 8;
 constexpr int kWarpMmaO = 9;
+constexpr int kWarpGradO = 10;
 constexpr int kStagesMax = 4;
 
 struct OvHdr {
@@ -372,7 +376,7 @@ struct OvHdr {
   unsigned long long s_full, dp_full;      // MMA -> compute
   unsigned long long sig1, sig2;           // compute -> MMA (8 warps each)
   unsigned long long free1, free2;         // MMA -> compute: packed operand regions read
-  unsigned long long acc_full, mma_done;
+  unsigned long long acc_full, mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
   float nlse2[kStagesMax][kT];  // per streamed block: -LSE * log2(e) (dK/dV only)
@@ -404,7 +408,8 @@ __device__ __forceinline__ void ov_init(OvHdr* hdr, int stages, uint32_t full_co
   ptx::mbar_init(ptx::smem_u32(&hdr->free1), 1);
   ptx::mbar_init(ptx::smem_u32(&hdr->free2), 1);
   ptx::mbar_init(ptx::smem_u32(&hdr->acc_full), 1);
-  ptx::mbar_init(ptx::smem_u32(&hdr->mma_done), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[0]), 1);
+  ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[1]), 1);
   hdr->abort_flag = 0;
   ptx::fence_mbar_init();
 }
@@ -453,11 +458,33 @@ __global__ void __launch_bounds__(kThreadsO, 1)
 
   if (warp == kWarpProdO) {
     // ------------------------------------------------------------ producer (whole warp)
+    // Walks (item, query block) in order. -LSE (base 2) and -delta of a block's queries
+    // are read from global memory one block ahead into registers (lane l holds queries
+    // l, l+32, l+64, l+96), so their latency overlaps the wait for the next free stage.
+    constexpr int kQL = kT / 32;
+    float nl_v[kQL], nd_v[kQL];
+    auto fetch = [&](const BwdItem& it, int i) {
+#pragma unroll
+      for (int k = 0; k < kQL; ++k) {
+        const int row = i * kT + lane + 32 * k;
+        const bool in = row < M;  // past M: P = 0 (exp of -inf), delta = 0
+        const size_t g = static_cast<size_t>(it.bh) * M + (in ? row : 0);
+        nl_v[k] = in ? -LSE[g] * kLog2eB : -INFINITY;
+        nd_v[k] = in ? -delta[g] : 0.f;
+      }
+    };
     uint32_t it_s = 0;
     int n_item = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
-      const BwdItem itm = item(w);
+    int w = blockIdx.x;
+    BwdItem itm{};
+    // first item that has a query block (items without one need only their fixed tiles)
+    if (w < items) {
+      itm = item(w);
+      if (itm.lo < itm.hi) fetch(itm, itm.lo);
+    }
+    for (; w < items && ok; w += gridDim.x, ++n_item) {
+      itm = item(w);
       if (lane == 0) {
         ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10);
         if (ok) {
@@ -480,25 +507,36 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::tma_load_3d(sQ(st), &tmQ, fb, 0, i * kT, itm.bh);
           ptx::tma_load_3d(sdO(st), &tmdO, fb, 0, i * kT, itm.bh);
         }
-        // -LSE (base 2) and -delta of the block's queries; past M: P = 0, delta = 0
-        for (int q = lane; q < kT; q += 32) {
-          const int row = i * kT + q;
-          const bool in = row < M;
-          const size_t g = static_cast<size_t>(itm.bh) * M + (in ? row : 0);
-          hdr->nlse2[st][q] = in ? -LSE[g] * kLog2eB : -INFINITY;
-          hdr->ndlt[st][q] = in ? -delta[g] : 0.f;
+#pragma unroll
+        for (int k = 0; k < kQL; ++k) {
+          hdr->nlse2[st][lane + 32 * k] = nl_v[k];
+          hdr->ndlt[st][lane + 32 * k] = nd_v[k];
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(fb);
+        // next block's values: this item's next block, else the first block of the next
+        // item that has one
+        if (i + 1 < itm.hi) {
+          fetch(itm, i + 1);
+        } else {
+          for (int w2 = w + gridDim.x; w2 < items; w2 += gridDim.x) {
+            const BwdItem nx = item(w2);
+            if (nx.lo < nx.hi) {
+              fetch(nx, nx.lo);
+              break;
+            }
+          }
+        }
       }
     }
     if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
       for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
         ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
     }
-  } else if (warp == kWarpMmaO) {
-    // ------------------------------------------------------------ MMA issuer (lane 0)
+  } else if (warp == kWarpMmaO || warp == kWarpGradO) {
+    // ------------------------------------------------------------ MMA issuers (lane 0)
     if (lane == 0) {
+      const bool scores = warp == kWarpMmaO;
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
       constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
@@ -526,13 +564,15 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       };
       for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
         const BwdItem itm = item(w);
-        if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
-        if (itm.lo < itm.hi) {
-          ok = stage_ready(it_s);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          qk(it_s);
-          vdo(it_s);
+        if (scores) {
+          if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
+          if (itm.lo < itm.hi) {
+            ok = stage_ready(it_s);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            qk(it_s);
+            vdo(it_s);
+          }
         }
         for (int i = itm.lo; i < itm.hi; ++i, ++it_s) {
           const int st = it_s % C::kStages;
@@ -540,31 +580,37 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           const bool acc = i > itm.lo;
           // S^T(i) read and P^T(i) stored
           ok = wait(&hdr->sig1, (n1++) & 1u, 22);
-          if (ok && more) ok = stage_ready(it_s + 1);
+          if (ok && scores && more) ok = stage_ready(it_s + 1);
           if (!ok) break;
           ptx::tc_fence_after();
-          if (more) qk(it_s + 1);
+          if (scores) {
+            if (more) qk(it_s + 1);
+          } else {
 #pragma unroll
-          for (int ks = 0; ks < kT / 16; ++ks)  // dV += P^T dO
-            ptx::mma_f16_ts(tmem + cdV, tmem + cP + ks * 8, mnmajor_desc(sdO(st), ks), id_g, (acc || ks > 0));
-          commit(&hdr->free1);
+            for (int ks = 0; ks < kT / 16; ++ks)  // dV += P^T dO
+              ptx::mma_f16_ts(tmem + cdV, tmem + cP + ks * 8, mnmajor_desc(sdO(st), ks), id_g, (acc || ks > 0));
+            commit(&hdr->free1);
+          }
           // dP^T(i) read and dS^T(i) stored
           ok = wait(&hdr->sig2, (n2++) & 1u, 23);
           if (!ok) break;
           ptx::tc_fence_after();
-          if (more) vdo(it_s + 1);
+          if (scores) {
+            if (more) vdo(it_s + 1);
+          } else {
 #pragma unroll
-          for (int ks = 0; ks < kT / 16; ++ks)  // dK += dS^T Q
-            ptx::mma_f16_ts(tmem + cdK, tmem + cdS + ks * 8, mnmajor_desc(sQ(st), ks), id_g, (acc || ks > 0));
-          commit(&hdr->free2);
-          commit(&hdr->empty[st]);
+            for (int ks = 0; ks < kT / 16; ++ks)  // dK += dS^T Q
+              ptx::mma_f16_ts(tmem + cdK, tmem + cdS + ks * 8, mnmajor_desc(sQ(st), ks), id_g, (acc || ks > 0));
+            commit(&hdr->free2);
+            commit(&hdr->empty[st]);
+          }
         }
         if (!ok) break;
-        commit(&hdr->fixed_empty);
-        commit(&hdr->acc_full);
+        commit(scores ? &hdr->fixed_empty : &hdr->acc_full);
       }
-      commit(&hdr->mma_done);
-      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
+      const int me = scores ? 0 : 1;
+      commit(&hdr->mma_done[me]);
+      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[me]), 0u, 1000000000ull);
     }
   } else {
     // ------------------------------------------------------------ compute warps: one key row per thread
@@ -762,8 +808,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
       }
     }
-  } else if (warp == kWarpMmaO) {
+  } else if (warp == kWarpMmaO || warp == kWarpGradO) {
+    // ------------------------------------------------------------ MMA issuers (lane 0)
     if (lane == 0) {
+      const bool scores = warp == kWarpMmaO;
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
       constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
@@ -791,41 +839,48 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       };
       for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
         const BwdItem itm = item(w);
-        if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
-        if (itm.lo < itm.hi) {
-          ok = stage_ready(it_s);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          qk(it_s);
-          dov(it_s);
+        if (scores) {
+          if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
+          if (itm.lo < itm.hi) {
+            ok = stage_ready(it_s);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            qk(it_s);
+            dov(it_s);
+          }
         }
         for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
           const int st = it_s % C::kStages;
           const bool more = j + 1 < itm.hi;
-          // S(j) read
-          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
-          if (ok && more) ok = stage_ready(it_s + 1);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          if (more) qk(it_s + 1);
+          if (scores) {
+            // S(j) read
+            ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+            if (ok && more) ok = stage_ready(it_s + 1);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (more) qk(it_s + 1);
+          }
           // dP(j) read and dS(j) stored
           ok = wait(&hdr->sig2, (n2++) & 1u, 23);
           if (!ok) break;
           ptx::tc_fence_after();
-          if (more) dov(it_s + 1);
+          if (scores) {
+            if (more) dov(it_s + 1);
+          } else {
 #pragma unroll
-          for (int ks = 0; ks < kT / 16; ++ks)  // dQ += dS K
-            ptx::mma_f16_ts(tmem + cdQ, tmem + cdS + ks * 8, mnmajor_desc(sK(st), ks), id_g,
-                            (j > itm.lo || ks > 0));
-          commit(&hdr->free2);
-          commit(&hdr->empty[st]);
+            for (int ks = 0; ks < kT / 16; ++ks)  // dQ += dS K
+              ptx::mma_f16_ts(tmem + cdQ, tmem + cdS + ks * 8, mnmajor_desc(sK(st), ks), id_g,
+                              (j > itm.lo || ks > 0));
+            commit(&hdr->free2);
+            commit(&hdr->empty[st]);
+          }
         }
         if (!ok) break;
-        commit(&hdr->fixed_empty);
-        commit(&hdr->acc_full);
+        commit(scores ? &hdr->fixed_empty : &hdr->acc_full);
       }
-      commit(&hdr->mma_done);
-      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
+      const int me = scores ? 0 : 1;
+      commit(&hdr->mma_done[me]);
+      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[me]), 0u, 1000000000ull);
     }
   } else {
     // ------------------------------------------------------------ compute warps: one query row per thread
