@@ -438,8 +438,17 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   const float sl2 = scale * kLog2eB;
   auto item = [&](int w) {
     BwdItem it;
-    it.bh = w / nkb;
-    it.r0 = (w - it.bh * nkb) * kT;
+    // causal: key tiles with the most query blocks (the first ones) go first, all heads of a
+    // key tile together; non-causal: the key tiles of a head are adjacent (shared Q/dO in L2)
+    int kb;
+    if (CAUSAL) {
+      kb = w / BH;
+      it.bh = w - kb * BH;
+    } else {
+      it.bh = w / nkb;
+      kb = w - it.bh * nkb;
+    }
+    it.r0 = kb * kT;
     it.lo = CAUSAL ? min(it.r0 / kT, nqb) : 0;  // query blocks before the diagonal see no key here
     it.hi = nqb;
     return it;
