@@ -23,11 +23,14 @@ from ._binding import (  # noqa: F401
     fa_decode_static,
     fa_decode_workspace_bytes,
     fa_fwd,
+    fa_fwd_workspace_bytes,
+    fa_fwd_ws,
     fa_last_error_message,
     fa_last_status,
     fa_set_wait_budget_ns,
     fa_status_string,
     forward,
+    forward_workspace,
     lib,
     split_workspace,
 )

@@ -24,6 +24,8 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 # every symbol include/fa.h declares
 EXPORTS = (
     "fa_fwd",
+    "fa_fwd_ws",
+    "fa_fwd_workspace_bytes",
     "fa_bwd",
     "fa_bwd_workspace_bytes",
     "fa_decode",
@@ -58,6 +60,10 @@ def lib() -> ctypes.CDLL:
     vp, i, f, st = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int
     L.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     L.fa_fwd.restype = st
+    L.fa_fwd_ws.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_ws.restype = st
+    L.fa_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    L.fa_fwd_workspace_bytes.restype = ctypes.c_size_t
     L.fa_bwd.argtypes = [vp] * 10 + [i, i, i, i, i, f, i, i, vp]
     L.fa_bwd.restype = st
     L.fa_decode.argtypes = [vp] * 5 + [i, i, i, i, f, i, i, vp]
@@ -101,6 +107,15 @@ def _stream(s) -> Optional[int]:
 def fa_fwd(Q, K, V, O, LSE, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
     return lib().fa_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, H, M, N, D, float(scale), int(causal),
                         int(dtype), _stream(stream))
+
+def fa_fwd_ws(Q, K, V, O, LSE, workspace, workspace_bytes, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
+    return lib().fa_fwd_ws(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(workspace), int(workspace_bytes), B, H,
+                           M, N, D, float(scale), int(causal), int(dtype), _stream(stream))
+
+
+def fa_fwd_workspace_bytes(B, H, M, N, D, causal, dtype) -> int:
+    return lib().fa_fwd_workspace_bytes(B, H, M, N, D, int(causal), int(dtype))
+
 
 
 def fa_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
@@ -163,8 +178,28 @@ def _dims4(t, name):
     return t.shape
 
 
-def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, stream=None):
-    """O, LSE = attention(q [B,H,M,D], k/v [B,H,N,D]); LSE is float32 [B,H,M]."""
+_fwd_workspaces = {}  # device index -> zero-filled uint8 tensor (grown on demand)
+
+
+def forward_workspace(device, nbytes: int):
+    """A zero-filled device buffer of at least nbytes for fa_fwd_ws, kept per device and
+    reused by later calls (they run in stream order on one stream; two streams calling
+    forward at once would need a workspace each)."""
+    import torch
+    dev = torch.device(device)
+    idx = dev.index if dev.index is not None else torch.cuda.current_device()
+    ws = _fwd_workspaces.get(idx)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 16), dtype=torch.uint8, device=f"cuda:{idx}")
+        _fwd_workspaces[idx] = ws
+    return ws
+
+
+def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, stream=None, workspace=None):
+    """O, LSE = attention(q [B,H,M,D], k/v [B,H,N,D]); LSE is float32 [B,H,M].
+
+    workspace: None uses a cached per-device workspace (see forward_workspace); False
+    runs without one (fa_fwd); a zero-initialised uint8 tensor is used as given."""
     import torch
     B, H, M, D = _dims4(q, "q")
     N = _dims4(k, "k")[2]
@@ -172,7 +207,14 @@ def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, str
         out = torch.empty_like(q)
     if lse is None:
         lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
-    _check(fa_fwd(q, k, v, out, lse, B, H, M, N, D, scale, causal, fa_dtype(q), stream), "fa_fwd")
+    dt = fa_dtype(q)
+    nbytes = fa_fwd_workspace_bytes(B, H, M, N, D, causal, dt) if workspace is not False else 0
+    if nbytes == 0:
+        _check(fa_fwd(q, k, v, out, lse, B, H, M, N, D, scale, causal, dt, stream), "fa_fwd")
+        return out, lse
+    ws = forward_workspace(q.device, nbytes) if workspace is None else workspace
+    _check(fa_fwd_ws(q, k, v, out, lse, ws, ws.numel() * ws.element_size(), B, H, M, N, D, scale, causal, dt, stream),
+           "fa_fwd_ws")
     return out, lse
 
 

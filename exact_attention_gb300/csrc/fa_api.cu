@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/fa.h"
@@ -173,6 +174,69 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner,
 
 using namespace fa;
 
+namespace {
+
+// Whether a forward call with a workspace runs the split schedule (D = 64 halves,
+// non-causal). FA_FWD_SPLIT=0 / 1 forces it off / on (tests use it); by default it is
+// used when whole pairs would leave the last wave of CTAs less than 90 % full.
+bool split_capable(int D, int causal, int dtype) { return D == 64 && causal == 0 && dtype != FA_F32; }
+
+bool use_split(int BH, int M, int N, int num_sms) {
+  const long long pairs = static_cast<long long>(BH) * ((M + 255) / 256);
+  const long long units = pairs * ((N + 127) / 128);
+  if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
+  if (const char* e = std::getenv("FA_FWD_SPLIT")) {
+    if (e[0] == '0') return false;
+    if (e[0] == '1') return true;
+  }
+  if (units < 4ll * num_sms) return false;
+  const long long rounds = (pairs + num_sms - 1) / num_sms;
+  return pairs * 10 < rounds * num_sms * 9;
+}
+
+std::atomic<uint32_t> g_epoch{0};
+
+fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, void* ws, size_t ws_bytes, int B,
+                   int H, int M, int N, int D, float scale, int causal, fa_dtype dtype, void* stream,
+                   const char* name) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, M, N, D));
+  FA_TRY(check_scale(scale, true));
+  if (B * H == 0 || M == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  FA_TRY(check_ptr(Q, "Q"));
+  FA_TRY(check_ptr(K, "K"));
+  FA_TRY(check_ptr(V, "V"));
+  FA_TRY(check_ptr(O, "O"));
+  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return fail(FA_ERR_INVALID, "LSE misaligned");
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  FwdSplit sp{};
+  if (ws != nullptr && split_capable(D, causal, dtype)) {
+    FA_TRY(check_ptr(ws, "workspace"));
+    const size_t need = fwd_d64_split_bytes(ctx.num_sms);
+    if (ws_bytes < need) return fail(FA_ERR_INVALID, "%s: workspace of %zu bytes, %zu needed", name, ws_bytes, need);
+    if (use_split(B * H, M, N, ctx.num_sms)) {
+      sp.ws = static_cast<float*>(ws);
+      sp.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + need - ctx.num_sms * 8 * sizeof(uint32_t));
+      uint32_t ep = ++g_epoch;
+      if (ep == 0u) ep = ++g_epoch;  // 0 is what a fresh workspace holds
+      sp.epoch = ep;
+    }
+  }
+  cudaError_t e;
+  if (dtype == FA_F32)
+    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, ctx);
+  else
+    e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
+  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "%s: TMA descriptor rejected by the driver", name);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  return FA_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {
@@ -205,29 +269,23 @@ size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits) {
   return static_cast<size_t>(B) * H * n_splits * (D + 2) * sizeof(float);
 }
 
+size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype) {
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || !split_capable(D, causal, dtype)) return 0;
+  DevState* st = nullptr;
+  if (device_state(&st) != FA_OK) return 0;
+  return fwd_d64_split_bytes(st->num_sms);
+}
+
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int M, int N, int D,
                  float scale, int causal, fa_dtype dtype, void* stream) {
-  FA_TRY(check_dtype(dtype));
-  FA_TRY(check_sizes(B, H, M, N, D));
-  FA_TRY(check_scale(scale, true));
-  if (B * H == 0 || M == 0) return FA_OK;
-  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
-  FA_TRY(check_ptr(Q, "Q"));
-  FA_TRY(check_ptr(K, "K"));
-  FA_TRY(check_ptr(V, "V"));
-  FA_TRY(check_ptr(O, "O"));
-  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return fail(FA_ERR_INVALID, "LSE misaligned");
-  LaunchCtx ctx{};
-  FA_TRY(make_ctx(&ctx, stream));
-  cudaError_t e;
-  if (dtype == FA_F32)
-    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, ctx);
-  else
-    e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, ctx);
-  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_fwd: configuration not supported");
-  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "fa_fwd: TMA descriptor rejected by the driver");
-  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd launch");
-  return FA_OK;
+  return fwd_impl(Q, K, V, O, LSE, nullptr, 0, B, H, M, N, D, scale, causal, dtype, stream, "fa_fwd");
+}
+
+fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE, void* workspace,
+                    size_t workspace_bytes, int B, int H, int M, int N, int D, float scale, int causal, fa_dtype dtype,
+                    void* stream) {
+  return fwd_impl(Q, K, V, O, LSE, workspace, workspace_bytes, B, H, M, N, D, scale, causal, dtype, stream,
+                  "fa_fwd_ws");
 }
 
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,

@@ -45,12 +45,21 @@ struct LaunchCtx {
 cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N, int D,
                           float scale, int n_splits, int dtype, const LaunchCtx& ctx);
 
-cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                            int D, float scale, bool causal, int dtype, const LaunchCtx& ctx);
-
+// Split schedule of the D = 64 forward (non-causal): the caller's workspace holds one
+// partial-result slot and 8 ready flags per SM; ws == nullptr selects the classic schedule.
+// epoch is unique per launch (flags from earlier launches never match it).
+struct FwdSplit {
+  float* ws = nullptr;
+  uint32_t* flags = nullptr;
+  uint32_t epoch = 0;
+};
+size_t fwd_d64_split_bytes(int num_sms);
 // head dimension 64 only (fp16 / bf16); called by launch_fwd_half
 cudaError_t launch_fwd_d64(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                           float scale, bool causal, int dtype, const LaunchCtx& ctx);
+                           float scale, bool causal, int dtype, const FwdSplit& sp, const LaunchCtx& ctx);
+cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
+                            int D, float scale, bool causal, int dtype, const FwdSplit& sp, const LaunchCtx& ctx);
+
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                            int D, float scale, bool causal, const LaunchCtx& ctx);
 

@@ -68,8 +68,74 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // tensor-memory columns
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 
+// Partial result of a piece (see Schedule), one slot per CTA: O (unnormalised,
+// 256 rows x 64 columns), the running maximum (log2 units), the rounded and the
+// exact weight sums, f32; plus one ready flag per softmax warp.
+constexpr int kPairRows = 2 * kBM;
+constexpr int kSlotFloats = kPairRows * kD + 3 * kPairRows;
+
+// A CTA's unit of work: tile t of pair `pair` processes key blocks [jb, jb + nb_t).
+struct Piece {
+  int pair, bh, q0, jb, nb0, nb1;
+  int kind;  // 0: the whole pair; 1: its first blocks, finished here together with the partials of
+             // the CTAs that took the rest; 2: later blocks, written out as a partial
+};
+
+// Which pieces a CTA takes. Classic: whole pairs blockIdx.x, +gridDim.x, ... (tile_info
+// order). Split (non-causal only): the contiguous range [c U / G, (c+1) U / G) of the
+// U = pairs x key-blocks units (U < 2^31, checked by the host), so every CTA does the same
+// number of blocks and no partial last wave is left; a pair cut by a range boundary is
+// finished by the CTA that holds its first block, which processes that piece last, while
+// the CTAs holding the rest process theirs first.
+template <bool CAUSAL>
+struct Schedule {
+  uint32_t u, e;  // split: the remaining unit range; classic: u = next pair, e = pair count
+  __device__ static uint32_t start(uint32_t c, uint32_t units) {
+    return static_cast<uint32_t>(static_cast<uint64_t>(c) * units / gridDim.x);
+  }
+  __device__ Schedule(bool split, int BH, int num_pairs, int nkb) {
+    if (split) {
+      const uint32_t units = static_cast<uint32_t>(BH * num_pairs * nkb);
+      u = start(blockIdx.x, units);
+      e = start(blockIdx.x + 1, units);
+    } else {
+      u = blockIdx.x;
+      e = static_cast<uint32_t>(BH * num_pairs);
+    }
+  }
+  __device__ bool next(Piece& pc, bool split, int BH, int num_pairs, int nkb) {
+    if (u >= e) return false;
+    if (!split) {
+      const TileInfo ti = tile_info<CAUSAL>(static_cast<int>(u), BH, num_pairs, nkb);
+      pc.pair = static_cast<int>(u);
+      pc.bh = ti.bh;
+      pc.q0 = ti.q0;
+      pc.jb = 0;
+      pc.nb0 = ti.nb0;
+      pc.nb1 = ti.nb1;
+      pc.kind = 0;
+      u += gridDim.x;
+      return true;
+    }
+    const int p = static_cast<int>(u / nkb);
+    const int jb = static_cast<int>(u - static_cast<uint32_t>(p) * nkb);
+    const uint32_t left = e - u;
+    const int je = left < static_cast<uint32_t>(nkb - jb) ? jb + static_cast<int>(left) : nkb;
+    const TileInfo ti = tile_info<false>(p, BH, num_pairs, nkb);
+    pc.pair = p;
+    pc.bh = ti.bh;
+    pc.q0 = ti.q0;
+    pc.jb = jb;
+    pc.nb0 = pc.nb1 = je - jb;
+    pc.kind = (jb == 0 && je == nkb) ? 0 : (jb == 0 ? 1 : 2);
+    u += static_cast<uint32_t>(je - jb);
+    return true;
+  }
+};
+
 struct Hdr {
-  unsigned long long q_full[kQBuf], q_empty[kQBuf];       // q_empty: one commit per issuer
+  unsigned long long q_full[kQBuf], q_empty[kQBuf];       // q_empty: one arrival per tile (after its O store)
+  unsigned long long epi[2];  // tile t's 4 softmax warps have written their O rows into its Q buffer
   unsigned long long kv_full[kStages], kv_empty[kStages];  // kv_empty: one commit per issuer
   unsigned long long s_full[2];   // S_t(j) computed
   unsigned long long sm_a[2];     // softmax of tile t: first half of P_t(j) stored (4 warps)
@@ -85,8 +151,9 @@ struct Hdr {
 template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_d64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, void* __restrict__ Optr, float* __restrict__ LSE, int BH,
-                   int M, int N, float scale_log2, DevStatus* status, unsigned long long budget_ns) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, float* __restrict__ LSE, int BH,
+                   int M, int N, float scale_log2, float* __restrict__ ws, uint32_t* __restrict__ flags, uint32_t epoch,
+                   DevStatus* status, unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
   Hdr* hdr = reinterpret_cast<Hdr*>(smem_raw);
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
@@ -99,12 +166,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM);
   const int nkb = (N + kBN - 1) / kBN;
-  const int num_tiles = num_pairs * BH;
+  const bool split = !CAUSAL && ws != nullptr;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQBuf; ++i) {
       ptx::mbar_init(ptx::smem_u32(&hdr->q_full[i]), 1);
       ptx::mbar_init(ptx::smem_u32(&hdr->q_empty[i]), 2);
+      ptx::mbar_init(ptx::smem_u32(&hdr->epi[i]), 4);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&hdr->s_full[i]), 1);
@@ -143,8 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_it = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
-        const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
+      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+      Piece ti;
+      for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
         const int qb = it % kQBuf;
         const uint32_t qph = static_cast<uint32_t>(it / kQBuf) & 1u;
         if (!ptx::mbar_wait(ptx::smem_u32(&hdr->q_empty[qb]), qph ^ 1u, wc, 10)) break;
@@ -160,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t f = ptx::smem_u32(&hdr->kv_full[st]);
           ptx::mbar_arrive_expect_tx(f, 2 * kTile);
-          ptx::tma_load_3d(k_addr(st), &tmK, f, 0, j * kBN, ti.bh);
-          ptx::tma_load_3d(v_addr(st), &tmV, f, 0, j * kBN, ti.bh);
+          ptx::tma_load_3d(k_addr(st), &tmK, f, 0, (ti.jb + j) * kBN, ti.bh);
+          ptx::tma_load_3d(v_addr(st), &tmV, f, 0, (ti.jb + j) * kBN, ti.bh);
         }
       }
       if (hdr->abort_flag) {  // let issued copies land before shared memory is released
@@ -188,8 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dS = tmem + kColS + t * kBN;
       const uint32_t dO = tmem + kColO + t * kD;
       const uint32_t aP = tmem + kColP + t * (kBN / 2);
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
-        const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
+      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+      Piece ti;
+      for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
         const int qb = it % kQBuf;
         const int nb = t == 0 ? ti.nb0 : ti.nb1;
         if (!wait(&hdr->q_full[qb], static_cast<uint32_t>(it / kQBuf) & 1u, 20)) break;
@@ -207,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < kD / 16; ++ks) ptx::mma_f16_ss(dS, a0 + 2 * ks, b0 + 2 * ks, idesc_qk, ks > 0 ? 1u : 0u);
           commit(&hdr->s_full[t]);
-          if (j == nb - 1) commit(&hdr->q_empty[qb]);  // the tile's last S: Q_t no longer read
         };
         // O_t (+)= P_t(j) V_j over keys [64h, 64h + 64) of the block
         auto pv = [&](int j, int h) {
@@ -271,9 +340,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nblk = 0u;  // blocks processed by this tile slot (all pairs)
     uint32_t o_ph = 0u;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-      const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
+    Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+    Piece ti;
+    int it = 0;          // pieces taken (Q buffer = it % kQBuf)
+    uint32_t epi_ph = 0u;
+    const bool leader = wq == 0 && lane == 0;  // stores tile t's O and frees its Q buffer
+    for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
       const int nbt = t == 0 ? ti.nb0 : ti.nb1;
+      const int qb = it % kQBuf;
       const int row = ti.q0 + t * kBM + wq * 32 + lane;  // query index within the head
       float m2 = -INFINITY;  // running max of scale*log2(e)*s (stale by at most 2^8)
       float l = 0.f;         // sum of the half-rounded weights (normalises O)
@@ -294,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0 && (j > 0 || nbt > 1)) ptx::mbar_arrive(sm_b);
 
-        const int kbase = j * kBN;
+        const int kbase = (ti.jb + j) * kBN;
         if ((kbase + kBN > N) || (CAUSAL && kbase + kBN - 1 > ti.q0 + t * kBM)) {
 #pragma unroll
           for (int c = 0; c < kBN; c += 32) mask32<CAUSAL>(r + c, kbase + c, N, row);
@@ -389,32 +463,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       o_ph ^= 1u;
       ptx::tc_fence_after();
-      const float inv = 1.f / l;
-      const bool valid = row < M;
-      const size_t orow = (static_cast<size_t>(ti.bh) * M + (valid ? row : 0)) * kD;
+      // this thread's row of the unnormalised O
+      float oacc[kD];
 #pragma unroll
       for (int c = 0; c < kD; c += 32) {
         uint32_t o[32];
         ptx::tmem_ld32(tO + c, o);
         ptx::tmem_wait_ld32(o);
-        uint32_t h[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = __uint_as_float(o[2 * i]) * inv, b = __uint_as_float(o[2 * i + 1]) * inv;
-          h[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+        for (int i = 0; i < 32; ++i) oacc[c + i] = __uint_as_float(o[i]);
+      }
+      const int prow = t * kBM + wq * 32 + lane;  // row within the pair
+      // Frees the tile's Q buffer once its 4 warps are past their use of it (the leader waits
+      // for the other warps with a bounded wait; its store, if any, has then been issued).
+      auto release_q = [&](bool store) {
+        ptx::fence_proxy_async_smem();  // this warp's shared-memory writes -> the TMA engine
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->epi[t]));
+        if (leader) {
+          if (ptx::mbar_wait(ptx::smem_u32(&hdr->epi[t]), epi_ph, wc, 37)) {
+            if (store) {
+              ptx::tma_store_3d(&tmO, q_addr(qb, t), 0, ti.q0 + t * kBM, ti.bh);
+              ptx::bulk_commit();
+              ptx::bulk_wait_read();
+            }
+            ptx::mbar_arrive(ptx::smem_u32(&hdr->q_empty[qb]));
+          }
         }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(Optr) + orow + c);
+        epi_ph ^= 1u;
+      };
+      if (ti.kind == 2) {
+        // later blocks of a split pair: hand (O, m, l, le) to the CTA that holds its first block.
+        // Column-major, so a warp's 32 rows of one column are one contiguous 128-byte line.
+        float* slot = ws + static_cast<size_t>(blockIdx.x) * kSlotFloats;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+        for (int c = 0; c < kD; ++c) slot[c * kPairRows + prow] = oacc[c];
+        slot[kPairRows * kD + prow] = m2;
+        slot[kPairRows * kD + kPairRows + prow] = l;
+        slot[kPairRows * kD + 2 * kPairRows + prow] = le;
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + warp, epoch);
+        release_q(false);
+        ptx::tc_fence_before();
+        continue;
+      }
+      if (ti.kind == 1) {
+        // first blocks of a split pair: merge the partials of the CTAs that took the rest
+        // (they processed those pieces first, so they are normally long ready)
+        const uint32_t units = static_cast<uint32_t>(BH * num_pairs * nkb);
+        const uint32_t end_u = static_cast<uint32_t>(ti.pair + 1) * static_cast<uint32_t>(nkb);
+        for (uint32_t c2 = blockIdx.x + 1; c2 < gridDim.x && Schedule<CAUSAL>::start(c2, units) < end_u && ok; ++c2) {
+          // a CTA with an empty range (more CTAs than units) writes no partial
+          if (Schedule<CAUSAL>::start(c2 + 1, units) == Schedule<CAUSAL>::start(c2, units)) continue;
+          uint32_t* f = flags + static_cast<size_t>(c2) * 8 + warp;
+          bool got = true;
+          if (lane == 0) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            got = false;
+            for (uint32_t k = 0; k < (1u << 30); ++k) {
+              if (ptx::ld_acquire_u32(f) == epoch) {
+                got = true;
+                break;
+              }
+              if ((k & 255u) == 255u && (*wc.abort_flag || ptx::globaltimer_ns() - t0 > wc.budget_ns)) break;
+            }
+            if (!got) ptx::raise_error(wc, kStatusTimeout, 36);
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, got, 0);
+          if (!ok) break;
+          (void)ptx::ld_acquire_u32(f);  // orders this lane's reads of the slot after the flag
+          const float* slot = ws + static_cast<size_t>(c2) * kSlotFloats;
+          const float m_p = slot[kPairRows * kD + prow];
+          const float l_p = slot[kPairRows * kD + kPairRows + prow];
+          const float le_p = slot[kPairRows * kD + 2 * kPairRows + prow];
+          const float mn = fmaxf(m2, m_p);
+          const float a = ptx::ex2(m2 - mn), b = ptx::ex2(m_p - mn);
+#pragma unroll
+          for (int c = 0; c < kD; ++c) oacc[c] = oacc[c] * a + slot[c * kPairRows + prow] * b;
+          l = l * a + l_p * b;
+          le = le * a + le_p * b;
+          m2 = mn;
+        }
+        if (!ok) break;
+      }
+      // O = acc / l into the tile's Q buffer (its last S has completed before O was final) in the
+      // tensor map's 128-byte swizzled layout, then one TMA store per tile (rows past M are
+      // clipped by the tensor map)
+      const float inv = 1.f / l;
+      {
+        const int r = wq * 32 + lane;  // row within the tile
+        uint8_t* buf = smem_raw + (q_addr(qb, t) - raw_u32);
+#pragma unroll
+        for (int v = 0; v < kD / 8; ++v) {
+          uint32_t h[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float a = oacc[8 * v + 2 * i] * inv, b = oacc[8 * v + 2 * i + 1] * inv;
+            h[i] = BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
+          }
+          *reinterpret_cast<uint4*>(buf + r * 128 + ((v ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
         }
       }
-      if (valid && LSE != nullptr) LSE[static_cast<size_t>(ti.bh) * M + row] = (m2 + __log2f(le)) * kLn2;
+      if (row < M && LSE != nullptr) LSE[static_cast<size_t>(ti.bh) * M + row] = (m2 + __log2f(le)) * kLn2;
+      release_q(true);
       // O_t is read: the next pair's first P V may overwrite it (ordered by the next sm_a arrive)
       ptx::tc_fence_before();
     }
   }
 
+  if (warp < 8 && (warp & 3) == 0 && lane == 0) ptx::bulk_wait_all();  // this tile's O stores completed
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
@@ -425,31 +583,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool BF16, bool CAUSAL>
-cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* O, float* LSE,
-                     int BH, int M, int N, float scale, const LaunchCtx& ctx) {
+cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, float* LSE,
+                     int BH, int M, int N, float scale, const FwdSplit& sp, const LaunchCtx& ctx) {
   auto kern = fwd_d64_kernel<BF16, CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>((M + 2 * kBM - 1) / (2 * kBM)) * BH;
+  if (!CAUSAL && sp.ws != nullptr) {
+    // split schedule: every SM holds one CTA for the whole launch, and a CTA may wait for the
+    // partials of later CTAs, so all of them must be resident at once (cooperative launch)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(ctx.num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, BH, M, N, scale * kLog2e, sp.ws, sp.flags, sp.epoch,
+                              ctx.status, ctx.wait_budget_ns);
+  }
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
-  kern<<<grid, kThreads, kSmemBytes, ctx.stream>>>(mq, mk, mv, O, LSE, BH, M, N, scale * kLog2e, ctx.status,
-                                                   ctx.wait_budget_ns);
+  kern<<<grid, kThreads, kSmemBytes, ctx.stream>>>(mq, mk, mv, mo, LSE, BH, M, N, scale * kLog2e, nullptr, nullptr, 0u,
+                                                   ctx.status, ctx.wait_budget_ns);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+size_t fwd_d64_split_bytes(int num_sms) {
+  return static_cast<size_t>(num_sms) * (kSlotFloats * sizeof(float) + 8 * sizeof(uint32_t));
+}
+
 cudaError_t launch_fwd_d64(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                           float scale, bool causal, int dtype, const LaunchCtx& ctx) {
-  CUtensorMap mq, mk, mv;
+                           float scale, bool causal, int dtype, const FwdSplit& sp, const LaunchCtx& ctx) {
+  CUtensorMap mq, mk, mv, mo;
   if (!make_tmap_3d(&mq, Q, dtype, kD, M, BH, 64, kBM) || !make_tmap_3d(&mk, K, dtype, kD, N, BH, 64, kBN) ||
-      !make_tmap_3d(&mv, V, dtype, kD, N, BH, 64, kBN))
+      !make_tmap_3d(&mv, V, dtype, kD, N, BH, 64, kBN) || !make_tmap_3d(&mo, O, dtype, kD, M, BH, 64, kBM))
     return cudaErrorInvalidValue;
   const bool bf = dtype == kBF16;
-  if (bf) return causal ? launch_t<true, true>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx)
-                        : launch_t<true, false>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx);
-  return causal ? launch_t<false, true>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx)
-                : launch_t<false, false>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx);
+  if (bf) return causal ? launch_t<true, true>(mq, mk, mv, mo, LSE, BH, M, N, scale, sp, ctx)
+                        : launch_t<true, false>(mq, mk, mv, mo, LSE, BH, M, N, scale, sp, ctx);
+  return causal ? launch_t<false, true>(mq, mk, mv, mo, LSE, BH, M, N, scale, sp, ctx)
+                : launch_t<false, false>(mq, mk, mv, mo, LSE, BH, M, N, scale, sp, ctx);
 }
 
 }  // namespace fa

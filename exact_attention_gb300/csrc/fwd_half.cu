@@ -459,8 +459,8 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
 }  // namespace
 
 cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                            int D, float scale, bool causal, int dtype, const LaunchCtx& ctx) {
-  if (D == 64) return launch_fwd_d64(Q, K, V, O, LSE, BH, M, N, scale, causal, dtype, ctx);
+                            int D, float scale, bool causal, int dtype, const FwdSplit& sp, const LaunchCtx& ctx) {
+  if (D == 64) return launch_fwd_d64(Q, K, V, O, LSE, BH, M, N, scale, causal, dtype, sp, ctx);
   if (D != 128) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   if (!make_tmap_3d(&mq, Q, dtype, D, M, BH, 64, kBM) || !make_tmap_3d(&mk, K, dtype, D, N, BH, 64, kBN) ||

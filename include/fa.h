@@ -66,6 +66,41 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
                  int D, float scale, int causal, fa_dtype dtype, void* stream);
 
 /*
+ * Bytes of device workspace fa_fwd_ws can use for this problem on the current
+ * device: nonzero only for fp16/bf16 with D = 64 and causal == 0, where it is one
+ * partial-result slot (a 256x64 f32 block and three 256-float statistics) plus
+ * eight 32-bit flags per SM. 0 on bad sizes or when no device is usable.
+ */
+size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype);
+
+/*
+ * fa_fwd with a caller-owned workspace; same arguments, same results.
+ *
+ * The pages' forward gives each CTA whole blocks of query rows. When the number
+ * of 256-row query pairs does not fill the last wave of SMs, this call instead
+ * gives every SM an equal contiguous share of (query pair, key block) work; a
+ * pair whose key blocks are shared by two or more SMs is merged at the end by the
+ * SM holding its first blocks, with the same (m, l) rescaling the online softmax
+ * uses between key blocks. The merge waits on flags written by other SMs, so the
+ * kernel is launched cooperatively (all CTAs resident at once).
+ *
+ *   workspace        device pointer, 16-byte aligned, at least
+ *                    fa_fwd_workspace_bytes(...) bytes, or NULL (then this is
+ *                    fa_fwd). Zero-filled by the caller before its first use;
+ *                    afterwards the library leaves it in a reusable state.
+ *                    Owned by the caller; two calls must not use the same
+ *                    workspace at the same time.
+ *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
+ *
+ * The split is used when the last wave would be less than 90 % full and every SM
+ * gets at least four key blocks; FA_FWD_SPLIT=0 or 1 in the environment turns it
+ * off or on regardless.
+ */
+fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE, void* workspace,
+                    size_t workspace_bytes, int B, int H, int M, int N, int D, float scale, int causal, fa_dtype dtype,
+                    void* stream);
+
+/*
  * Backward pass: gradients of sum(dO o O).
  *
  * Follows "06: Fused attention" (attn_bwd_delta, attn_bwd_dkdv, attn_bwd_dq)

@@ -137,3 +137,31 @@ def test_forward_f32_head_dim_128_is_unsupported():
     import torch
     q = torch.zeros((1, 1, 8, 128), dtype=torch.float32, device="cuda")
     assert fa.fa_fwd(q, q, q, q, None, 1, 1, 8, 8, 128, 0.1, 0, fa.FA_F32) == fa.FA_ERR_UNSUPPORTED
+
+
+SPLIT_SHAPES = [
+    # B, H, M, N
+    (1, 1, 256, 384),    # one pair cut into one-block pieces; most CTAs get no work
+    (2, 3, 300, 200),    # ragged M and N
+    (1, 2, 1024, 1024),  # 8 pairs x 8 key blocks spread over all SMs
+    (3, 5, 700, 1500),   # pieces crossing pair boundaries, ragged tails
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("B,H,M,N", SPLIT_SHAPES)
+def test_forward_split_schedule_matches_oracle(monkeypatch, dtype, B, H, M, N):
+    """The split schedule (each SM an equal share of (query pair, key block) units, cut
+    pairs merged with the online-softmax rescaling) forced on."""
+    monkeypatch.setenv("FA_FWD_SPLIT", "1")
+    scale = 0.125
+    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, False, scale, seed=M + N)
+    check_heads(inputs, out, lse, dtype, False, scale)
+
+
+def test_forward_split_schedule_repeated_calls(monkeypatch):
+    """Back-to-back calls reuse one workspace; each launch's flags carry a new epoch."""
+    monkeypatch.setenv("FA_FWD_SPLIT", "1")
+    for seed in (1, 2, 3):
+        inputs, out, lse = run_fwd(1, 3, 512, 640, 64, "f16", False, 0.125, seed=seed)
+        check_heads(inputs, out, lse, "f16", False, 0.125)
