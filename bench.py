@@ -243,13 +243,17 @@ def run_ours(args):
     ws = torch.empty(fa.fa_decode_workspace_bytes(d["B"], d["H"], d["D"], d["n_splits"]) // 4,
                      dtype=torch.float32, device="cuda")
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    # forward workspace (split schedule), zero-filled once as fa_fwd_ws requires
+    fws_bytes = fa.fa_fwd_workspace_bytes(*BHMND, c["causal"], fa.FA_F16)
+    fws = torch.zeros(max(fws_bytes, 16), dtype=torch.uint8, device="cuda")
 
     def check(s, what):
         if s != fa.FA_OK:
             raise RuntimeError(f"{what}: {fa.fa_status_string(s)}: {fa.fa_last_error_message()}")
 
     def run_fwd():
-        check(fa.fa_fwd(qd, kd, vd, od, lse, *BHMND, c["scale"], c["causal"], fa.FA_F16, stream), "fa_fwd")
+        check(fa.fa_fwd_ws(qd, kd, vd, od, lse, fws if fws_bytes else None, fws_bytes, *BHMND, c["scale"], c["causal"],
+                           fa.FA_F16, stream), "fa_fwd_ws")
 
     have_bwd = True
 
