@@ -377,6 +377,39 @@ def run_ours(args):
 
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    # ---- f32 forward on its own (one head, M=N=4096, D=64, 3xTF32), L2 flushed before each call
+    f32 = None
+    if world == 1:
+        q32, k32, v32 = synth.attention_inputs(1, 1, 4096, 4096, 64, "f32", seed=0)
+        q32, k32, v32 = (torch.from_numpy(x).to("cuda") for x in (q32, k32, v32))
+        o32 = torch.empty_like(q32)
+        l32 = torch.empty((1, 1, 4096), dtype=torch.float32, device="cuda")
+
+        def run_f32():
+            check(fa.fa_fwd(q32, k32, v32, o32, l32, 1, 1, 4096, 4096, 64, 0.125, 0, fa.FA_F32, stream), "fa_fwd f32")
+
+        for _ in range(3):
+            run_f32()
+        recs32 = []
+        for _ in range(30):
+            flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            run_f32()
+            b.record(stream)
+            recs32.append((a, b))
+        torch.cuda.synchronize()
+        check(fa.fa_last_status(stream), "f32 forward")
+        t32 = sum(a.elapsed_time(b) for a, b in recs32) / len(recs32) / 1e3
+        tf32 = 4.0 * 4096 * 4096 * 64 / t32 / 1e12
+        peak32 = peak_tf * 1.1 / 2.25 / 3.0
+        f32 = {"config": "f32 forward, 1 head, M=N=4096, D=64, scale 0.125 (3xTF32)", "value": round(tf32, 2),
+               "unit": "TFLOP/s", "us_per_call": round(t32 * 1e6, 1),
+               "roofline": {"kernel": "fwd_f32_kernel<non-causal>", "bound": "tensor", "achieved": round(tf32, 2),
+                            "peak": round(peak32, 1), "unit": "TFLOP/s", "frac": round(tf32 / peak32, 4),
+                            "peak_source": f"{peaks_src} bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products",
+                            "traffic": None}}
+
     launches_per_step = 1 + (3 if have_bwd else 0) + 2
     traffic = load_traffic()
     line = {
@@ -429,6 +462,7 @@ def run_ours(args):
             },
             "e2e": dec_e2e,
         },
+        "f32": f32,
         "backward": None if bwd_tflops is None else {
             "value": round(bwd_tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(t_bwd / K * 1e3, 4),
             "flops": "2.5 x forward"},

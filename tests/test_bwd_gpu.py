@@ -77,3 +77,11 @@ def test_backward_gradient_identities():
     do = f64(inputs[3], "f16")
     assert np.max(np.abs(dk.sum(axis=2))) < 0.05
     assert np.max(np.abs(dv.sum(axis=2) - do.sum(axis=2))) < 0.05
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_full_workload_sampled_heads(causal):
+    """B4 H12 M=N=2048 D64 fp16 (the measured workload): every gradient entry of three heads
+    spread over the batch against the oracle."""
+    inputs, o, grads, delta = run_bwd(4, 12, 2048, 2048, 64, "f16", causal, 0.125, seed=5)
+    check(inputs, o, grads, delta, "f16", causal, 0.125, heads=[(0, 0), (1, 7), (3, 11)])
