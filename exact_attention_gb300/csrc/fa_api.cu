@@ -224,9 +224,18 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
       sp.epoch = ep;
     }
   }
+  int parts = 1;
+  if (dtype == FA_F32 && ws != nullptr && D == 64) {
+    parts = fwd_f32_parts(B * H, M, N, ctx.num_sms);
+    const size_t need = fwd_f32_split_bytes(B * H, M, parts);
+    if (parts > 1) {
+      FA_TRY(check_ptr(ws, "workspace"));
+      if (ws_bytes < need) return fail(FA_ERR_INVALID, "%s: workspace of %zu bytes, %zu needed", name, ws_bytes, need);
+    }
+  }
   cudaError_t e;
   if (dtype == FA_F32)
-    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, ctx);
+    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, parts, static_cast<float*>(ws), ctx);
   else
     e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
@@ -270,9 +279,11 @@ size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits) {
 }
 
 size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype) {
-  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || !split_capable(D, causal, dtype)) return 0;
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return 0;
   DevState* st = nullptr;
   if (device_state(&st) != FA_OK) return 0;
+  if (dtype == FA_F32 && D == 64) return fwd_f32_split_bytes(B * H, M, fwd_f32_parts(B * H, M, N, st->num_sms));
+  if (!split_capable(D, causal, dtype)) return 0;
   return fwd_d64_split_bytes(st->num_sms);
 }
 

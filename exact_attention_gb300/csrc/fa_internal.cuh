@@ -60,8 +60,12 @@ cudaError_t launch_fwd_d64(const void* Q, const void* K, const void* V, void* O,
 cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                             int D, float scale, bool causal, int dtype, const FwdSplit& sp, const LaunchCtx& ctx);
 
+// f32 forward; with few query tiles (under half the SMs) each tile's key blocks are shared by
+// `parts` CTAs whose partials a second launch merges (ws: fwd_f32_split_bytes floats' worth).
+int fwd_f32_parts(int BH, int M, int N, int num_sms);
+size_t fwd_f32_split_bytes(int BH, int M, int parts);
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                           int D, float scale, bool causal, const LaunchCtx& ctx);
+                           int D, float scale, bool causal, int parts, float* ws, const LaunchCtx& ctx);
 
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                        void* dQ, void* dK, void* dV, float* delta, int BH, int M, int N, int D, float scale,

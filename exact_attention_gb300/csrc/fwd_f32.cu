@@ -45,6 +45,7 @@ constexpr int kThreads32 = 320;     // softmax 0-3, split 4-7, producer 8, MMA 9
 constexpr int kWarpProd32 = 8, kWarpMma32 = 9;
 constexpr float kLog2e32 = 1.4426950408889634f;
 constexpr float kLn2_32 = 0.6931471805599453f;
+constexpr int kF32Slot = kD32 * 128 + 2 * 128;  // one part's partial: O [64][128 rows], m, l
 
 struct F32Hdr {
   unsigned long long q_full, q_split, q_empty;
@@ -103,7 +104,8 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads32, 1)
     fwd_f32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, float* __restrict__ O, float* __restrict__ LSE, int BH,
-                   int M, int N, float scale_log2, DevStatus* status, unsigned long long budget_ns) {
+                   int M, int N, float scale_log2, int parts, float* __restrict__ ws, DevStatus* status,
+                   unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
   F32Hdr* hdr = reinterpret_cast<F32Hdr*>(smem_raw);
   const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -121,12 +123,19 @@ __global__ void __launch_bounds__(kThreads32, 1)
   const int nkb = (N + kBN32 - 1) / kBN32;
   const int tiles = BH * nqt;
 
-  auto tile_of = [&](int w, int& bh, int& q0, int& nb) {
-    const int qt_rev = w / BH;
-    bh = w - qt_rev * BH;
+  // Unit w = (tile w / parts, part w % parts): the tile's key blocks [jb, jb + nb) of its part.
+  // With parts > 1 each part leaves an unnormalised partial that fwd_f32_combine merges;
+  // empty parts (causal tiles with fewer blocks than parts) are skipped by every role.
+  const int units = tiles * parts;
+  auto tile_of = [&](int w, int& bh, int& q0, int& jb, int& nb) {
+    const int tile = w / parts, part = w - tile * parts;
+    const int qt_rev = tile / BH;
+    bh = tile - qt_rev * BH;
     const int qt = CAUSAL ? nqt - 1 - qt_rev : qt_rev;  // causal: heaviest tiles first
     q0 = qt * kBM32;
-    nb = CAUSAL ? min(nkb, (q0 + kBM32 - 1) / kBN32 + 1) : nkb;
+    const int nbt = CAUSAL ? min(nkb, (q0 + kBM32 - 1) / kBN32 + 1) : nkb;
+    jb = part * nbt / parts;
+    nb = (part + 1) * nbt / parts - jb;
   };
 
   if (threadIdx.x == 0) {
@@ -161,10 +170,12 @@ __global__ void __launch_bounds__(kThreads32, 1)
       uint32_t it = 0;
       int n = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < tiles && ok; w += gridDim.x, ++n) {
-        int bh, q0, nb;
-        tile_of(w, bh, q0, nb);
+      for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+        int bh, q0, jb, nb;
+        tile_of(w, bh, q0, jb, nb);
+        if (nb == 0) continue;
         if (!ptx::mbar_wait(ptx::smem_u32(&hdr->q_empty), (n & 1) ^ 1, wc, 10)) break;
+        ++n;
         const uint32_t qf = ptx::smem_u32(&hdr->q_full);
         ptx::mbar_arrive_expect_tx(qf, kQBytes);
         for (int c = 0; c < 2; ++c) ptx::tma_load_3d(sQh + c * kQChunk, &tmQ, qf, c * 32, q0, bh);
@@ -177,8 +188,8 @@ __global__ void __launch_bounds__(kThreads32, 1)
           const uint32_t f = ptx::smem_u32(&hdr->kv_full[st]);
           ptx::mbar_arrive_expect_tx(f, 2 * kKBytes);
           for (int c = 0; c < 2; ++c) {
-            ptx::tma_load_3d(sKh(st) + c * kKChunk, &tmK, f, c * 32, j * kBN32, bh);
-            ptx::tma_load_3d(sV(st) + c * kKChunk, &tmV, f, c * 32, j * kBN32, bh);
+            ptx::tma_load_3d(sKh(st) + c * kKChunk, &tmK, f, c * 32, (jb + j) * kBN32, bh);
+            ptx::tma_load_3d(sV(st) + c * kKChunk, &tmV, f, c * 32, (jb + j) * kBN32, bh);
           }
         }
       }
@@ -189,10 +200,12 @@ __global__ void __launch_bounds__(kThreads32, 1)
     uint32_t it = 0;
     int n = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < tiles && ok; w += gridDim.x, ++n) {
-      int bh, q0, nb;
-      tile_of(w, bh, q0, nb);
+    for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+      int bh, q0, jb, nb;
+      tile_of(w, bh, q0, jb, nb);
+      if (nb == 0) continue;
       ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(&hdr->q_full), n & 1, wc, 40));
+      ++n;
       if (!ok) break;
       split_block(gen(sQh), gen(sQl), kQBytes / 16, tid, 128);
       ptx::fence_proxy_async_smem();  // generic stores -> tensor-core reads
@@ -222,10 +235,12 @@ __global__ void __launch_bounds__(kThreads32, 1)
       auto kdesc = [](uint32_t base, uint32_t chunk, int ks) {
         return ptx::sdesc_sw128(base + (ks >> 2) * chunk + (ks & 3) * 32, 16, 1024);
       };
-      for (int w = blockIdx.x; w < tiles && ok; w += gridDim.x, ++n) {
-        int bh, q0, nb;
-        tile_of(w, bh, q0, nb);
+      for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+        int bh, q0, jb, nb;
+        tile_of(w, bh, q0, jb, nb);
+        if (nb == 0) continue;
         if (!ptx::mbar_wait(ptx::smem_u32(&hdr->q_split), n & 1, wc, 20)) break;
+        ++n;
         ptx::tc_fence_after();
         for (int j = 0; j < nb; ++j, ++it) {
           const int st = it % kStages32;
@@ -271,9 +286,10 @@ __global__ void __launch_bounds__(kThreads32, 1)
     uint32_t s_ph = 0;
     int n = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < tiles && ok; w += gridDim.x, ++n) {
-      int bh, q0, nb;
-      tile_of(w, bh, q0, nb);
+    for (int w = blockIdx.x; w < units && ok; w += gridDim.x) {
+      int bh, q0, jb, nb;
+      tile_of(w, bh, q0, jb, nb);
+      if (nb == 0) continue;
       const int row = q0 + warp * 32 + lane;
       float m2 = -INFINITY, l = 0.f;
       float oacc[kD32];
@@ -297,7 +313,7 @@ __global__ void __launch_bounds__(kThreads32, 1)
         ptx::tc_fence_after();
         // S(j) complete implies P V of block j-1 complete (issued before it by the same thread)
         if (j > 0) add_partial();
-        const int k0 = j * kBN32;
+        const int k0 = (jb + j) * kBN32;
         const bool edge = k0 + kBN32 > N || (CAUSAL && k0 + kBN32 - 1 > q0);
         auto load_s = [&](int c, uint32_t* r) {
           ptx::tmem_ld32(tS + c, r);
@@ -351,8 +367,21 @@ __global__ void __launch_bounds__(kThreads32, 1)
       if (!ok) break;
       ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(&hdr->o_full), n & 1, wc, 31));
       if (!ok) break;
+      ++n;
       ptx::tc_fence_after();
       add_partial();
+      if (parts > 1) {
+        // unnormalised partial of this part, column-major (a warp's 32 rows of a column are
+        // one contiguous line): O [64][128], m [128], l [128]
+        float* slot = ws + static_cast<size_t>(w) * kF32Slot;
+        const int r = warp * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < kD32; ++c) slot[c * kBM32 + r] = oacc[c];
+        slot[kD32 * kBM32 + r] = m2;
+        slot[kD32 * kBM32 + kBM32 + r] = l;
+        ptx::tc_fence_before();
+        continue;
+      }
       const float inv = 1.f / l;
       const bool valid = row < M;
       const size_t g = static_cast<size_t>(bh) * M + (valid ? row : 0);
@@ -376,30 +405,90 @@ __global__ void __launch_bounds__(kThreads32, 1)
   }
 }
 
+// Merges the parts of each row: m = max_s m_s, w_s = 2^(m_s - m), O = sum_s w_s O_s / sum_s w_s l_s
+// (the online-softmax rescaling between key blocks), LSE = m + log sum_s w_s l_s. Empty parts
+// (no key blocks) wrote nothing and are skipped. One thread per (row, 4 columns).
+template <bool CAUSAL>
+__global__ void __launch_bounds__(256)
+    fwd_f32_combine(const float* __restrict__ ws, float* __restrict__ O, float* __restrict__ LSE, int BH, int M,
+                    int N, int parts) {
+  const long long gid = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);  // global row
+  const int c4 = threadIdx.x & 15;
+  if (gid >= static_cast<long long>(BH) * M) return;
+  const int bh = static_cast<int>(gid / M), row = static_cast<int>(gid - static_cast<long long>(bh) * M);
+  const int nqt = (M + kBM32 - 1) / kBM32, nkb = (N + kBN32 - 1) / kBN32;
+  const int qt = row / kBM32, r = row - qt * kBM32;
+  const int qt_rev = CAUSAL ? nqt - 1 - qt : qt;
+  const int tile = qt_rev * BH + bh;
+  const int nbt = CAUSAL ? min(nkb, (qt * kBM32 + kBM32 - 1) / kBN32 + 1) : nkb;
+  float m = -INFINITY;
+  for (int p = 0; p < parts; ++p) {
+    if ((p + 1) * nbt / parts == p * nbt / parts) continue;
+    const float* slot = ws + (static_cast<size_t>(tile) * parts + p) * kF32Slot;
+    m = fmaxf(m, slot[kD32 * kBM32 + r]);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lsum = 0.f;
+  for (int p = 0; p < parts; ++p) {
+    if ((p + 1) * nbt / parts == p * nbt / parts) continue;
+    const float* slot = ws + (static_cast<size_t>(tile) * parts + p) * kF32Slot;
+    const float wgt = ptx::ex2(slot[kD32 * kBM32 + r] - m);
+    lsum = fmaf(wgt, slot[kD32 * kBM32 + kBM32 + r], lsum);
+    acc.x = fmaf(wgt, slot[(4 * c4 + 0) * kBM32 + r], acc.x);
+    acc.y = fmaf(wgt, slot[(4 * c4 + 1) * kBM32 + r], acc.y);
+    acc.z = fmaf(wgt, slot[(4 * c4 + 2) * kBM32 + r], acc.z);
+    acc.w = fmaf(wgt, slot[(4 * c4 + 3) * kBM32 + r], acc.w);
+  }
+  const float inv = 1.f / lsum;
+  reinterpret_cast<float4*>(O + static_cast<size_t>(gid) * kD32)[c4] =
+      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (c4 == 0 && LSE != nullptr) LSE[gid] = (m + __log2f(lsum)) * kLn2_32;
+}
+
 template <bool CAUSAL>
 cudaError_t launch32(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* O, float* LSE, int BH,
-                     int M, int N, float scale, const LaunchCtx& ctx) {
+                     int M, int N, float scale, int parts, float* ws, const LaunchCtx& ctx) {
   auto kern = fwd_f32_kernel<CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem32);
   if (e != cudaSuccess) return e;
-  const long long tiles = static_cast<long long>((M + kBM32 - 1) / kBM32) * BH;
-  const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
+  const long long units = static_cast<long long>((M + kBM32 - 1) / kBM32) * BH * parts;
+  const int grid = static_cast<int>(units < ctx.num_sms ? units : ctx.num_sms);
   kern<<<grid, kThreads32, kSmem32, ctx.stream>>>(mq, mk, mv, static_cast<float*>(O), LSE, BH, M, N,
-                                                  scale * kLog2e32, ctx.status, ctx.wait_budget_ns);
+                                                  scale * kLog2e32, parts, ws, ctx.status, ctx.wait_budget_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || parts == 1) return e;
+  const long long rows = static_cast<long long>(BH) * M;
+  fwd_f32_combine<CAUSAL><<<static_cast<unsigned>((rows + 15) / 16), 256, 0, ctx.stream>>>(
+      ws, static_cast<float*>(O), LSE, BH, M, N, parts);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+int fwd_f32_parts(int BH, int M, int N, int num_sms) {
+  const long long tiles = static_cast<long long>((M + kBM32 - 1) / kBM32) * BH;
+  const int nkb = (N + kBN32 - 1) / kBN32;
+  if (tiles * 2 > num_sms || nkb < 4) return 1;  // enough tiles, or too few key blocks to share
+  long long parts = num_sms / tiles;
+  if (parts > nkb / 2) parts = nkb / 2;
+  return parts < 2 ? 1 : static_cast<int>(parts);
+}
+
+size_t fwd_f32_split_bytes(int BH, int M, int parts) {
+  if (parts <= 1) return 0;
+  return static_cast<size_t>((M + kBM32 - 1) / kBM32) * BH * parts * kF32Slot * sizeof(float);
+}
+
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                           int D, float scale, bool causal, const LaunchCtx& ctx) {
+                           int D, float scale, bool causal, int parts, float* ws, const LaunchCtx& ctx) {
   if (D != kD32) return cudaErrorNotSupported;
+  if (parts < 1 || (parts > 1 && ws == nullptr)) parts = 1;
   CUtensorMap mq, mk, mv;
   if (!make_tmap_3d(&mq, Q, kF32, D, M, BH, 32, kBM32) || !make_tmap_3d(&mk, K, kF32, D, N, BH, 32, kBN32) ||
       !make_tmap_3d(&mv, V, kF32, D, N, BH, 32, kBN32))
     return cudaErrorInvalidValue;
-  return causal ? launch32<true>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx)
-                : launch32<false>(mq, mk, mv, O, LSE, BH, M, N, scale, ctx);
+  return causal ? launch32<true>(mq, mk, mv, O, LSE, BH, M, N, scale, parts, ws, ctx)
+                : launch32<false>(mq, mk, mv, O, LSE, BH, M, N, scale, parts, ws, ctx);
 }
 
 }  // namespace fa

@@ -67,9 +67,11 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 
 /*
  * Bytes of device workspace fa_fwd_ws can use for this problem on the current
- * device: nonzero only for fp16/bf16 with D = 64 and causal == 0, where it is one
- * partial-result slot (a 256x64 f32 block and three 256-float statistics) plus
- * eight 32-bit flags per SM. 0 on bad sizes or when no device is usable.
+ * device. fp16/bf16 with D = 64 and causal == 0: one partial-result slot (a
+ * 256x64 f32 block and three 256-float statistics) plus eight 32-bit flags per
+ * SM. f32 with D = 64 when its 128-row query tiles fill fewer than half the SMs:
+ * one 128x64 f32 block plus two 128-float statistics per (tile, part), where the
+ * key blocks of a tile are shared by `parts` SMs. Otherwise, or on bad sizes, 0.
  */
 size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype);
 
@@ -94,7 +96,8 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  *
  * The split is used when the last wave would be less than 90 % full and every SM
  * gets at least four key blocks; FA_FWD_SPLIT=0 or 1 in the environment turns it
- * off or on regardless.
+ * off or on regardless. For f32 (few query tiles) the parts of a tile write
+ * unnormalised partials that a second launch on `stream` merges the same way.
  */
 fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE, void* workspace,
                     size_t workspace_bytes, int B, int H, int M, int N, int D, float scale, int causal, fa_dtype dtype,

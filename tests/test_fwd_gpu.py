@@ -165,3 +165,16 @@ def test_forward_split_schedule_repeated_calls(monkeypatch):
     for seed in (1, 2, 3):
         inputs, out, lse = run_fwd(1, 3, 512, 640, 64, "f16", False, 0.125, seed=seed)
         check_heads(inputs, out, lse, "f16", False, 0.125)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_f32_without_workspace(causal):
+    """The f32 path with one CTA per query tile (no key-range split): fa_fwd without a workspace."""
+    import torch
+    q, k, v = synth.attention_inputs(1, 2, 300, 700, 64, "f32", seed=4)
+    out = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    fa.forward(to_device(q, "f32"), to_device(k, "f32"), to_device(v, "f32"), 0.125, causal, out=out, lse=lse,
+               workspace=False)
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    check_heads((q, k, v), to_f64(out), to_f64(lse), "f32", causal, 0.125, rel_l2=REL_L2_F32)
