@@ -35,6 +35,7 @@ EXPORTS = (
     "fa_status_string",
     "fa_last_error_message",
     "fa_set_wait_budget_ns",
+    "fa_debug_inject",
 )
 
 _lib = None
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
     L.fa_last_error_message.restype = ctypes.c_char_p
     L.fa_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
     L.fa_set_wait_budget_ns.restype = st
+    L.fa_debug_inject.argtypes = [i]
+    L.fa_debug_inject.restype = st
     _lib = L
     return L
 
@@ -156,6 +159,10 @@ def fa_last_error_message() -> str:
 
 def fa_set_wait_budget_ns(ns: int) -> int:
     return lib().fa_set_wait_budget_ns(int(ns))
+
+def fa_debug_inject(kind: int) -> int:
+    return lib().fa_debug_inject(int(kind))
+
 
 
 # ------------------------------------------------------- tensor helpers

@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
                                                                    float* __restrict__ ws, int BH, int N,
                                                                    int n_splits, float scale_log2,
                                                                    DevStatus* status,
-                                                                   unsigned long long budget_ns) {
+                                                                   unsigned long long budget_ns, int inject) {
   using C = DecCfg<D, DT>;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecSmemHdr* hdr = reinterpret_cast<DecSmemHdr*>(smem_raw);
@@ -152,9 +152,16 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
       const char* kb = reinterpret_cast<const char*>(K + head_off);
       const char* vb = reinterpret_cast<const char*>(V + head_off);
       int issued = 0;
+      // test-only fault injection: the first CTA never fills its first stage, so its consumers'
+      // bounded wait runs out and the launch reports a timeout (no fault, no trap)
+      const bool skip_first = inject == 1 && blockIdx.x == 0 && blockIdx.y == 0;
       for (int it = 0; it < nstage; ++it) {
         const int st = it % kDecStages;
         const uint32_t ph = static_cast<uint32_t>(it / kDecStages) & 1u;
+        if (it == 0 && skip_first) {
+          issued = 1;
+          continue;
+        }
         if (!ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ph ^ 1u, wc, 1)) break;
         const int k0 = n_start + it * C::kTK;
         const int nk = min(C::kTK, n_end - k0);
@@ -169,8 +176,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
       }
       if (hdr->abort_flag) {  // let copies already in flight land before the CTA exits
         for (int it = max(0, issued - kDecStages); it < issued; ++it)
-          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[it % kDecStages]),
-                               static_cast<uint32_t>(it / kDecStages) & 1u, 100000000ull);
+          if (!(it == 0 && skip_first))
+            ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[it % kDecStages]),
+                                 static_cast<uint32_t>(it / kDecStages) & 1u, 100000000ull);
       }
     }
     return;
@@ -349,7 +357,7 @@ cudaError_t launch_decode_t(const void* q, const void* K, const void* V, void* O
   dim3 grid(n_splits, BH);
   kern<<<grid, kDecThreads, smem, ctx.stream>>>(static_cast<const T*>(q), static_cast<const T*>(K),
                                                 static_cast<const T*>(V), ws, BH, N, n_splits, scale * kLog2e,
-                                                ctx.status, ctx.wait_budget_ns);
+                                                ctx.status, ctx.wait_budget_ns, ctx.inject);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -195,6 +195,7 @@ bool use_split(int BH, int M, int N, int num_sms) {
 }
 
 std::atomic<uint32_t> g_epoch{0};
+std::atomic<int> g_inject{0};  // fa_debug_inject: consumed by the next decode launch
 
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, void* ws, size_t ws_bytes, int B,
                    int H, int M, int N, int D, float scale, int causal, fa_dtype dtype, void* stream,
@@ -265,6 +266,12 @@ fa_status fa_set_wait_budget_ns(unsigned long long ns) {
   if (ns < 1000ull) return fail(FA_ERR_INVALID, "wait budget %llu ns is below 1000 ns", ns);
   std::lock_guard<std::mutex> lock(g_mutex);
   g_wait_budget_ns = ns;
+  return FA_OK;
+}
+
+fa_status fa_debug_inject(int kind) {
+  if (kind != 0 && kind != 1) return fail(FA_ERR_INVALID, "unknown fault-injection kind %d", kind);
+  g_inject.store(kind);
   return FA_OK;
 }
 
@@ -344,6 +351,7 @@ fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void*
   FA_TRY(check_ptr(partial_ws, "partial_ws"));
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
+  ctx.inject = g_inject.exchange(0);
   cudaError_t e = launch_decode(q, Kcache, Vcache, O, partial_ws, B * H, N, D, scale, n_splits, dtype, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode: configuration not supported");
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode launch");
@@ -418,6 +426,7 @@ fa_status fa_decode_static(const void* q, const void* Kcache, const void* Vcache
   FA_TRY(static_scratch(&ws));
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
+  ctx.inject = g_inject.exchange(0);
   cudaError_t e = launch_decode(q, Kcache, Vcache, O, ws, B * H, N, D, scale, n_splits, dtype, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode_static: configuration not supported");
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_static launch");

@@ -39,6 +39,7 @@ struct LaunchCtx {
   unsigned long long wait_budget_ns;
   int num_sms;
   cudaStream_t stream;
+  int inject = 0;  // test-only fault injection for this launch (see fa_debug_inject)
 };
 
 // ---- launchers (each returns a cudaError_t from the launch itself)

@@ -203,6 +203,17 @@ const char* fa_last_error_message(void);
  */
 fa_status fa_set_wait_budget_ns(unsigned long long ns);
 
+/*
+ * Test-only fault injection (no counterpart on the pages; exercises the bounded
+ * waits described at fa_set_wait_budget_ns). kind 1: in the next fa_decode /
+ * fa_decode_static launch the first CTA never loads its first stage of keys, so
+ * its compute warps' bounded wait runs out, the CTA drains and exits, and
+ * fa_last_status reports FA_ERR_TIMEOUT naming the decode kernel and wait site.
+ * Nothing faults and the context stays usable. One-shot: the next decode launch
+ * consumes it. kind 0 cancels a pending injection. Other kinds: FA_ERR_INVALID.
+ */
+fa_status fa_debug_inject(int kind);
+
 #ifdef __cplusplus
 }
 #endif
