@@ -193,14 +193,21 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """The slowest rank's time: the whole job takes as long as its slowest replica."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, steps: int, seconds_max: float, world: int) -> float:
+    """Whole-job throughput of `world` replicas that each did `units_per_rank` per step for
+    `steps` steps, timed by the slowest rank (weak scaling: per-rank work is fixed)."""
+    return world * steps * units_per_rank / seconds_max
 
 
 # --------------------------------------------------------------- our arm
@@ -321,9 +328,9 @@ def run_ours(args):
     t_dec = max_over_ranks(t_dec, world)
     t_step = max_over_ranks(t_step, world)
     K = args.steps
-    fwd_tflops = world * K * fwd_flops() / t_fwd / 1e12
-    dec_gbs = world * K * dec_bytes() / t_dec / 1e9
-    bwd_tflops = world * K * 2.5 * fwd_flops() / t_bwd / 1e12 if have_bwd and t_bwd > 0 else None
+    fwd_tflops = whole_job_rate(fwd_flops(), K, t_fwd, world) / 1e12
+    dec_gbs = whole_job_rate(dec_bytes(), K, t_dec, world) / 1e9
+    bwd_tflops = whole_job_rate(2.5 * fwd_flops(), K, t_bwd, world) / 1e12 if have_bwd and t_bwd > 0 else None
 
     # ---- end to end through the C ABI: pinned host inputs in, O and LSE out, every step
     hq, hk, hv = (x.cpu().pin_memory() for x in (qd, kd, vd))
@@ -344,7 +351,7 @@ def run_ours(args):
             e2e_recs.append((a, b))
     torch.cuda.synchronize()
     t_e2e = max_over_ranks(sum(a.elapsed_time(b) for a, b in e2e_recs) / 1e3, world)
-    e2e_tflops = world * K * fwd_flops() / t_e2e / 1e12
+    e2e_tflops = whole_job_rate(fwd_flops(), K, t_e2e, world) / 1e12
     h2d = 3 * qd.numel() * qd.element_size()
     d2h = od.numel() * od.element_size() + lse.numel() * 4
 
