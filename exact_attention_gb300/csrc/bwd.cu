@@ -581,6 +581,9 @@ __global__ void __launch_bounds__(kThreadsO, 1)
             ptx::tc_fence_after();
             qk(it_s);
             vdo(it_s);
+            // the next block's stage has normally landed long ago: check it while the
+            // compute warps work, not between their signal and the next scores
+            if (itm.lo + 1 < itm.hi && !stage_ready(it_s + 1)) break;
           }
         }
         for (int i = itm.lo; i < itm.hi; ++i, ++it_s) {
@@ -589,7 +592,6 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           const bool acc = i > itm.lo;
           // S^T(i) read and P^T(i) stored
           ok = wait(&hdr->sig1, (n1++) & 1u, 22);
-          if (ok && scores && more) ok = stage_ready(it_s + 1);
           if (!ok) break;
           ptx::tc_fence_after();
           if (scores) {
@@ -606,6 +608,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::tc_fence_after();
           if (scores) {
             if (more) vdo(it_s + 1);
+            if (i + 2 < itm.hi && !stage_ready(it_s + 2)) {
+              ok = false;
+              break;
+            }
           } else {
 #pragma unroll
             for (int ks = 0; ks < kT / 16; ++ks)  // dK += dS^T Q
@@ -856,6 +862,8 @@ __global__ void __launch_bounds__(kThreadsO, 1)
             ptx::tc_fence_after();
             qk(it_s);
             dov(it_s);
+            // the next block's stage: checked while the compute warps work
+            if (itm.lo + 1 < itm.hi && !stage_ready(it_s + 1)) break;
           }
         }
         for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
@@ -864,7 +872,6 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           if (scores) {
             // S(j) read
             ok = wait(&hdr->sig1, (n1++) & 1u, 22);
-            if (ok && more) ok = stage_ready(it_s + 1);
             if (!ok) break;
             ptx::tc_fence_after();
             if (more) qk(it_s + 1);
@@ -875,6 +882,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::tc_fence_after();
           if (scores) {
             if (more) dov(it_s + 1);
+            if (j + 2 < itm.hi && !stage_ready(it_s + 2)) {
+              ok = false;
+              break;
+            }
           } else {
 #pragma unroll
             for (int ks = 0; ks < kT / 16; ++ks)  // dQ += dS K
