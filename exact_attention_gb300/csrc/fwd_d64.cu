@@ -53,11 +53,12 @@ constexpr int kD = 64;
 constexpr int kTile = kBM * kD * 2;  // 16 KB: one 128-row x 64-column half tile (128-byte rows)
 constexpr int kStages = 4;           // K/V ring depth (blocks j..j+2 in use, j+3 loading)
 constexpr int kQBuf = 2;             // Q pair buffers
-// softmax 0-3 (tile 0), 4-7 (tile 1), producer 8, MMA issuers 9 (tile 0) and 10 (tile 1).
-// At most three warps share an SM sub-partition (16K registers): 168 registers a thread.
-constexpr int kThreads = 352;
+// softmax 0-3 (tile 0), 4-7 (tile 1), producer 8, MMA issuers 9 (tile 0) and 10 (tile 1),
+// epilogue helper 11. Three warps share an SM sub-partition (16K registers): 168 registers a thread.
+constexpr int kThreads = 384;
 constexpr int kWarpProd = 8;
 constexpr int kWarpMma = 9;
+constexpr int kWarpEpi = 11;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -134,8 +135,11 @@ struct Schedule {
 };
 
 struct Hdr {
-  unsigned long long q_full[kQBuf], q_empty[kQBuf];       // q_empty: one arrival per tile (after its O store)
-  unsigned long long epi[2];  // tile t's 4 softmax warps have written their O rows into its Q buffer
+  unsigned long long q_full[kQBuf], q_empty[kQBuf];  // q_empty: the helper is done with the buffer
+  // epi[qb][t]: tile t's 4 softmax warps are done with a piece held in Q buffer qb (O rows written
+  // into the buffer, or the partial written to global memory). One barrier per buffer, so the
+  // next arrival on it needs q_empty[qb] first and the helper is never two phases behind.
+  unsigned long long epi[kQBuf][2];
   unsigned long long kv_full[kStages], kv_empty[kStages];  // kv_empty: one commit per issuer
   unsigned long long s_full[2];   // S_t(j) computed
   unsigned long long sm_a[2];     // softmax of tile t: first half of P_t(j) stored (4 warps)
@@ -171,8 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQBuf; ++i) {
       ptx::mbar_init(ptx::smem_u32(&hdr->q_full[i]), 1);
-      ptx::mbar_init(ptx::smem_u32(&hdr->q_empty[i]), 2);
-      ptx::mbar_init(ptx::smem_u32(&hdr->epi[i]), 4);
+      ptx::mbar_init(ptx::smem_u32(&hdr->q_empty[i]), 1);
+      ptx::mbar_init(ptx::smem_u32(&hdr->epi[i][0]), 4);
+      ptx::mbar_init(ptx::smem_u32(&hdr->epi[i][1]), 4);
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(ptx::smem_u32(&hdr->s_full[i]), 1);
@@ -199,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
   }
+  if (warp == kWarpEpi && lane == 0) ptx::prefetch_tmap(&tmO);
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -323,6 +329,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       commit(&hdr->mma_done[t]);
       ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[t]), 0u, 1000000000ull);
     }
+  } else if (warp == kWarpEpi) {
+    // ------------------------------------------------------------ epilogue helper (lane 0)
+    // Per piece, once a tile's softmax warps are done with it: the TMA store of the tile's O from
+    // its Q buffer, or (a partial) the fence and the ready flags that publish the partial the
+    // warps wrote; then, both tiles done, the Q buffer's release. None of this waits on the
+    // softmax warps' critical path.
+    if (lane == 0) {
+      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+      Piece ti;
+      for (int it = 0; sch.next(ti, split, BH, num_pairs, nkb); ++it) {
+        const int qb = it % kQBuf;
+        const uint32_t ph = static_cast<uint32_t>(it / kQBuf) & 1u;
+        bool ok = true;
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->epi[qb][t]), ph, wc, 37);
+          if (ok && ti.kind != 2) {
+            ptx::tma_store_3d(&tmO, q_addr(qb, t), 0, ti.q0 + t * kBM, ti.bh);
+            ptx::bulk_commit();
+          }
+        }
+        if (!ok) break;
+        if (ti.kind == 2) {
+          // the softmax warps' partial writes were ordered before their epi arrivals, which this
+          // thread has observed: a gpu-scope release from here publishes them (cumulativity)
+          __threadfence();
+          for (int w = 0; w < 8; ++w) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + w, epoch);
+        } else {
+          ptx::bulk_wait_read();  // both stores have read the buffer
+        }
+        ptx::mbar_arrive(ptx::smem_u32(&hdr->q_empty[qb]));
+      }
+      ptx::bulk_wait_all();  // the O stores have completed
+    }
   } else {
     // ------------------------------------------------------------ softmax / epilogue (one row per thread)
     const int t = warp >> 2;  // tile of the pair
@@ -343,8 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
     Piece ti;
     int it = 0;          // pieces taken (Q buffer = it % kQBuf)
-    uint32_t epi_ph = 0u;
-    const bool leader = wq == 0 && lane == 0;  // stores tile t's O and frees its Q buffer
     for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
       const int nbt = t == 0 ? ti.nb0 : ti.nb1;
       const int qb = it % kQBuf;
@@ -474,23 +511,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 32; ++i) oacc[c + i] = __uint_as_float(o[i]);
       }
       const int prow = t * kBM + wq * 32 + lane;  // row within the pair
-      // Frees the tile's Q buffer once its 4 warps are past their use of it (the leader waits
-      // for the other warps with a bounded wait; its store, if any, has then been issued).
+      // Hands the piece to the epilogue helper: this warp's writes (O rows in the Q buffer, or
+      // the partial in global memory) are ordered before the arrival.
       auto release_q = [&](bool store) {
-        ptx::fence_proxy_async_smem();  // this warp's shared-memory writes -> the TMA engine
+        if (store) ptx::fence_proxy_async_smem();  // shared-memory writes -> the TMA engine
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->epi[t]));
-        if (leader) {
-          if (ptx::mbar_wait(ptx::smem_u32(&hdr->epi[t]), epi_ph, wc, 37)) {
-            if (store) {
-              ptx::tma_store_3d(&tmO, q_addr(qb, t), 0, ti.q0 + t * kBM, ti.bh);
-              ptx::bulk_commit();
-              ptx::bulk_wait_read();
-            }
-            ptx::mbar_arrive(ptx::smem_u32(&hdr->q_empty[qb]));
-          }
-        }
-        epi_ph ^= 1u;
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->epi[qb][t]));
       };
       if (ti.kind == 2) {
         // later blocks of a split pair: hand (O, m, l, le) to the CTA that holds its first block.
@@ -501,10 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         slot[kPairRows * kD + prow] = m2;
         slot[kPairRows * kD + kPairRows + prow] = l;
         slot[kPairRows * kD + 2 * kPairRows + prow] = le;
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + warp, epoch);
-        release_q(false);
+        release_q(false);  // the helper publishes the partial
         ptx::tc_fence_before();
         continue;
       }
@@ -572,7 +595,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (warp < 8 && (warp & 3) == 0 && lane == 0) ptx::bulk_wait_all();  // this tile's O stores completed
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kWarpMma) {
