@@ -176,20 +176,36 @@ using namespace fa;
 
 namespace {
 
-// Whether a forward call with a workspace runs the split schedule (D = 64 halves,
-// non-causal). FA_FWD_SPLIT=0 / 1 forces it off / on (tests use it); by default it is
-// used when whole pairs would leave the last wave of CTAs less than 90 % full.
-bool split_capable(int D, int causal, int dtype) { return D == 64 && causal == 0 && dtype != FA_F32; }
+// Whether a forward call with a workspace runs the split schedule (D = 64 halves).
+// FA_FWD_SPLIT=0 / 1 forces it off / on (tests use it); by default it is used for non-causal
+// calls when whole pairs would leave the last wave of CTAs less than 90 % full.
+bool split_capable(int D, int dtype) { return D == 64 && dtype != FA_F32; }
 
-bool use_split(int BH, int M, int N, int num_sms) {
+// Units of the D=64 forward's split schedule: the key blocks of each query-tile pair's tile 0
+// (causal: min(nkb, 2p + 1) for pair p of a head, so p^2 of them before pair p while
+// 2p - 1 < nkb, nkb per pair after that).
+long long split_units(int BH, int M, int N, int causal) {
+  const long long pairs = (M + 255) / 256, nkb = (N + 127) / 128;
+  long long per_head = pairs * nkb;
+  if (causal) {
+    const long long c = (nkb + 1) / 2;
+    per_head = pairs <= c ? pairs * pairs : c * c + (pairs - c) * nkb;
+  }
+  return static_cast<long long>(BH) * per_head;
+}
+
+bool use_split(int BH, int M, int N, int causal, int num_sms) {
   const long long pairs = static_cast<long long>(BH) * ((M + 255) / 256);
-  const long long units = pairs * ((N + 127) / 128);
+  const long long units = split_units(BH, M, N, causal);
   if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
   if (const char* e = std::getenv("FA_FWD_SPLIT")) {
     if (e[0] == '0') return false;
     if (e[0] == '1') return true;
   }
   if (units < 4ll * num_sms) return false;
+  // causal: whole pairs dealt in a serpentine order (heaviest with lightest) measured faster
+  // than the split, whose extra pieces cost more than the balance gains
+  if (causal) return false;
   const long long rounds = (pairs + num_sms - 1) / num_sms;
   return pairs * 10 < rounds * num_sms * 9;
 }
@@ -213,11 +229,11 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
   FwdSplit sp{};
-  if (ws != nullptr && split_capable(D, causal, dtype)) {
+  if (ws != nullptr && split_capable(D, dtype)) {
     FA_TRY(check_ptr(ws, "workspace"));
     const size_t need = fwd_d64_split_bytes(ctx.num_sms);
     if (ws_bytes < need) return fail(FA_ERR_INVALID, "%s: workspace of %zu bytes, %zu needed", name, ws_bytes, need);
-    if (use_split(B * H, M, N, ctx.num_sms)) {
+    if (use_split(B * H, M, N, causal, ctx.num_sms)) {
       sp.ws = static_cast<float*>(ws);
       sp.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + need - ctx.num_sms * 8 * sizeof(uint32_t));
       uint32_t ep = ++g_epoch;
@@ -290,7 +306,7 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
   DevState* st = nullptr;
   if (device_state(&st) != FA_OK) return 0;
   if (dtype == FA_F32 && D == 64) return fwd_f32_split_bytes(B * H, M, fwd_f32_parts(B * H, M, N, st->num_sms));
-  if (!split_capable(D, causal, dtype)) return 0;
+  if (!split_capable(D, dtype)) return 0;
   return fwd_d64_split_bytes(st->num_sms);
 }
 

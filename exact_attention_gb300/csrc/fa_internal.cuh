@@ -46,7 +46,7 @@ struct LaunchCtx {
 cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N, int D,
                           float scale, int n_splits, int dtype, const LaunchCtx& ctx);
 
-// Split schedule of the D = 64 forward (non-causal): the caller's workspace holds one
+// Split schedule of the D = 64 forward: the caller's workspace holds one
 // partial-result slot and 8 ready flags per SM; ws == nullptr selects the classic schedule.
 // epoch is unique per launch (flags from earlier launches never match it).
 struct FwdSplit {

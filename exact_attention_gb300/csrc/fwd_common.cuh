@@ -37,6 +37,15 @@ __device__ __forceinline__ TileInfo tile_info(int tile, int BH, int num_pairs, i
   return ti;
 }
 
+// The CTA's r-th pair of the classic schedule (whole pairs, one CTA per SM): round-robin
+// over the tile_info order, every other round reversed when causal (serpentine), so the CTA
+// that took one of the heaviest pairs of a round takes one of the lightest of the next.
+template <bool CAUSAL>
+__device__ __forceinline__ int classic_tile(int r) {
+  const int c = (CAUSAL && (r & 1)) ? static_cast<int>(gridDim.x - 1u - blockIdx.x) : static_cast<int>(blockIdx.x);
+  return r * static_cast<int>(gridDim.x) + c;
+}
+
 // packed f32 arithmetic lives in ptx.cuh
 using ptx::fadd2;
 using ptx::ffma2;

@@ -45,6 +45,7 @@ using fwdc::ffma2;
 using fwdc::fmax3;
 using fwdc::kBM;
 using fwdc::kBN;
+using fwdc::classic_tile;
 using fwdc::mask32;
 using fwdc::tile_info;
 using fwdc::TileInfo;
@@ -82,53 +83,93 @@ struct Piece {
              // the CTAs that took the rest; 2: later blocks, written out as a partial
 };
 
+// Units of the split schedule: the key blocks of a pair's tile 0, pairs of one head adjacent
+// and in query order. Non-causal every pair has nkb of them. Causal, pair p's tile 0 (queries
+// [256p, 256p + 128)) needs min(nkb, 2p + 1) blocks and its tile 1 one more while that is
+// <= nkb (its diagonal block, taken by the piece that holds the pair's last unit), so the
+// pairs before p hold p^2 units while 2p - 1 < nkb and nkb each after that.
+template <bool CAUSAL>
+__device__ __forceinline__ uint32_t units_before(int p, int nkb) {
+  if (!CAUSAL) return static_cast<uint32_t>(p) * static_cast<uint32_t>(nkb);
+  const uint32_t c = static_cast<uint32_t>(nkb + 1) / 2u;  // pairs whose tile 0 needs 2p + 1 <= nkb blocks
+  const uint32_t pp = static_cast<uint32_t>(p);
+  return pp <= c ? pp * pp : c * c + (pp - c) * static_cast<uint32_t>(nkb);
+}
+// Pair p and block jb of unit uh of a head (inverse of units_before).
+template <bool CAUSAL>
+__device__ __forceinline__ void unit_pair(uint32_t uh, int nkb, int& p, int& jb) {
+  const uint32_t n = static_cast<uint32_t>(nkb);
+  const uint32_t c = static_cast<uint32_t>(nkb + 1) / 2u;
+  if (CAUSAL && uh < c * c) {
+    uint32_t r = static_cast<uint32_t>(sqrtf(static_cast<float>(uh)));  // within one of floor(sqrt(uh))
+    if (r * r > uh) --r;
+    if ((r + 1u) * (r + 1u) <= uh) ++r;
+    p = static_cast<int>(r);
+    jb = static_cast<int>(uh - r * r);
+    return;
+  }
+  const uint32_t base = CAUSAL ? c * c : 0u;
+  const uint32_t q = (uh - base) / n;
+  p = static_cast<int>((CAUSAL ? c : 0u) + q);
+  jb = static_cast<int>(uh - base - q * n);
+}
+
 // Which pieces a CTA takes. Classic: whole pairs blockIdx.x, +gridDim.x, ... (tile_info
-// order). Split (non-causal only): the contiguous range [c U / G, (c+1) U / G) of the
-// U = pairs x key-blocks units (U < 2^31, checked by the host), so every CTA does the same
-// number of blocks and no partial last wave is left; a pair cut by a range boundary is
-// finished by the CTA that holds its first block, which processes that piece last, while
-// the CTAs holding the rest process theirs first.
+// order). Split: the contiguous range [c U / G, (c+1) U / G) of the U units of all heads
+// (U < 2^31, checked by the host), so every CTA does the same number of blocks and no
+// partial last wave is left; a pair cut by a range boundary is finished by the CTA that
+// holds its first block, which processes that piece last, while the CTAs holding the rest
+// process theirs first.
 template <bool CAUSAL>
 struct Schedule {
-  uint32_t u, e;  // split: the remaining unit range; classic: u = next pair, e = pair count
+  uint32_t u, e;  // split: the remaining unit range; classic: u = next round, e = pair count
   __device__ static uint32_t start(uint32_t c, uint32_t units) {
     return static_cast<uint32_t>(static_cast<uint64_t>(c) * units / gridDim.x);
   }
+  __device__ static uint32_t total_units(int BH, int num_pairs, int nkb) {
+    return static_cast<uint32_t>(BH) * units_before<CAUSAL>(num_pairs, nkb);
+  }
   __device__ Schedule(bool split, int BH, int num_pairs, int nkb) {
     if (split) {
-      const uint32_t units = static_cast<uint32_t>(BH * num_pairs * nkb);
+      const uint32_t units = total_units(BH, num_pairs, nkb);
       u = start(blockIdx.x, units);
       e = start(blockIdx.x + 1, units);
     } else {
-      u = blockIdx.x;
+      u = 0;
       e = static_cast<uint32_t>(BH * num_pairs);
     }
   }
   __device__ bool next(Piece& pc, bool split, int BH, int num_pairs, int nkb) {
-    if (u >= e) return false;
     if (!split) {
-      const TileInfo ti = tile_info<CAUSAL>(static_cast<int>(u), BH, num_pairs, nkb);
-      pc.pair = static_cast<int>(u);
+      const int tile = classic_tile<CAUSAL>(static_cast<int>(u));
+      if (tile >= static_cast<int>(e)) return false;
+      const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
+      pc.pair = tile;
       pc.bh = ti.bh;
       pc.q0 = ti.q0;
       pc.jb = 0;
       pc.nb0 = ti.nb0;
       pc.nb1 = ti.nb1;
       pc.kind = 0;
-      u += gridDim.x;
+      ++u;
       return true;
     }
-    const int p = static_cast<int>(u / nkb);
-    const int jb = static_cast<int>(u - static_cast<uint32_t>(p) * nkb);
+    if (u >= e) return false;
+    const uint32_t hu = units_before<CAUSAL>(num_pairs, nkb);
+    const uint32_t bh = u / hu;
+    int p, jb;
+    unit_pair<CAUSAL>(u - bh * hu, nkb, p, jb);
+    const int nb0p = CAUSAL ? min(nkb, 2 * p + 1) : nkb;  // the pair's units
+    const int nb1p = CAUSAL ? min(nkb, 2 * p + 2) : nkb;
     const uint32_t left = e - u;
-    const int je = left < static_cast<uint32_t>(nkb - jb) ? jb + static_cast<int>(left) : nkb;
-    const TileInfo ti = tile_info<false>(p, BH, num_pairs, nkb);
-    pc.pair = p;
-    pc.bh = ti.bh;
-    pc.q0 = ti.q0;
+    const int je = left < static_cast<uint32_t>(nb0p - jb) ? jb + static_cast<int>(left) : nb0p;
+    pc.pair = static_cast<int>(bh) * num_pairs + p;
+    pc.bh = static_cast<int>(bh);
+    pc.q0 = p * 2 * kBM;
     pc.jb = jb;
-    pc.nb0 = pc.nb1 = je - jb;
-    pc.kind = (jb == 0 && je == nkb) ? 0 : (jb == 0 ? 1 : 2);
+    pc.nb0 = je - jb;
+    pc.nb1 = pc.nb0 + (je == nb0p ? nb1p - nb0p : 0);  // tile 1's diagonal block goes with the last unit
+    pc.kind = (jb == 0 && je == nb0p) ? 0 : (jb == 0 ? 1 : 2);
     u += static_cast<uint32_t>(je - jb);
     return true;
   }
@@ -170,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM);
   const int nkb = (N + kBN - 1) / kBN;
-  const bool split = !CAUSAL && ws != nullptr;
+  const bool split = ws != nullptr;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQBuf; ++i) {
@@ -305,17 +346,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) qk(1);
         }
         for (int j = 0; j < nb && ok; ++j) {
+          // K_{j+2} is normally long loaded: its barrier is checked while the softmax forms
+          // P_t(j), since a barrier operation right after tcgen05 work is slow for this thread
+          if (j + 2 < nb) {
+            ok = kv_ready(j + 2);
+            if (!ok) break;
+          }
           ok = arrival_a();  // first half of P_t(j) stored
           if (!ok) break;
           pv(j, 0);
           ok = arrival_b();  // second half of P_t(j) stored (and S_t(j+1) read)
           if (!ok) break;
           pv(j, 1);
-          if (j + 2 < nb) {
-            ok = kv_ready(j + 2);
-            if (!ok) break;
-            qk(j + 2);
-          }
+          if (j + 2 < nb) qk(j + 2);
           commit(&hdr->kv_empty[(kv_base + j) % kStages]);  // this tile is done with K_j, V_j
         }
         // blocks of the pair this tile does not use (causal): release them once loaded
@@ -534,8 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ti.kind == 1) {
         // first blocks of a split pair: merge the partials of the CTAs that took the rest
         // (they processed those pieces first, so they are normally long ready)
-        const uint32_t units = static_cast<uint32_t>(BH * num_pairs * nkb);
-        const uint32_t end_u = static_cast<uint32_t>(ti.pair + 1) * static_cast<uint32_t>(nkb);
+        const uint32_t units = Schedule<CAUSAL>::total_units(BH, num_pairs, nkb);
+        const uint32_t end_u = static_cast<uint32_t>(ti.bh) * units_before<CAUSAL>(num_pairs, nkb) +
+                               units_before<CAUSAL>(ti.q0 / (2 * kBM) + 1, nkb);  // the pair's last unit + 1
         for (uint32_t c2 = blockIdx.x + 1; c2 < gridDim.x && Schedule<CAUSAL>::start(c2, units) < end_u && ok; ++c2) {
           // a CTA with an empty range (more CTAs than units) writes no partial
           if (Schedule<CAUSAL>::start(c2 + 1, units) == Schedule<CAUSAL>::start(c2, units)) continue;
@@ -611,7 +655,7 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>((M + 2 * kBM - 1) / (2 * kBM)) * BH;
-  if (!CAUSAL && sp.ws != nullptr) {
+  if (sp.ws != nullptr) {
     // split schedule: every SM holds one CTA for the whole launch, and a CTA may wait for the
     // partials of later CTAs, so all of them must be resident at once (cooperative launch)
     cudaLaunchConfig_t cfg{};

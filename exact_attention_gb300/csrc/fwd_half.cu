@@ -54,6 +54,7 @@ using fwdc::tile_info;
 using fwdc::ffma2;
 using fwdc::fadd2;
 using fwdc::fmax3;
+using fwdc::classic_tile;
 using fwdc::mask32;
 constexpr int kChunk = 16384;   // one 128-row x 128-byte swizzled chunk
 // 10 warps: three share one SM sub-partition (16K registers), so a thread has
@@ -173,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t kv_it = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+      for (int r = 0, tile = classic_tile<CAUSAL>(0); tile < num_tiles && ok; tile = classic_tile<CAUSAL>(++r), ++it) {
         const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
         const int qb = it % C::kQBuf;
         const uint32_t qph = static_cast<uint32_t>(it / C::kQBuf) & 1u;
@@ -247,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
         return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
       };
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++it) {
+      for (int r = 0, tile = classic_tile<CAUSAL>(0); tile < num_tiles && ok; tile = classic_tile<CAUSAL>(++r), ++it) {
         const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
         const int qb = it % C::kQBuf;
         const uint32_t qph = static_cast<uint32_t>(it / C::kQBuf) & 1u;
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_full = ptx::smem_u32(&hdr->o_full[t]);
     uint32_t s_ph = 0u, o_ph = 0u;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    for (int r = 0, tile = classic_tile<CAUSAL>(0); tile < num_tiles && ok; tile = classic_tile<CAUSAL>(++r)) {
       const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
       const int nbt = t == 0 ? ti.nb0 : ti.nb1;
       const int row = ti.q0 + t * kBM + wq * 32 + lane;  // query index within the head

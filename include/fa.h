@@ -67,7 +67,7 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
 
 /*
  * Bytes of device workspace fa_fwd_ws can use for this problem on the current
- * device. fp16/bf16 with D = 64 and causal == 0: one partial-result slot (a
+ * device. fp16/bf16 with D = 64 (causal or not): one partial-result slot (a
  * 256x64 f32 block and three 256-float statistics) plus eight 32-bit flags per
  * SM. f32 with D = 64 when its 128-row query tiles fill fewer than half the SMs:
  * one 128x64 f32 block plus two 128-float statistics per (tile, part), where the
@@ -94,9 +94,10 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  *                    workspace at the same time.
  *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
  *
- * The split is used when the last wave would be less than 90 % full and every SM
- * gets at least four key blocks; FA_FWD_SPLIT=0 or 1 in the environment turns it
- * off or on regardless. For f32 (few query tiles) the parts of a tile write
+ * The split is used when the call is not causal, every SM gets at least four key
+ * blocks and the last wave would be less than 90 % full (causal pairs, whose key
+ * ranges differ in length, are dealt whole in a serpentine order, which measured
+ * faster); FA_FWD_SPLIT=0 or 1 in the environment turns it off or on regardless. For f32 (few query tiles) the parts of a tile write
  * unnormalised partials that a second launch on `stream` merges the same way.
  */
 fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE, void* workspace,

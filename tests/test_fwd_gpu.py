@@ -148,15 +148,17 @@ SPLIT_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("B,H,M,N", SPLIT_SHAPES)
-def test_forward_split_schedule_matches_oracle(monkeypatch, dtype, B, H, M, N):
+def test_forward_split_schedule_matches_oracle(monkeypatch, dtype, B, H, M, N, causal):
     """The split schedule (each SM an equal share of (query pair, key block) units, cut
-    pairs merged with the online-softmax rescaling) forced on."""
+    pairs merged with the online-softmax rescaling) forced on; causal pairs hold
+    different numbers of units."""
     monkeypatch.setenv("FA_FWD_SPLIT", "1")
     scale = 0.125
-    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, False, scale, seed=M + N)
-    check_heads(inputs, out, lse, dtype, False, scale)
+    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, causal, scale, seed=M + N)
+    check_heads(inputs, out, lse, dtype, causal, scale)
 
 
 def test_forward_split_schedule_repeated_calls(monkeypatch):
