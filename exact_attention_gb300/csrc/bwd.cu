@@ -24,6 +24,16 @@
 namespace fa {
 namespace {
 
+// The CTA's r-th work item of a persistent loop (one CTA per SM): round-robin over the item
+// order, every other round reversed when causal (serpentine), so a CTA that took one of the
+// heaviest items of a round takes one of the lightest of the next; `items` when none is left.
+template <bool CAUSAL>
+__device__ __forceinline__ int item_of_round(int r, int items) {
+  const int c = (CAUSAL && (r & 1)) ? static_cast<int>(gridDim.x - 1u - blockIdx.x) : static_cast<int>(blockIdx.x);
+  const long long w = static_cast<long long>(r) * gridDim.x + c;
+  return w < items ? static_cast<int>(w) : items;
+}
+
 constexpr int kT = 128;          // tile rows (keys or queries) and streamed block rows
 constexpr int kChunkB = 16384;   // 128 rows x 128 bytes, one swizzled chunk
 constexpr int kStagesB = 2;
@@ -132,8 +142,16 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   auto item = [&](int w) {
     BwdItem it;
-    it.bh = w / nkb;
-    const int kb = w - it.bh * nkb;
+    // causal: key tiles with the most query blocks (the first ones) go first, all heads of a
+    // key tile together; non-causal: the key tiles of a head are adjacent
+    int kb;
+    if (CAUSAL) {
+      kb = w / BH;
+      it.bh = w - kb * BH;
+    } else {
+      it.bh = w / nkb;
+      kb = w - it.bh * nkb;
+    }
     it.r0 = kb * kT;
     // causal: query block i has keys <= its last row; start at the block holding query k0
     it.lo = CAUSAL ? min(it.r0 / kT, nqb) : 0;
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     uint32_t it_s = 0;
     int n_item = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+    for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
       const BwdItem itm = item(w);
       if (lane == 0) {
         ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10);
@@ -218,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       uint32_t it_s = 0, p_ph = 0;
       int n_item = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+      for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
         const BwdItem itm = item(w);
         if (!ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_full), n_item & 1, wc, 20)) break;
         ptx::tc_fence_after();
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     uint32_t it_s = 0, s_ph = 0;
     int n_item = 0;
     bool ok = true;
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+    for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
       const BwdItem itm = item(w);
       const int key = itm.r0 + warp * 32 + lane;
       for (int i = itm.lo; i < itm.hi; ++i, ++it_s) {
@@ -485,14 +503,15 @@ __global__ void __launch_bounds__(kThreadsO, 1)
     uint32_t it_s = 0;
     int n_item = 0;
     bool ok = true;
-    int w = blockIdx.x;
+    int r = 0;
+    int w = item_of_round<CAUSAL>(0, items);
     BwdItem itm{};
     // first item that has a query block (items without one need only their fixed tiles)
     if (w < items) {
       itm = item(w);
       if (itm.lo < itm.hi) fetch(itm, itm.lo);
     }
-    for (; w < items && ok; w += gridDim.x, ++n_item) {
+    for (; w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
       itm = item(w);
       if (lane == 0) {
         ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10);
@@ -528,7 +547,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         if (i + 1 < itm.hi) {
           fetch(itm, i + 1);
         } else {
-          for (int w2 = w + gridDim.x; w2 < items; w2 += gridDim.x) {
+          for (int r2 = r + 1, w2 = item_of_round<CAUSAL>(r2, items); w2 < items; w2 = item_of_round<CAUSAL>(++r2, items)) {
             const BwdItem nx = item(w2);
             if (nx.lo < nx.hi) {
               fetch(nx, nx.lo);
@@ -571,7 +590,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
         commit(&hdr->dp_full);
       };
-      for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+      for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
         const BwdItem itm = item(w);
         if (scores) {
           if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
@@ -645,7 +664,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
     };
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+    for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
       const BwdItem itm = item(w);
       const int key = itm.r0 + quarter * 32 + lane;
       for (int i = itm.lo; i < itm.hi; ++i, ++it_s, ++nb) {
@@ -797,7 +816,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       uint32_t it_s = 0;
       int n_item = 0;
       bool ok = true;
-      for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+      for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
         const BwdItem itm = item(w);
         if (!ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10)) break;
         const uint32_t ff = ptx::smem_u32(&hdr->fixed_full);
@@ -852,7 +871,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sdO, ks), kmajor_desc(sV(st), ks), id_s, ks > 0);
         commit(&hdr->dp_full);
       };
-      for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+      for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
         const BwdItem itm = item(w);
         if (scores) {
           if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
@@ -920,7 +939,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
     };
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++n_item) {
+    for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
       const BwdItem itm = item(w);
       const int row = itm.r0 + quarter * 32 + lane;
       const bool valid = row < M;
