@@ -21,6 +21,8 @@ from ._binding import (  # noqa: F401
     fa_bwd_workspace_bytes,
     fa_decode,
     fa_decode_static,
+    fa_decode_ex,
+    fa_decode_ex_workspace_bytes,
     fa_debug_inject,
     fa_decode_workspace_bytes,
     fa_fwd,

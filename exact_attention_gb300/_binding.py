@@ -31,6 +31,8 @@ EXPORTS = (
     "fa_decode",
     "fa_decode_workspace_bytes",
     "fa_decode_static",
+    "fa_decode_ex",
+    "fa_decode_ex_workspace_bytes",
     "fa_last_status",
     "fa_status_string",
     "fa_last_error_message",
@@ -73,6 +75,10 @@ def lib() -> ctypes.CDLL:
     L.fa_decode_static.restype = st
     L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_decode_ex.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, vp]
+    L.fa_decode_ex.restype = st
+    L.fa_decode_ex_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.fa_decode_ex_workspace_bytes.restype = ctypes.c_size_t
     L.fa_bwd_workspace_bytes.argtypes = [i, i, i]
     L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
     L.fa_last_status.argtypes = [vp]
@@ -139,6 +145,15 @@ def fa_decode_static(q, Kcache, Vcache, O, B, H, N, D, scale, n_splits, dtype, s
 
 def fa_decode_workspace_bytes(B, H, D, n_splits) -> int:
     return lib().fa_decode_workspace_bytes(B, H, D, n_splits)
+
+
+def fa_decode_ex(q, Kcache, Vcache, O, LSE, partial_ws, B, H, R, N, D, scale, n_splits, dtype, stream=None) -> int:
+    return lib().fa_decode_ex(_ptr(q), _ptr(Kcache), _ptr(Vcache), _ptr(O), _ptr(LSE), _ptr(partial_ws), B, H, R, N,
+                              D, float(scale), n_splits, int(dtype), _stream(stream))
+
+
+def fa_decode_ex_workspace_bytes(B, H, R, D, n_splits) -> int:
+    return lib().fa_decode_ex_workspace_bytes(B, H, R, D, n_splits)
 
 
 def fa_bwd_workspace_bytes(B, H, M) -> int:
@@ -237,21 +252,31 @@ def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=Non
     return dq, dk, dv, ws
 
 
-def decode(q, k_cache, v_cache, scale: float, n_splits: int, out=None, workspace=None, stream=None):
-    """O [B,H,1,D] for one query row per (batch, head); returns (O, partial workspace)."""
+def decode(q, k_cache, v_cache, scale: float, n_splits: int, out=None, workspace=None, stream=None, lse=None):
+    """O [B,H,R,D] for R (1..4) query rows per (batch, head); returns (O, partial workspace).
+
+    With lse (a float32 [B,H,R] tensor, or True to allocate one) the LSE is written too and
+    (O, workspace, lse) is returned; R = 1 without lse goes through fa_decode."""
     import torch
-    B, H, one, D = _dims4(q, "q")
-    if one != 1:
-        raise ValueError("decode takes one query row per (batch, head)")
+    B, H, R, D = _dims4(q, "q")
     N = _dims4(k_cache, "k_cache")[2]
     if out is None:
         out = torch.empty_like(q)
+    if lse is True:
+        lse = torch.empty((B, H, R), dtype=torch.float32, device=q.device)
+    if R == 1 and lse is None:
+        if workspace is None:
+            nbytes = fa_decode_workspace_bytes(B, H, D, n_splits)
+            workspace = torch.empty((max(nbytes, 4) // 4,), dtype=torch.float32, device=q.device)
+        _check(fa_decode(q, k_cache, v_cache, out, workspace, B, H, N, D, scale, n_splits, fa_dtype(q), stream),
+               "fa_decode")
+        return out, workspace
     if workspace is None:
-        nbytes = fa_decode_workspace_bytes(B, H, D, n_splits)
+        nbytes = fa_decode_ex_workspace_bytes(B, H, R, D, n_splits)
         workspace = torch.empty((max(nbytes, 4) // 4,), dtype=torch.float32, device=q.device)
-    _check(fa_decode(q, k_cache, v_cache, out, workspace, B, H, N, D, scale, n_splits, fa_dtype(q), stream),
-           "fa_decode")
-    return out, workspace
+    _check(fa_decode_ex(q, k_cache, v_cache, out, lse, workspace, B, H, R, N, D, scale, n_splits, fa_dtype(q),
+                        stream), "fa_decode_ex")
+    return (out, workspace) if lse is None else (out, workspace, lse)
 
 
 def split_workspace(ws, B: int, H: int, D: int, n_splits: int):

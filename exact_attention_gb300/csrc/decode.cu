@@ -1,4 +1,4 @@
-// Flash decoding: one query row per (batch, head) against a long KV cache.
+// Flash decoding: a few query rows per (batch, head) against a long KV cache.
 //
 // Follows "Flash decoding" (linear algebra for programmers, part 4),
 // "Overview of the algorithm": the keys are split into n_splits chunks; the
@@ -14,6 +14,11 @@
 // its own (m, l, acc) online-softmax state in registers, and the units of the
 // CTA are merged with the (m, l) monoid at the end ("Flash Attention" notes,
 // "Deriving the online softmax").
+//
+// Several query rows (R <= 4) of one (batch, head) share the cache: each K and V
+// vector a lane unpacks serves all of them, so the HBM traffic stays that of
+// one row. Row r of head bh is partial row bh*R + r, so the combine runs over
+// B*H*R rows unchanged; it also writes LSE = m_g + ln l_g when asked.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -94,11 +99,12 @@ struct DecSmemHdr {
   int abort_flag;
 };
 
-template <int D, int DT>
+// R: query rows held per thread (template); rows <= R of them are real (q, ws hold `rows`).
+template <int D, int DT, int R>
 __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typename Elem<DT>::T* __restrict__ q,
                                                                    const typename Elem<DT>::T* __restrict__ K,
                                                                    const typename Elem<DT>::T* __restrict__ V,
-                                                                   float* __restrict__ ws, int BH, int N,
+                                                                   float* __restrict__ ws, int BH, int rows, int N,
                                                                    int n_splits, float scale_log2,
                                                                    DevStatus* status,
                                                                    unsigned long long budget_ns, int inject) {
@@ -119,15 +125,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
   const int nkeys = n_end - n_start;
   const int nstage = (nkeys + C::kTK - 1) / C::kTK;
 
-  float* ws_O = ws + (static_cast<size_t>(bh) * n_splits + split) * D;
-  float* ws_m = ws + static_cast<size_t>(BH) * n_splits * D + static_cast<size_t>(bh) * n_splits + split;
-  float* ws_l = ws_m + static_cast<size_t>(BH) * n_splits;
+  // partial of query row r of this head (row bh*rows + r of the combine)
+  const size_t nrow = static_cast<size_t>(BH) * rows;
+  auto ws_O = [&](int r) { return ws + ((static_cast<size_t>(bh) * rows + r) * n_splits + split) * D; };
+  auto ws_m = [&](int r) { return ws + nrow * n_splits * D + (static_cast<size_t>(bh) * rows + r) * n_splits + split; };
+  auto ws_l = [&](int r) { return ws_m(r) + nrow * n_splits; };
 
   if (nkeys <= 0) {  // empty split: the identity of the merge
-    for (int d = threadIdx.x; d < D; d += blockDim.x) ws_O[d] = 0.f;
-    if (threadIdx.x == 0) {
-      *ws_m = -INFINITY;
-      *ws_l = 0.f;
+    for (int i = threadIdx.x; i < rows * D; i += blockDim.x) ws_O(i / D)[i % D] = 0.f;
+    if (threadIdx.x < rows) {
+      *ws_m(threadIdx.x) = -INFINITY;
+      *ws_l(threadIdx.x) = 0.f;
     }
     return;
   }
@@ -187,18 +195,29 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
   // ------------------------------------------------------------ consumers
   const int ru = warp * C::kKPW + lane / C::kLPK;  // row unit
   const int sl = lane % C::kLPK;                   // 16-byte slot within the key row
-  float qv[C::kEPL];
-  {
-    const uint4 u = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(q + static_cast<size_t>(bh) * D) +
-                                                    sl * 16);
-    Elem<DT>::unpack(u, qv);
+  float qv[R][C::kEPL];
 #pragma unroll
-    for (int e = 0; e < C::kEPL; ++e) qv[e] *= scale_log2;  // scores come out in log2 units
+  for (int r = 0; r < R; ++r) {
+    if (r < rows) {
+      const uint4 u = *reinterpret_cast<const uint4*>(
+          reinterpret_cast<const char*>(q + (static_cast<size_t>(bh) * rows + r) * D) + sl * 16);
+      Elem<DT>::unpack(u, qv[r]);
+#pragma unroll
+      for (int e = 0; e < C::kEPL; ++e) qv[r][e] *= scale_log2;  // scores come out in log2 units
+    } else {
+#pragma unroll
+      for (int e = 0; e < C::kEPL; ++e) qv[r][e] = 0.f;  // a padding row: computed, never written
+    }
   }
-  float m = -INFINITY, l = 0.f;
-  float acc[C::kEPL];
+  float m[R], l[R];
+  float acc[R][C::kEPL];
 #pragma unroll
-  for (int e = 0; e < C::kEPL; ++e) acc[e] = 0.f;
+  for (int r = 0; r < R; ++r) {
+    m[r] = -INFINITY;
+    l[r] = 0.f;
+#pragma unroll
+    for (int e = 0; e < C::kEPL; ++e) acc[r][e] = 0.f;
+  }
 
   for (int it = 0; it < nstage; ++it) {
     const int st = it % kDecStages;
@@ -208,38 +227,48 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
     const uint8_t* sk = ring + st * kDecStageBytes;
     const uint8_t* sv = sk + kDecStageBytes / 2;
 
-    float s[C::kG];
+    float s[C::kG][R];
 #pragma unroll
     for (int g = 0; g < C::kG; ++g) {
       const int kk = ru + g * C::kNU;
-      float part = 0.f;
+      float part[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) part[r] = 0.f;
       if (kk < nk) {
         float kf[C::kEPL];
         Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sk + kk * C::kRow + sl * 16), kf);
 #pragma unroll
-        for (int e = 0; e < C::kEPL; ++e) part = fmaf(qv[e], kf[e], part);
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < C::kEPL; ++e) part[r] = fmaf(qv[r][e], kf[e], part[r]);
       }
 #pragma unroll
-      for (int o = C::kLPK / 2; o >= 1; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
-      s[g] = kk < nk ? part : -INFINITY;
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int o = C::kLPK / 2; o >= 1; o >>= 1) part[r] += __shfl_xor_sync(0xFFFFFFFFu, part[r], o);
+        s[g][r] = kk < nk ? part[r] : -INFINITY;
+      }
     }
-    float mb = s[0];
+    float p[C::kG][R];
 #pragma unroll
-    for (int g = 1; g < C::kG; ++g) mb = fmaxf(mb, s[g]);
-    const float m_new = fmaxf(m, mb);
-    const float m_safe = m_new == -INFINITY ? 0.f : m_new;
-    const float corr = ptx::ex2(m - m_safe);
-    float p[C::kG];
-    float ps = 0.f;
+    for (int r = 0; r < R; ++r) {
+      float mb = s[0][r];
 #pragma unroll
-    for (int g = 0; g < C::kG; ++g) {
-      p[g] = ptx::ex2(s[g] - m_safe);
-      ps += p[g];
+      for (int g = 1; g < C::kG; ++g) mb = fmaxf(mb, s[g][r]);
+      const float m_new = fmaxf(m[r], mb);
+      const float m_safe = m_new == -INFINITY ? 0.f : m_new;
+      const float corr = ptx::ex2(m[r] - m_safe);
+      float ps = 0.f;
+#pragma unroll
+      for (int g = 0; g < C::kG; ++g) {
+        p[g][r] = ptx::ex2(s[g][r] - m_safe);
+        ps += p[g][r];
+      }
+      l[r] = fmaf(l[r], corr, ps);
+      m[r] = m_new;
+#pragma unroll
+      for (int e = 0; e < C::kEPL; ++e) acc[r][e] *= corr;
     }
-    l = fmaf(l, corr, ps);
-    m = m_new;
-#pragma unroll
-    for (int e = 0; e < C::kEPL; ++e) acc[e] *= corr;
 #pragma unroll
     for (int g = 0; g < C::kG; ++g) {
       const int kk = ru + g * C::kNU;
@@ -247,42 +276,53 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
         float vf[C::kEPL];
         Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sv + kk * C::kRow + sl * 16), vf);
 #pragma unroll
-        for (int e = 0; e < C::kEPL; ++e) acc[e] = fmaf(p[g], vf[e], acc[e]);
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+          for (int e = 0; e < C::kEPL; ++e) acc[r][e] = fmaf(p[g][r], vf[e], acc[r][e]);
       }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->empty[st]));
   }
 
-  // Merge the row units of this CTA: (m, l) monoid, then write the partial.
-  float* red_m = red;                 // [kNU]
-  float* red_l = red + C::kNU;        // [kNU]
-  float* red_acc = red + 2 * C::kNU;  // [kNU][D]
-  if (sl == 0) {
-    red_m[ru] = m;
-    red_l[ru] = l;
-  }
+  // Merge the row units of this CTA: (m, l) monoid per query row, then write the partials.
+  float* red_m = red;                     // [kNU][R]
+  float* red_l = red + C::kNU * R;        // [kNU][R]
+  float* red_acc = red + 2 * C::kNU * R;  // [kNU][R][D]
 #pragma unroll
-  for (int e = 0; e < C::kEPL; ++e) red_acc[ru * D + sl * C::kEPL + e] = acc[e];
+  for (int r = 0; r < R; ++r) {
+    if (sl == 0) {
+      red_m[ru * R + r] = m[r];
+      red_l[ru * R + r] = l[r];
+    }
+#pragma unroll
+    for (int e = 0; e < C::kEPL; ++e) red_acc[(ru * R + r) * D + sl * C::kEPL + e] = acc[r][e];
+  }
   asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");
   if (hdr->abort_flag) return;
 
-  float mg = -INFINITY;
+  for (int i = threadIdx.x; i < rows * D; i += kDecWarps * 32) {
+    const int r = i / D, d = i - r * D;
+    float mg = -INFINITY;
 #pragma unroll
-  for (int u = 0; u < C::kNU; ++u) mg = fmaxf(mg, red_m[u]);
-  const float mg_safe = mg == -INFINITY ? 0.f : mg;
-  for (int d = threadIdx.x; d < D; d += kDecWarps * 32) {
+    for (int u = 0; u < C::kNU; ++u) mg = fmaxf(mg, red_m[u * R + r]);
+    const float mg_safe = mg == -INFINITY ? 0.f : mg;
     float o = 0.f;
 #pragma unroll
-    for (int u = 0; u < C::kNU; ++u) o = fmaf(ptx::ex2(red_m[u] - mg_safe), red_acc[u * D + d], o);
-    ws_O[d] = o;
+    for (int u = 0; u < C::kNU; ++u) o = fmaf(ptx::ex2(red_m[u * R + r] - mg_safe), red_acc[(u * R + r) * D + d], o);
+    ws_O(r)[d] = o;
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < rows) {
+    const int r = threadIdx.x;
+    float mg = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < C::kNU; ++u) mg = fmaxf(mg, red_m[u * R + r]);
+    const float mg_safe = mg == -INFINITY ? 0.f : mg;
     float lg = 0.f;
 #pragma unroll
-    for (int u = 0; u < C::kNU; ++u) lg = fmaf(ptx::ex2(red_m[u] - mg_safe), red_l[u], lg);
-    *ws_m = mg * kLn2;  // natural-log units, as in the page's equations (-inf stays -inf)
-    *ws_l = lg;
+    for (int u = 0; u < C::kNU; ++u) lg = fmaf(ptx::ex2(red_m[u * R + r] - mg_safe), red_l[u * R + r], lg);
+    *ws_m(r) = mg * kLn2;  // natural-log units, as in the page's equations (-inf stays -inf)
+    *ws_l(r) = lg;
   }
 }
 
@@ -290,8 +330,10 @@ constexpr int kCombThreads = 128;
 constexpr int kCombChunk = 1024;
 
 template <int D, int DT>
+// One CTA per query row (B*H*R of them, row-major like O); LSE may be null.
 __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const float* __restrict__ ws,
-                                                                      typename Elem<DT>::T* __restrict__ O, int BH,
+                                                                      typename Elem<DT>::T* __restrict__ O,
+                                                                      float* __restrict__ LSE, int BH,
                                                                       int n_splits) {
   __shared__ float w[kCombChunk];
   __shared__ float red[kCombThreads / 32];
@@ -343,26 +385,27 @@ __global__ void __launch_bounds__(kCombThreads) decode_combine_kernel(const floa
   }
   __syncthreads();
   if (tid < D) O[static_cast<size_t>(bh) * D + tid] = Elem<DT>::from_f32(o / s_lg);
+  if (LSE != nullptr && tid == 0) LSE[bh] = mg + logf(s_lg);  // natural log, like the forward's LSE
 }
 
-template <int D, int DT>
-cudaError_t launch_decode_t(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N,
-                            float scale, int n_splits, const LaunchCtx& ctx) {
+template <int D, int DT, int R>
+cudaError_t launch_decode_t(const void* q, const void* K, const void* V, void* O, float* LSE, float* ws, int BH,
+                            int rows, int N, float scale, int n_splits, const LaunchCtx& ctx) {
   using C = DecCfg<D, DT>;
   using T = typename Elem<DT>::T;
-  const size_t smem = 128 + kDecStages * kDecStageBytes + (2 * C::kNU + C::kNU * D) * sizeof(float);
-  auto kern = decode_split_kernel<D, DT>;
+  const size_t smem = 128 + kDecStages * kDecStageBytes + (2 * C::kNU * R + C::kNU * R * D) * sizeof(float);
+  auto kern = decode_split_kernel<D, DT, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(n_splits, BH);
   kern<<<grid, kDecThreads, smem, ctx.stream>>>(static_cast<const T*>(q), static_cast<const T*>(K),
-                                                static_cast<const T*>(V), ws, BH, N, n_splits, scale * kLog2e,
+                                                static_cast<const T*>(V), ws, BH, rows, N, n_splits, scale * kLog2e,
                                                 ctx.status, ctx.wait_budget_ns, ctx.inject);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(BH);
+  cfg.gridDim = dim3(BH * rows);
   cfg.blockDim = dim3(kCombThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = ctx.stream;
@@ -372,16 +415,22 @@ cudaError_t launch_decode_t(const void* q, const void* K, const void* V, void* O
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_combine_kernel<D, DT>, static_cast<const float*>(ws), static_cast<T*>(O),
-                            BH, n_splits);
+                            LSE, BH * rows, n_splits);
 }
 
 }  // namespace
 
-cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N, int D,
-                          float scale, int n_splits, int dtype, const LaunchCtx& ctx) {
+cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* LSE, float* ws, int BH,
+                          int rows, int N, int D, float scale, int n_splits, int dtype, const LaunchCtx& ctx) {
   if (BH > 65535) return cudaErrorNotSupported;  // grid.y limit of the split kernel
-#define FA_DEC(DD, TT) \
-  if (D == DD && dtype == TT) return launch_decode_t<DD, TT>(q, K, V, O, ws, BH, N, scale, n_splits, ctx);
+  if (rows < 1 || rows > kDecMaxRows) return cudaErrorNotSupported;
+  // query rows held per thread: 1, 2 or 4 (three rows run the four-row kernel with one padding row)
+#define FA_DEC(DD, TT)                                                                                   \
+  if (D == DD && dtype == TT) {                                                                          \
+    if (rows == 1) return launch_decode_t<DD, TT, 1>(q, K, V, O, LSE, ws, BH, rows, N, scale, n_splits, ctx); \
+    if (rows == 2) return launch_decode_t<DD, TT, 2>(q, K, V, O, LSE, ws, BH, rows, N, scale, n_splits, ctx); \
+    return launch_decode_t<DD, TT, 4>(q, K, V, O, LSE, ws, BH, rows, N, scale, n_splits, ctx);             \
+  }
   FA_DEC(64, kF32)
   FA_DEC(64, kF16)
   FA_DEC(64, kBF16)

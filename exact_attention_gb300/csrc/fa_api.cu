@@ -213,6 +213,36 @@ bool use_split(int BH, int M, int N, int causal, int num_sms) {
 std::atomic<uint32_t> g_epoch{0};
 std::atomic<int> g_inject{0};  // fa_debug_inject: consumed by the next decode launch
 
+// fa_decode / fa_decode_ex: R query rows per (batch, head), each against all N keys.
+fa_status decode_impl(const void* q, const void* Kcache, const void* Vcache, void* O, float* LSE, float* partial_ws,
+                      int B, int H, int R, int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream,
+                      const char* name) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, 1, N, D));
+  FA_TRY(check_scale(scale, false));
+  if (R < 1) return fail(FA_ERR_INVALID, "%s: R=%d query rows", name, R);
+  if (R > kDecMaxRows)
+    return fail(FA_ERR_UNSUPPORTED, "%s: R=%d query rows above %d (fa_fwd takes any number)", name, R, kDecMaxRows);
+  if (B * H == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  if (n_splits < 1 || n_splits > N || n_splits > 65535)
+    return fail(FA_ERR_INVALID, "n_splits=%d outside [1, min(N=%d, 65535)]", n_splits, N);
+  if (B * H > 65535) return fail(FA_ERR_UNSUPPORTED, "%s: B*H=%d above 65535", name, B * H);
+  FA_TRY(check_ptr(q, "q"));
+  FA_TRY(check_ptr(Kcache, "Kcache"));
+  FA_TRY(check_ptr(Vcache, "Vcache"));
+  FA_TRY(check_ptr(O, "O"));
+  FA_TRY(check_ptr(partial_ws, "partial_ws"));
+  if (LSE != nullptr) FA_TRY(check_ptr(LSE, "LSE"));
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  ctx.inject = g_inject.exchange(0);
+  cudaError_t e = launch_decode(q, Kcache, Vcache, O, LSE, partial_ws, B * H, R, N, D, scale, n_splits, dtype, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return FA_OK;
+}
+
 fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* LSE, void* ws, size_t ws_bytes, int B,
                    int H, int M, int N, int D, float scale, int causal, fa_dtype dtype, void* stream,
                    const char* name) {
@@ -301,6 +331,11 @@ size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits) {
   return static_cast<size_t>(B) * H * n_splits * (D + 2) * sizeof(float);
 }
 
+size_t fa_decode_ex_workspace_bytes(int B, int H, int R, int D, int n_splits) {
+  if (B <= 0 || H <= 0 || R <= 0 || D <= 0 || n_splits <= 0) return 0;
+  return static_cast<size_t>(B) * H * R * n_splits * (D + 2) * sizeof(float);
+}
+
 size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype) {
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return 0;
   DevState* st = nullptr;
@@ -352,26 +387,14 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 
 fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void* O, float* partial_ws, int B, int H,
                     int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream) {
-  FA_TRY(check_dtype(dtype));
-  FA_TRY(check_sizes(B, H, 1, N, D));
-  FA_TRY(check_scale(scale, false));
-  if (B * H == 0) return FA_OK;
-  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
-  if (n_splits < 1 || n_splits > N || n_splits > 65535)
-    return fail(FA_ERR_INVALID, "n_splits=%d outside [1, min(N=%d, 65535)]", n_splits, N);
-  if (B * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode: B*H=%d above 65535", B * H);
-  FA_TRY(check_ptr(q, "q"));
-  FA_TRY(check_ptr(Kcache, "Kcache"));
-  FA_TRY(check_ptr(Vcache, "Vcache"));
-  FA_TRY(check_ptr(O, "O"));
-  FA_TRY(check_ptr(partial_ws, "partial_ws"));
-  LaunchCtx ctx{};
-  FA_TRY(make_ctx(&ctx, stream));
-  ctx.inject = g_inject.exchange(0);
-  cudaError_t e = launch_decode(q, Kcache, Vcache, O, partial_ws, B * H, N, D, scale, n_splits, dtype, ctx);
-  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode: configuration not supported");
-  if (e != cudaSuccess) return cuda_fail(e, "fa_decode launch");
-  return FA_OK;
+  return decode_impl(q, Kcache, Vcache, O, nullptr, partial_ws, B, H, 1, N, D, scale, n_splits, dtype, stream,
+                     "fa_decode");
+}
+
+fa_status fa_decode_ex(const void* q, const void* Kcache, const void* Vcache, void* O, float* LSE, float* partial_ws,
+                       int B, int H, int R, int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream) {
+  return decode_impl(q, Kcache, Vcache, O, LSE, partial_ws, B, H, R, N, D, scale, n_splits, dtype, stream,
+                     "fa_decode_ex");
 }
 
 }  // extern "C"
@@ -443,7 +466,7 @@ fa_status fa_decode_static(const void* q, const void* Kcache, const void* Vcache
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
   ctx.inject = g_inject.exchange(0);
-  cudaError_t e = launch_decode(q, Kcache, Vcache, O, ws, B * H, N, D, scale, n_splits, dtype, ctx);
+  cudaError_t e = launch_decode(q, Kcache, Vcache, O, nullptr, ws, B * H, 1, N, D, scale, n_splits, dtype, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode_static: configuration not supported");
   if (e != cudaSuccess) return cuda_fail(e, "fa_decode_static launch");
   return FA_OK;

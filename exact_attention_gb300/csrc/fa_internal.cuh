@@ -43,8 +43,10 @@ struct LaunchCtx {
 };
 
 // ---- launchers (each returns a cudaError_t from the launch itself)
-cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* ws, int BH, int N, int D,
-                          float scale, int n_splits, int dtype, const LaunchCtx& ctx);
+// Decode: `rows` (1..kDecMaxRows) query rows per (batch, head); LSE may be null.
+constexpr int kDecMaxRows = 4;
+cudaError_t launch_decode(const void* q, const void* K, const void* V, void* O, float* LSE, float* ws, int BH,
+                          int rows, int N, int D, float scale, int n_splits, int dtype, const LaunchCtx& ctx);
 
 // Split schedule of the D = 64 forward: the caller's workspace holds one
 // partial-result slot and 8 ready flags per SM; ws == nullptr selects the classic schedule.

@@ -129,7 +129,8 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 size_t fa_bwd_workspace_bytes(int B, int H, int M);
 
 /*
- * Decode (flash decoding): one query row per (batch, head) against a KV cache.
+ * Decode (flash decoding): one query row per (batch, head) against a KV cache
+ * (fa_decode_ex below takes up to four rows and returns the LSE too).
  *
  * Follows "Flash decoding" (linear algebra for programmers, part 4),
  * "Overview of the algorithm": the keys are cut into n_splits chunks of
@@ -155,6 +156,38 @@ fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void*
 
 /* Bytes of scratch fa_decode needs: B*H*n_splits*(D+2) float32. */
 size_t fa_decode_workspace_bytes(int B, int H, int D, int n_splits);
+
+/*
+ * Decode of R query rows per (batch, head), with an optional LSE.
+ *
+ * The same split-and-combine as fa_decode, for R >= 1 query rows that all see
+ * the whole cache of their (batch, head) (no mask among them): for example the
+ * R query heads of grouped-query attention that share one K/V head, laid out
+ * as that head's rows. Each K and V vector read from HBM serves all R rows.
+ * fa_decode is this call with R = 1 and LSE = NULL.
+ *
+ *   q [B,H,R,D]                    input, dtype
+ *   Kcache, Vcache [B,H,N,D]       input, dtype
+ *   O [B,H,R,D]                    output, dtype
+ *   LSE [B,H,R]                    output, float32, natural log of the row's
+ *                                  softmax denominator over scaled scores
+ *                                  (m_g + ln l_g), or NULL for none
+ *   partial_ws                     caller-owned scratch of
+ *                                  fa_decode_ex_workspace_bytes(B,H,R,D,n_splits)
+ *                                  bytes; on return, float32, O_s
+ *                                  [B*H*R][n_splits][D], then m_s
+ *                                  [B*H*R][n_splits], then l_s, row
+ *                                  (b*H + h)*R + r
+ *   R                              1 <= R <= 4; R > 4 is FA_ERR_UNSUPPORTED
+ *                                  (fa_fwd with M = R takes any number of rows)
+ *   scale, n_splits                as for fa_decode
+ */
+fa_status fa_decode_ex(const void* q, const void* Kcache, const void* Vcache, void* O, float* LSE,
+                       float* partial_ws, int B, int H, int R, int N, int D, float scale, int n_splits,
+                       fa_dtype dtype, void* stream);
+
+/* Bytes of scratch fa_decode_ex needs: B*H*R*n_splits*(D+2) float32. */
+size_t fa_decode_ex_workspace_bytes(int B, int H, int R, int D, int n_splits);
 
 /*
  * Decode that allocates nothing and needs no workspace argument.
