@@ -421,6 +421,40 @@ def run_ours(args):
                             "peak_source": f"{peaks_src} bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products",
                             "traffic": None}}
 
+    # ---- grouped-query decode on its own: four query rows per K/V head of the same cache,
+    # with the LSE (fa_decode_ex); the cache is larger than L2, so no flush is needed
+    dec_rows = None
+    if world == 1:
+        R = 4
+        qr = dev(synth.normal(np.random.default_rng(7), (d["B"], d["H"], R, d["D"]), "bf16"), "bf16")
+        outr = torch.empty_like(qr)
+        lser = torch.empty((d["B"], d["H"], R), dtype=torch.float32, device="cuda")
+        wsr = torch.empty(fa.fa_decode_ex_workspace_bytes(d["B"], d["H"], R, d["D"], d["n_splits"]) // 4,
+                          dtype=torch.float32, device="cuda")
+
+        def run_rows():
+            check(fa.fa_decode_ex(qr, kc, vc, outr, lser, wsr, d["B"], d["H"], R, d["N"], d["D"],
+                                  1 / math.sqrt(d["D"]), d["n_splits"], fa.FA_BF16, stream), "fa_decode_ex")
+
+        for _ in range(3):
+            run_rows()
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(20):
+            run_rows()
+        b.record(stream)
+        torch.cuda.synchronize()
+        check(fa.fa_last_status(stream), "grouped-query decode")
+        tr = a.elapsed_time(b) / 20 / 1e3
+        gbs_r = dec_bytes() / tr / 1e9
+        dec_rows = {"config": f"bf16 B{d['B']} H{d['H']} (K/V heads) x 4 query rows, N{d['N']} D{d['D']}, n_splits "
+                              f"{d['n_splits']}, LSE written", "value": round(gbs_r, 1), "unit": "GB/s",
+                    "us_per_call": round(tr * 1e6, 1),
+                    "roofline": {"kernel": "decode_split_kernel<128,bf16,4 rows>", "bound": "hbm",
+                                 "achieved": round(gbs_r, 1), "peak": peak_bw, "unit": "GB/s",
+                                 "frac": round(gbs_r / peak_bw, 4), "peak_source": f"{peaks_src} copy bandwidth",
+                                 "traffic": None}}
+
     launches_per_step = 1 + (3 if have_bwd else 0) + 2
     traffic = load_traffic()
     line = {
@@ -474,6 +508,7 @@ def run_ours(args):
             "e2e": dec_e2e,
         },
         "f32": f32,
+        "decode_rows": dec_rows,
         "backward": None if bwd_tflops is None else {
             "value": round(bwd_tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(t_bwd / K * 1e3, 4),
             "flops": "2.5 x forward"},
