@@ -209,6 +209,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
       for (int e = 0; e < C::kEPL; ++e) qv[r][e] = 0.f;  // a padding row: computed, never written
     }
   }
+  // several rows: lane offsets of the butterfly and the lane (within the key's group) that ends
+  // up holding row r; with R > 1, m[0] and l[0] are the state of this lane's row my_row
+  constexpr int kO1 = C::kLPK / 2, kO2 = C::kLPK / 4;
+  static_assert(R == 1 || R == 2 || (R == 4 && kO2 >= 1), "decode rows");
+  auto row_lane = [](int r) { return R == 4 ? (r >> 1) * kO1 + (r & 1) * kO2 : r * kO1; };
+  const int group0 = lane - sl;  // first lane of this key's group
+  const int my_row = R == 1 ? 0 : (R == 2 ? ((sl & kO1) ? 1 : 0) : ((sl & kO1) ? 2 : 0) + ((sl & kO2) ? 1 : 0));
   float m[R], l[R];
   float acc[R][C::kEPL];
 #pragma unroll
@@ -227,58 +234,132 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
     const uint8_t* sk = ring + st * kDecStageBytes;
     const uint8_t* sv = sk + kDecStageBytes / 2;
 
-    float s[C::kG][R];
-#pragma unroll
-    for (int g = 0; g < C::kG; ++g) {
-      const int kk = ru + g * C::kNU;
-      float part[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) part[r] = 0.f;
-      if (kk < nk) {
-        float kf[C::kEPL];
-        Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sk + kk * C::kRow + sl * 16), kf);
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-          for (int e = 0; e < C::kEPL; ++e) part[r] = fmaf(qv[r][e], kf[e], part[r]);
+    if constexpr (R == 1) {
+      float s[C::kG][R];
+  #pragma unroll
+      for (int g = 0; g < C::kG; ++g) {
+        const int kk = ru + g * C::kNU;
+        float part[R];
+  #pragma unroll
+        for (int r = 0; r < R; ++r) part[r] = 0.f;
+        if (kk < nk) {
+          float kf[C::kEPL];
+          Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sk + kk * C::kRow + sl * 16), kf);
+  #pragma unroll
+          for (int r = 0; r < R; ++r)
+  #pragma unroll
+            for (int e = 0; e < C::kEPL; ++e) part[r] = fmaf(qv[r][e], kf[e], part[r]);
+        }
+  #pragma unroll
+        for (int r = 0; r < R; ++r) {
+  #pragma unroll
+          for (int o = C::kLPK / 2; o >= 1; o >>= 1) part[r] += __shfl_xor_sync(0xFFFFFFFFu, part[r], o);
+          s[g][r] = kk < nk ? part[r] : -INFINITY;
+        }
       }
-#pragma unroll
+      float p[C::kG][R];
+  #pragma unroll
       for (int r = 0; r < R; ++r) {
-#pragma unroll
-        for (int o = C::kLPK / 2; o >= 1; o >>= 1) part[r] += __shfl_xor_sync(0xFFFFFFFFu, part[r], o);
-        s[g][r] = kk < nk ? part[r] : -INFINITY;
+        float mb = s[0][r];
+  #pragma unroll
+        for (int g = 1; g < C::kG; ++g) mb = fmaxf(mb, s[g][r]);
+        const float m_new = fmaxf(m[r], mb);
+        const float m_safe = m_new == -INFINITY ? 0.f : m_new;
+        const float corr = ptx::ex2(m[r] - m_safe);
+        float ps = 0.f;
+  #pragma unroll
+        for (int g = 0; g < C::kG; ++g) {
+          p[g][r] = ptx::ex2(s[g][r] - m_safe);
+          ps += p[g][r];
+        }
+        l[r] = fmaf(l[r], corr, ps);
+        m[r] = m_new;
+  #pragma unroll
+        for (int e = 0; e < C::kEPL; ++e) acc[r][e] *= corr;
       }
-    }
-    float p[C::kG][R];
+  #pragma unroll
+      for (int g = 0; g < C::kG; ++g) {
+        const int kk = ru + g * C::kNU;
+        if (kk < nk) {
+          float vf[C::kEPL];
+          Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sv + kk * C::kRow + sl * 16), vf);
+  #pragma unroll
+          for (int r = 0; r < R; ++r)
+  #pragma unroll
+            for (int e = 0; e < C::kEPL; ++e) acc[r][e] = fmaf(p[g][r], vf[e], acc[r][e]);
+        }
+      }
+    } else {
+      // Several rows: a reduce-scatter butterfly over the key's lanes leaves each lane the full
+      // score of one row (my_row), so the online softmax runs once per lane; the weights are then
+      // broadcast from the lanes holding each row for the accumulator update. Every shuffle runs
+      // on all 32 lanes (kk differs between the key groups of a warp).
+      float sc[C::kG];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      float mb = s[0][r];
+      for (int g = 0; g < C::kG; ++g) {
+        const int kk = ru + g * C::kNU;
+        float part[R];
 #pragma unroll
-      for (int g = 1; g < C::kG; ++g) mb = fmaxf(mb, s[g][r]);
-      const float m_new = fmaxf(m[r], mb);
+        for (int r = 0; r < R; ++r) part[r] = 0.f;
+        if (kk < nk) {
+          float kf[C::kEPL];
+          Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sk + kk * C::kRow + sl * 16), kf);
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < C::kEPL; ++e) part[r] = fmaf(qv[r][e], kf[e], part[r]);
+        }
+        float c;
+        if constexpr (R == 2) {
+          const bool hi = (sl & kO1) != 0;
+          c = (hi ? part[1] : part[0]) + __shfl_xor_sync(0xFFFFFFFFu, hi ? part[0] : part[1], kO1);
+#pragma unroll
+          for (int o = kO1 / 2; o >= 1; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+        } else {
+          const bool hi = (sl & kO1) != 0, lo = (sl & kO2) != 0;
+          const float a0 = (hi ? part[2] : part[0]) + __shfl_xor_sync(0xFFFFFFFFu, hi ? part[0] : part[2], kO1);
+          const float a1 = (hi ? part[3] : part[1]) + __shfl_xor_sync(0xFFFFFFFFu, hi ? part[1] : part[3], kO1);
+          c = (lo ? a1 : a0) + __shfl_xor_sync(0xFFFFFFFFu, lo ? a0 : a1, kO2);
+#pragma unroll
+          for (int o = kO2 / 2; o >= 1; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+        }
+        sc[g] = kk < nk ? c : -INFINITY;
+      }
+      float mb = sc[0];
+#pragma unroll
+      for (int g = 1; g < C::kG; ++g) mb = fmaxf(mb, sc[g]);
+      const float m_new = fmaxf(m[0], mb);
       const float m_safe = m_new == -INFINITY ? 0.f : m_new;
-      const float corr = ptx::ex2(m[r] - m_safe);
+      const float corr = ptx::ex2(m[0] - m_safe);
+      float pw[C::kG];
       float ps = 0.f;
 #pragma unroll
       for (int g = 0; g < C::kG; ++g) {
-        p[g][r] = ptx::ex2(s[g][r] - m_safe);
-        ps += p[g][r];
+        pw[g] = ptx::ex2(sc[g] - m_safe);
+        ps += pw[g];
       }
-      l[r] = fmaf(l[r], corr, ps);
-      m[r] = m_new;
+      l[0] = fmaf(l[0], corr, ps);  // this lane's row
+      m[0] = m_new;
 #pragma unroll
-      for (int e = 0; e < C::kEPL; ++e) acc[r][e] *= corr;
-    }
+      for (int r = 0; r < R; ++r) {
+        const float cr = __shfl_sync(0xFFFFFFFFu, corr, group0 + row_lane(r));
 #pragma unroll
-    for (int g = 0; g < C::kG; ++g) {
-      const int kk = ru + g * C::kNU;
-      if (kk < nk) {
-        float vf[C::kEPL];
-        Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sv + kk * C::kRow + sl * 16), vf);
+        for (int e = 0; e < C::kEPL; ++e) acc[r][e] *= cr;
+      }
 #pragma unroll
-        for (int r = 0; r < R; ++r)
+      for (int g = 0; g < C::kG; ++g) {
+        const int kk = ru + g * C::kNU;
+        float pr[R];
 #pragma unroll
-          for (int e = 0; e < C::kEPL; ++e) acc[r][e] = fmaf(p[g][r], vf[e], acc[r][e]);
+        for (int r = 0; r < R; ++r) pr[r] = __shfl_sync(0xFFFFFFFFu, pw[g], group0 + row_lane(r));
+        if (kk < nk) {
+          float vf[C::kEPL];
+          Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sv + kk * C::kRow + sl * 16), vf);
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < C::kEPL; ++e) acc[r][e] = fmaf(pr[r], vf[e], acc[r][e]);
+        }
       }
     }
     __syncwarp();
@@ -289,12 +370,17 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
   float* red_m = red;                     // [kNU][R]
   float* red_l = red + C::kNU * R;        // [kNU][R]
   float* red_acc = red + 2 * C::kNU * R;  // [kNU][R][D]
+  if (R == 1) {
+    if (sl == 0) {
+      red_m[ru] = m[0];
+      red_l[ru] = l[0];
+    }
+  } else if (sl == row_lane(my_row)) {  // one lane per row holds its (m, l)
+    red_m[ru * R + my_row] = m[0];
+    red_l[ru * R + my_row] = l[0];
+  }
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    if (sl == 0) {
-      red_m[ru * R + r] = m[r];
-      red_l[ru * R + r] = l[r];
-    }
 #pragma unroll
     for (int e = 0; e < C::kEPL; ++e) red_acc[(ru * R + r) * D + sl * C::kEPL + e] = acc[r][e];
   }
