@@ -22,6 +22,8 @@ from ._binding import (  # noqa: F401
     fa_decode,
     fa_decode_static,
     fa_decode_ex,
+    fa_fwd_host,
+    fa_fwd_host_workspace_bytes,
     fa_decode_ex_workspace_bytes,
     fa_debug_inject,
     fa_decode_workspace_bytes,

@@ -26,6 +26,8 @@ EXPORTS = (
     "fa_fwd",
     "fa_fwd_ws",
     "fa_fwd_workspace_bytes",
+    "fa_fwd_host",
+    "fa_fwd_host_workspace_bytes",
     "fa_bwd",
     "fa_bwd_workspace_bytes",
     "fa_decode",
@@ -75,6 +77,10 @@ def lib() -> ctypes.CDLL:
     L.fa_decode_static.restype = st
     L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_fwd_host.argtypes = [vp] * 6 + [ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_host.restype = st
+    L.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    L.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     L.fa_decode_ex.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, vp]
     L.fa_decode_ex.restype = st
     L.fa_decode_ex_workspace_bytes.argtypes = [i, i, i, i, i]
@@ -124,6 +130,15 @@ def fa_fwd_ws(Q, K, V, O, LSE, workspace, workspace_bytes, B, H, M, N, D, scale,
 
 def fa_fwd_workspace_bytes(B, H, M, N, D, causal, dtype) -> int:
     return lib().fa_fwd_workspace_bytes(B, H, M, N, D, int(causal), int(dtype))
+
+
+def fa_fwd_host(hQ, hK, hV, hO, hLSE, dev_ws, dev_ws_bytes, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
+    return lib().fa_fwd_host(_ptr(hQ), _ptr(hK), _ptr(hV), _ptr(hO), _ptr(hLSE), _ptr(dev_ws), dev_ws_bytes, B, H, M,
+                             N, D, float(scale), int(causal), int(dtype), _stream(stream))
+
+
+def fa_fwd_host_workspace_bytes(B, H, M, N, D, causal, dtype) -> int:
+    return lib().fa_fwd_host_workspace_bytes(B, H, M, N, D, int(causal), int(dtype))
 
 
 

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <vector>
 
 #include "../../include/fa.h"
 #include "fa_internal.cuh"
@@ -490,6 +491,168 @@ fa_status fa_last_status(void* stream) {
   if (h.code == kStatusTimeout)
     return fail(FA_ERR_TIMEOUT, "kernel %s gave up wait site %u in block %u", kn, h.site, h.block);
   return fail(FA_ERR_CUDA, "kernel %s reported status %u (site %u, block %u)", kn, h.code, h.site, h.block);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward on host buffers, with the copies overlapped with the kernels.
+//
+// The (batch, head) heads are cut into kHostDefaultChunks chunks (FA_HOST_CHUNKS=1..8 in the
+// environment overrides it). Three internal
+// streams of the device carry the copies in, the kernels and the copies out, so
+// chunk c's inputs travel while chunk c-1 is computed and chunk c-2's output
+// travels back; events order each chunk's three steps, and the caller's stream
+// is joined at entry and at exit, so the call is ordered on it like any other.
+
+namespace {
+
+constexpr int kHostChunks = 8;         // events kept per device
+constexpr int kHostDefaultChunks = 4;  // measured best at B4 H12 N2048 D64: the copies in and out share
+                                       // the host link (about 220-260 GB/s together), and a chunk's
+                                       // kernel has a fixed cost of about 15 us, so more chunks lose
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, finish = nullptr;
+  cudaEvent_t in[kHostChunks] = {}, done[kHostChunks] = {};
+};
+
+HostPipe g_pipe[kMaxDevices];
+std::mutex g_pipe_mutex;  // the internal streams are shared by every caller of a device
+
+fa_status host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device ordinal %d out of range", dev);
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    for (cudaStream_t* s : {&hp.h2d, &hp.comp, &hp.d2h}) {
+      e = cudaStreamCreateWithFlags(s, cudaStreamNonBlocking);
+      if (e != cudaSuccess) return cuda_fail(e, "creating the copy/compute streams");
+    }
+    std::vector<cudaEvent_t*> evs = {&hp.start, &hp.finish};
+    for (int c = 0; c < kHostChunks; ++c) {
+      evs.push_back(&hp.in[c]);
+      evs.push_back(&hp.done[c]);
+    }
+    for (cudaEvent_t* ev : evs) {
+      e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "creating the pipeline events");
+    }
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
+// Device workspace of fa_fwd_host: the forward's own workspace for the largest chunk, then
+// Q, K, V, O and LSE of the whole problem, each 256-byte aligned.
+struct HostLayout {
+  int chunks = 0;
+  size_t split = 0, q = 0, k = 0, v = 0, o = 0, lse = 0, total = 0;
+};
+
+HostLayout host_layout(int B, int H, int M, int N, int D, int causal, fa_dtype dtype) {
+  HostLayout L;
+  const long long BH = static_cast<long long>(B) * H;
+  int want = kHostDefaultChunks;
+  if (const char* e = std::getenv("FA_HOST_CHUNKS")) {  // 1..8
+    const int v = std::atoi(e);
+    if (v >= 1 && v <= kHostChunks) want = v;
+  }
+  L.chunks = static_cast<int>(BH < want ? BH : want);
+  const int hi = static_cast<int>((BH + L.chunks - 1) / L.chunks), lo = static_cast<int>(BH / L.chunks);
+  const size_t w1 = fa_fwd_workspace_bytes(1, hi, M, N, D, causal, dtype);
+  const size_t w2 = lo > 0 ? fa_fwd_workspace_bytes(1, lo, M, N, D, causal, dtype) : 0;
+  const size_t es = dtype == FA_F32 ? 4 : 2;
+  const size_t qb = static_cast<size_t>(BH) * M * D * es, kb = static_cast<size_t>(BH) * N * D * es;
+  L.split = 0;
+  L.q = align256(w1 > w2 ? w1 : w2);
+  L.k = L.q + align256(qb);
+  L.v = L.k + align256(kb);
+  L.o = L.v + align256(kb);
+  L.lse = L.o + align256(qb);
+  L.total = L.lse + align256(static_cast<size_t>(BH) * M * sizeof(float));
+  return L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fa_fwd_host_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype) {
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || D <= 0) return 0;
+  if (check_dtype(dtype) != FA_OK) return 0;
+  return host_layout(B, H, M, N, D, causal, dtype).total;
+}
+
+fa_status fa_fwd_host(const void* hQ, const void* hK, const void* hV, void* hO, float* hLSE, void* dev_ws,
+                      size_t dev_ws_bytes, int B, int H, int M, int N, int D, float scale, int causal, fa_dtype dtype,
+                      void* stream) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, M, N, D));
+  FA_TRY(check_scale(scale, true));
+  if (B * H == 0 || M == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  // what the forward supports, checked before anything is queued
+  if ((D != 64 && D != 128) || (dtype == FA_F32 && D != 64))
+    return fail(FA_ERR_UNSUPPORTED, "fa_fwd_host: D=%d not supported for this dtype", D);
+  if (hQ == nullptr || hK == nullptr || hV == nullptr || hO == nullptr)
+    return fail(FA_ERR_INVALID, "fa_fwd_host: a host buffer is NULL");
+  FA_TRY(check_ptr(dev_ws, "dev_ws"));
+  const HostLayout L = host_layout(B, H, M, N, D, causal, dtype);
+  if (dev_ws_bytes < L.total)
+    return fail(FA_ERR_INVALID, "fa_fwd_host: dev_ws of %zu bytes, %zu needed", dev_ws_bytes, L.total);
+  HostPipe* hp = nullptr;
+  std::lock_guard<std::mutex> lock(g_pipe_mutex);
+  FA_TRY(host_pipe(&hp));
+  char* ws = static_cast<char*>(dev_ws);
+  const size_t es = dtype == FA_F32 ? 4 : 2;
+  const size_t qrow = static_cast<size_t>(M) * D * es, krow = static_cast<size_t>(N) * D * es;  // per head
+  const int BH = B * H;
+  cudaStream_t user = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaEventRecord(hp->start, user);
+  for (cudaStream_t s : {hp->h2d, hp->comp, hp->d2h})
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_host: joining the caller's stream");
+  for (int c = 0; c < L.chunks; ++c) {
+    const int h0 = static_cast<int>(static_cast<long long>(c) * BH / L.chunks);
+    const int h1 = static_cast<int>(static_cast<long long>(c + 1) * BH / L.chunks);
+    const int nh = h1 - h0;
+    char* dq = ws + L.q + h0 * qrow;
+    char* dk = ws + L.k + h0 * krow;
+    char* dv = ws + L.v + h0 * krow;
+    char* dout = ws + L.o + h0 * qrow;
+    float* dl = reinterpret_cast<float*>(ws + L.lse) + static_cast<size_t>(h0) * M;
+    e = cudaMemcpyAsync(dq, static_cast<const char*>(hQ) + h0 * qrow, nh * qrow, cudaMemcpyHostToDevice, hp->h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dk, static_cast<const char*>(hK) + h0 * krow, nh * krow, cudaMemcpyHostToDevice, hp->h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dv, static_cast<const char*>(hV) + h0 * krow, nh * krow, cudaMemcpyHostToDevice, hp->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in[c], hp->h2d);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->comp, hp->in[c], 0);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_host: copy in");
+    const fa_status s = fwd_impl(dq, dk, dv, dout, hLSE != nullptr ? dl : nullptr, ws + L.split, L.q, 1, nh, M, N, D,
+                                 scale, causal, dtype, hp->comp, "fa_fwd_host");
+    if (s != FA_OK) return s;
+    e = cudaEventRecord(hp->done[c], hp->comp);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->done[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<char*>(hO) + h0 * qrow, dout, nh * qrow, cudaMemcpyDeviceToHost, hp->d2h);
+    if (e == cudaSuccess && hLSE != nullptr)
+      e = cudaMemcpyAsync(hLSE + static_cast<size_t>(h0) * M, dl, static_cast<size_t>(nh) * M * sizeof(float),
+                          cudaMemcpyDeviceToHost, hp->d2h);
+    if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_host: copy out");
+  }
+  e = cudaEventRecord(hp->finish, hp->d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(user, hp->finish, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_host: joining the caller's stream");
+  return FA_OK;
 }
 
 }  // extern "C"

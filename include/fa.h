@@ -105,6 +105,42 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
                     void* stream);
 
 /*
+ * The forward on HOST buffers: copies in, computes and copies out, overlapped.
+ *
+ * For callers whose Q, K, V live in host memory and who want O (and LSE) back
+ * there. The (batch, head) heads are cut into 4 chunks (FA_HOST_CHUNKS=1..8 in
+ * the environment overrides that); the library's
+ * own copy and compute streams for the device move chunk c in while chunk c-1
+ * is computed (same kernels and results as fa_fwd_ws) and chunk c-2's output
+ * travels back. The call is asynchronous and ordered on `stream`: work queued
+ * on `stream` before it happens first, and `stream` waits for the last copy
+ * out before anything queued after it. Not for stream capture (the internal
+ * streams and events are not part of a capture).
+ *
+ *   hQ [B,H,M,D], hK, hV [B,H,N,D]   host inputs, dtype; page-locked
+ *                                     (cudaHostAlloc / cudaHostRegister) for
+ *                                     the copies to overlap, else they stage
+ *   hO [B,H,M,D]                      host output, dtype
+ *   hLSE [B,H,M]                      host output, float32, or NULL
+ *   dev_ws, dev_ws_bytes              device workspace of at least
+ *                                     fa_fwd_host_workspace_bytes(...) bytes,
+ *                                     16-byte aligned, zero-filled before its
+ *                                     first use; it holds the device copies of
+ *                                     Q, K, V, O, LSE and the forward's own
+ *                                     workspace; two calls must not share it
+ *                                     at the same time
+ *   the rest                          as for fa_fwd
+ * Errors as fa_fwd, plus FA_ERR_INVALID for a NULL host buffer or a small
+ * workspace; arguments are checked before anything is queued.
+ */
+fa_status fa_fwd_host(const void* hQ, const void* hK, const void* hV, void* hO, float* hLSE, void* dev_ws,
+                      size_t dev_ws_bytes, int B, int H, int M, int N, int D, float scale, int causal,
+                      fa_dtype dtype, void* stream);
+
+/* Bytes of device workspace fa_fwd_host needs (0 on bad sizes or dtype). */
+size_t fa_fwd_host_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype);
+
+/*
  * Backward pass: gradients of sum(dO o O).
  *
  * Follows "06: Fused attention" (attn_bwd_delta, attn_bwd_dkdv, attn_bwd_dq)

@@ -91,6 +91,20 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert fa.fa_set_wait_budget_ns(10) == fa.FA_ERR_INVALID
     assert fa.fa_debug_inject(7) == fa.FA_ERR_INVALID
     assert fa.fa_debug_inject(0) == fa.FA_OK  # cancels nothing pending; host-only
+    # host-buffer forward: NULL host buffers, a head dimension it cannot run, bad scale
+    assert fa.fa_fwd_host(None, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 64, 0.1, 0, fa.FA_F16, 0) == \
+        fa.FA_ERR_INVALID
+    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 96, 0.1, 0, fa.FA_F16, 0) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 128, 0.1, 0, fa.FA_F32, 0) == \
+        fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 64, 0.0, 0, fa.FA_F16, 0) == \
+        fa.FA_ERR_INVALID
+    # decode with rows: R = 0 invalid, R = 5 unsupported
+    assert fa.fa_decode_ex(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 1, 0, 100, 128, 0.1, 4, fa.FA_BF16, 0) == \
+        fa.FA_ERR_INVALID
+    assert fa.fa_decode_ex(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 1, 5, 100, 128, 0.1, 4, fa.FA_BF16, 0) == \
+        fa.FA_ERR_UNSUPPORTED
 
 
 def test_empty_problems_are_no_ops(lib):
@@ -98,3 +112,4 @@ def test_empty_problems_are_no_ops(lib):
     assert fa.fa_fwd(None, None, None, None, None, 0, 4, 8, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_OK
     assert fa.fa_fwd(None, None, None, None, None, 2, 4, 0, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_OK
     assert fa.fa_decode(None, None, None, None, None, 0, 4, 8, 64, 0.1, 1, fa.FA_F16, 0) == fa.FA_OK
+    assert fa.fa_fwd_host(None, None, None, None, None, None, 0, 0, 4, 8, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_OK

@@ -180,3 +180,58 @@ def test_forward_f32_without_workspace(causal):
                workspace=False)
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
     check_heads((q, k, v), to_f64(out), to_f64(lse), "f32", causal, 0.125, rel_l2=REL_L2_F32)
+
+
+HOST_CASES = [
+    # B, H, M, N, D, dtype, causal
+    (1, 1, 256, 300, 64, "f16", False),    # one head: one chunk
+    (2, 3, 300, 200, 64, "bf16", True),    # six heads: six chunks, ragged M and N
+    (3, 5, 700, 1500, 64, "f16", False),   # 15 heads over 8 chunks (two sizes)
+    (2, 2, 512, 512, 128, "f16", True),    # D = 128
+    (1, 3, 256, 384, 64, "f32", False),    # f32 (3xTF32 path)
+]
+
+
+@pytest.mark.parametrize("B,H,M,N,D,dtype,causal", HOST_CASES)
+@pytest.mark.parametrize("pinned", [True, False])
+def test_forward_host_buffers(B, H, M, N, D, dtype, causal, pinned):
+    """fa_fwd_host: host inputs in, host O and LSE out, chunked over heads with the copies
+    overlapped; same results as the device forward (checked against the oracle)."""
+    import torch
+    scale = 0.125
+    q, k, v = synth.attention_inputs(B, H, M, N, D, dtype, seed=B * H + M)
+    hq, hk, hv = (to_device(x, dtype).cpu() for x in (q, k, v))
+    ho, hl = torch.empty_like(hq), torch.empty((B, H, M), dtype=torch.float32)
+    if pinned:
+        hq, hk, hv, ho, hl = (t.pin_memory() for t in (hq, hk, hv, ho, hl))
+    dt = {"f32": fa.FA_F32, "f16": fa.FA_F16, "bf16": fa.FA_BF16}[dtype]
+    nbytes = fa.fa_fwd_host_workspace_bytes(B, H, M, N, D, causal, dt)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(2):  # the second call reuses the workspace
+        s = fa.fa_fwd_host(hq, hk, hv, ho, hl, ws, nbytes, B, H, M, N, D, scale, causal, dt)
+        assert s == fa.FA_OK, fa.fa_last_error_message()
+        torch.cuda.synchronize()
+        assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+        check_heads((q, k, v), to_f64(ho), to_f64(hl), dtype, causal, scale,
+                    rel_l2=REL_L2_F32 if dtype == "f32" else None)
+
+
+def test_forward_host_buffers_without_lse_and_checks():
+    import torch
+    B, H, M, N, D = 2, 2, 256, 256, 64
+    q, k, v = synth.attention_inputs(B, H, M, N, D, "f16", seed=4)
+    hq, hk, hv = (to_device(x, "f16").cpu().pin_memory() for x in (q, k, v))
+    ho = torch.empty_like(hq).pin_memory()
+    nbytes = fa.fa_fwd_host_workspace_bytes(B, H, M, N, D, 0, fa.FA_F16)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    assert fa.fa_fwd_host(hq, hk, hv, ho, None, ws, nbytes, B, H, M, N, D, 0.125, 0, fa.FA_F16) == fa.FA_OK
+    torch.cuda.synchronize()
+    ref = [oracle.forward(f64(q[b, h], "f16"), f64(k[b, h], "f16"), f64(v[b, h], "f16"), 0.125, False)[0]
+           for b in range(B) for h in range(H)]
+    assert_close(to_f64(ho).reshape(B * H, M, D), np.stack(ref), TOL_O["f16"], "host O without LSE")
+    # a small workspace or a NULL host buffer is rejected before anything is queued
+    assert fa.fa_fwd_host(hq, hk, hv, ho, None, ws, nbytes - 256, B, H, M, N, D, 0.125, 0, fa.FA_F16) == \
+        fa.FA_ERR_INVALID
+    assert fa.fa_fwd_host(hq, None, hv, ho, None, ws, nbytes, B, H, M, N, D, 0.125, 0, fa.FA_F16) == fa.FA_ERR_INVALID
+    assert fa.fa_fwd_host(hq, hk, hv, ho, None, ws, nbytes, B, H, M, N, 96, 0.125, 0, fa.FA_F16) == \
+        fa.FA_ERR_UNSUPPORTED
