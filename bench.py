@@ -510,7 +510,14 @@ def run_ours(args):
         "decode_rows": dec_rows,
         "backward": None if bwd_tflops is None else {
             "value": round(bwd_tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(t_bwd / K * 1e3, 4),
-            "flops": "2.5 x forward"},
+            "flops": "2.5 x forward",
+            # the whole call (delta, dK/dV, dQ) against the tensor peak; traffic is the dK/dV
+            # kernel's (the larger share of the call) from one ncu capture of this workload
+            "roofline": {"kernel": "bwd_dkdv64_kernel<f16,non-causal> + bwd_dq_kernel<64,f16,non-causal>",
+                         "bound": "tensor", "achieved": round(bwd_tflops / world, 2), "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": round(bwd_tflops / world / peak_tf, 4),
+                         "peak_source": f"{peaks_src} bf16 burst (fp16 dense rate equals bf16)",
+                         "traffic": traffic.get("bwd_dkdv")}},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,
