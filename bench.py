@@ -591,6 +591,7 @@ PROFILE_CASES = {
     "fwd": dict(B=16, H=16, M=4096, N=4096, D=64, dtype="f16"),     # Q/K/V 0.4 GB
     "decode": dict(B=8, H=8, N=32768, D=128, n_splits=64, dtype="bf16"),  # K/V 1.07 GB
     "bwd": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # Q/K/V/O/dO 0.34 GB
+    "decode_rows": dict(B=8, H=8, N=32768, D=128, n_splits=64, rows=4, dtype="bf16"),  # K/V 1.07 GB
 }
 
 
@@ -620,12 +621,14 @@ def run_profile(kind: str, launches: int = 5):
         for _ in range(launches):
             fa.backward(q, k, v, o, do, lse, 0.125, False)
     else:
-        q = torch.randn((c["B"], c["H"], 1, c["D"]), generator=g, device="cuda").bfloat16()
+        q = torch.randn((c["B"], c["H"], c.get("rows", 1), c["D"]), generator=g, device="cuda").bfloat16()
         kc = torch.randn((c["B"], c["H"], c["N"], c["D"]), generator=g, device="cuda").bfloat16()
         vc = torch.randn_like(kc)
         out = torch.empty_like(q)
         for _ in range(launches):
-            out, ws = fa.decode(q, kc, vc, 1 / math.sqrt(c["D"]), c["n_splits"], out=out)
+            res = fa.decode(q, kc, vc, 1 / math.sqrt(c["D"]), c["n_splits"], out=out,
+                            lse=True if "rows" in c else None)
+            out = res[0]
     torch.cuda.synchronize()
     s = fa.fa_last_status()
     if s != fa.FA_OK:
