@@ -112,7 +112,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
   extern __shared__ __align__(128) uint8_t smem_raw[];
   DecSmemHdr* hdr = reinterpret_cast<DecSmemHdr*>(smem_raw);
   uint8_t* ring = smem_raw + 128;  // stage st: K at ring + st*kDecStageBytes, V right after K
-  float* red = reinterpret_cast<float*>(ring + kDecStages * kDecStageBytes);  // merge scratch
+  // merge scratch: the ring itself, once every compute warp has read its last stage (saves the
+  // shared memory that would cost a resident CTA per SM with several rows)
+  float* red = reinterpret_cast<float*>(ring);
 
   const int split = blockIdx.x;
   const int bh = blockIdx.y;
@@ -370,6 +372,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
   float* red_m = red;                     // [kNU][R]
   float* red_l = red + C::kNU * R;        // [kNU][R]
   float* red_acc = red + 2 * C::kNU * R;  // [kNU][R][D]
+  asm volatile("bar.sync 1, %0;" ::"r"(kDecWarps * 32) : "memory");  // the ring is no longer read
   if (R == 1) {
     if (sl == 0) {
       red_m[ru] = m[0];
@@ -479,7 +482,9 @@ cudaError_t launch_decode_t(const void* q, const void* K, const void* V, void* O
                             int rows, int N, float scale, int n_splits, const LaunchCtx& ctx) {
   using C = DecCfg<D, DT>;
   using T = typename Elem<DT>::T;
-  const size_t smem = 128 + kDecStages * kDecStageBytes + (2 * C::kNU * R + C::kNU * R * D) * sizeof(float);
+  constexpr size_t kRed = (2 * C::kNU * R + C::kNU * R * D) * sizeof(float);  // merge scratch, over the ring
+  static_assert(kRed <= static_cast<size_t>(kDecStages) * kDecStageBytes, "decode merge scratch");
+  const size_t smem = 128 + static_cast<size_t>(kDecStages) * kDecStageBytes;
   auto kern = decode_split_kernel<D, DT, R>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
