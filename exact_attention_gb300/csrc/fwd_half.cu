@@ -30,13 +30,13 @@
 // scores' first 64 columns.
 //
 // O is divided by the sum of the half-rounded weights that multiplied V, so it
-// is a weighted mean of V rows; LSE uses the exact f32 sum. For D = 64 the
-// rounded sum comes from the MMA itself: V is extended by 16 columns of ones
-// (a constant shared-memory chunk), so O_t has 80 columns and column 64 holds
-// sum(P). For D = 128 tensor memory is full and the sum is formed in registers.
+// is a weighted mean of V rows (that sum is formed in registers); LSE uses the
+// exact f32 sum.
 //
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+DO),
-// O1 [384,384+DO), DO = 80 (D = 64) or 128.
+// This file serves D = 128; D = 64 has its own kernel (fwd_d64.cu), whose
+// tensor-memory plan only fits when D = 64.
+//
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512).
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -68,14 +68,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D>
 struct FwdCfg {
+  static_assert(D == 128, "this kernel serves D = 128");
   static constexpr int kDC = D / 64;                       // 64-column chunks
   static constexpr int kTileBytes = kDC * kChunk;          // one Q tile / K block / V block
-  static constexpr int kStages = D == 64 ? 4 : 2;          // K/V ring depth
-  static constexpr int kQBuf = D == 64 ? 2 : 1;            // Q pair buffers
-  static constexpr bool kOnesSum = D == 64;                // row sum from a ones block of V
-  static constexpr int kDO = kOnesSum ? D + 16 : D;        // O columns in tensor memory
-  static constexpr int kOnesOff = kQBuf * 2 * kTileBytes + kStages * 2 * kTileBytes;
-  static constexpr int kSmemData = kOnesOff + (kOnesSum ? kChunk : 0);
+  static constexpr int kStages = 2;                        // K/V ring depth
+  static constexpr int kQBuf = 1;                          // Q pair buffers
+  static constexpr int kDO = D;                            // O columns in tensor memory
+  static constexpr int kSmemData = kQBuf * 2 * kTileBytes + kStages * 2 * kTileBytes;
   static constexpr int kSmemBytes = 1024 + 1024 + kSmemData;  // header + alignment slack + data
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
@@ -118,11 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   FwdHdr* hdr = reinterpret_cast<FwdHdr*>(smem_raw);
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
   const uint32_t data_u32 = (raw_u32 + 1024u + 1023u) & ~1023u;  // 1024-aligned for the swizzle atoms
-  // data layout: Q[qbuf][tile], then stages (K, V), then the ones chunk (D = 64)
+  // data layout: Q[qbuf][tile], then stages (K, V)
   auto q_addr = [&](int qb, int t) { return data_u32 + (qb * 2 + t) * C::kTileBytes; };
   auto k_addr = [&](int st) { return data_u32 + C::kQBuf * 2 * C::kTileBytes + st * 2 * C::kTileBytes; };
   auto v_addr = [&](int st) { return k_addr(st) + C::kTileBytes; };
-  const uint32_t ones_addr = data_u32 + C::kOnesOff;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -146,12 +144,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&hdr->mma_done), 1);
     hdr->abort_flag = 0;
     ptx::fence_mbar_init();
-  }
-  if (C::kOnesSum) {  // 16 KB of ones: the extra B columns whose products sum P
-    const uint32_t one2 = BF16 ? 0x3F803F80u : 0x3C003C00u;
-    uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (ones_addr - raw_u32));
-    for (int i = threadIdx.x; i < kChunk / 4; i += kThreads) ones[i] = one2;
-    ptx::fence_proxy_async_smem();  // make the generic-proxy stores visible to the tensor core
   }
   if (warp == kWarpMma) {
     ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
@@ -234,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       };
       auto pv = [&](int t, int st, bool accumulate) {
-        // the second 64-column group of B is the next V chunk (D = 128) or the ones chunk (D = 64)
-        const uint32_t lbo = C::kOnesSum ? ones_addr - v_addr(st) : kChunk;
+        // the second 64-column group of B is the next V chunk
+        const uint32_t lbo = kChunk;
         const uint64_t b0 = ptx::sdesc_sw128(v_addr(st), lbo, 1024);
         const uint32_t d = tmem + 2 * kBN + t * 128;
         const uint32_t p = tmem + t * kBN;
@@ -298,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    constexpr bool kRounded = !C::kOnesSum;  // rounded row sum formed in registers
+    constexpr bool kRounded = true;  // rounded row sum formed in registers
     const int t = warp >> 2;          // which tile of the pair
     const int wq = warp & 3;          // TMEM lane quarter
     const uint32_t lane_sel = static_cast<uint32_t>(wq * 32) << 16;
@@ -404,12 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       o_ph ^= 1u;
       ptx::tc_fence_after();
-      if (C::kOnesSum) {  // column D of O holds sum(P) accumulated by the MMA
-        uint32_t s1[16];
-        ptx::tmem_ld16(tO + D, s1);
-        ptx::tmem_wait_ld16(s1);
-        l = __uint_as_float(s1[0]);
-      }
       const float inv = 1.f / l;
       const bool valid = row < M;
       const size_t orow = (static_cast<size_t>(ti.bh) * M + (valid ? row : 0)) * D;
