@@ -69,9 +69,14 @@ def test_forward_multihead_fp16_workload(N):
 
 
 def test_forward_fp16_error_magnitude_matches_the_pages():
-    """At B=4, H=12, M=N=2048, D=64 fp16 the pages print rel L2 2.819e-4 and max abs
-    1.098e-4 for an fp16 kernel against an fp32 reference (output rounding
-    dominates). Ours against the fp64 oracle must be of the same order."""
+    """At B=4, H=12, M=N=2048, D=64 fp16 the flash-attention README's "Accuracy" table
+    (tests/golden/fp16_forward_error_magnitudes.json) prints rel L2 2.819e-4 and max abs
+    1.098e-4 for an fp16 kernel against an fp32 reference (output rounding dominates).
+    Ours against the fp64 oracle must be of the same order."""
+    import json
+    import os
+    pr = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fp16_forward_error_magnitudes.json")))
+    pr = pr["printed"]
     inputs, out, lse = run_fwd(4, 12, 2048, 2048, 64, "f16", False, 0.125, seed=0)
     q, k, v = inputs
     num = den = 0.0
@@ -82,7 +87,7 @@ def test_forward_fp16_error_magnitude_matches_the_pages():
         den += float(np.sum(ro ** 2))
         mx = max(mx, float(np.max(np.abs(out[b, h] - ro))))
     rel = math.sqrt(num / den)
-    assert rel <= 2 * 2.819e-4 and mx <= 2 * 1.098e-4, (rel, mx)
+    assert rel <= 2 * pr["rel_l2"] and mx <= 2 * pr["max_abs"], (rel, mx)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -346,3 +346,28 @@ def test_synth_rounding_is_round_to_nearest_even():
     q, k, v = synth.attention_inputs(1, 2, 3, 4, 8, "bf16", seed=0)
     q2, _, _ = synth.attention_inputs(1, 2, 3, 4, 8, "bf16", seed=0)
     assert q.dtype == np.uint16 and np.array_equal(q, q2)
+
+
+# ------------------------------------------------------------- page-printed error magnitudes
+def test_fp16_error_magnitude_matches_the_printed_table():
+    """The fp16 forward's error figures printed by the flash-attention README (section
+    "Accuracy", tests/golden/fp16_forward_error_magnitudes.json) against the oracle: rounding the
+    oracle's output to fp16 (the dominant error of any correct fp16 kernel at this shape) must give
+    errors of the same order. A wrong normalisation or scale in the oracle moves |O|, and with it the
+    max-abs figure, by orders of magnitude."""
+    import json
+    import os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "fp16_forward_error_magnitudes.json")))
+    sh, pr = g["shape"], g["printed"]
+    q, k, v = synth.attention_inputs(1, 2, sh["M"], sh["N"], sh["D"], "f16", seed=0)
+    errs, refs = [], []
+    for h in range(2):
+        o, _ = oracle.forward(synth.to_f64(q[0, h], "f16"), synth.to_f64(k[0, h], "f16"),
+                              synth.to_f64(v[0, h], "f16"), 0.125, False)
+        errs.append(o.astype(np.float16).astype(np.float64) - o)
+        refs.append(o)
+    e, r = np.concatenate(errs), np.concatenate(refs)
+    max_abs = float(np.max(np.abs(e)))
+    rel_l2 = float(np.linalg.norm(e) / np.linalg.norm(r))
+    assert pr["max_abs"] / 5 <= max_abs <= pr["max_abs"] * 5, max_abs
+    assert pr["rel_l2"] / 3 <= rel_l2 <= pr["rel_l2"] * 3, rel_l2
