@@ -23,6 +23,8 @@ from ._binding import (  # noqa: F401
     fa_decode_static,
     fa_decode_ex,
     fa_fwd_host,
+    fa_bwd_ws,
+    fa_bwd_ws_workspace_bytes,
     fa_fwd_host_workspace_bytes,
     fa_decode_ex_workspace_bytes,
     fa_debug_inject,

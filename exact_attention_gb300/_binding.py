@@ -30,6 +30,8 @@ EXPORTS = (
     "fa_fwd_host_workspace_bytes",
     "fa_bwd",
     "fa_bwd_workspace_bytes",
+    "fa_bwd_ws",
+    "fa_bwd_ws_workspace_bytes",
     "fa_decode",
     "fa_decode_workspace_bytes",
     "fa_decode_static",
@@ -77,6 +79,10 @@ def lib() -> ctypes.CDLL:
     L.fa_decode_static.restype = st
     L.fa_decode_workspace_bytes.argtypes = [i, i, i, i]
     L.fa_decode_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_bwd_ws.argtypes = [vp] * 10 + [ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
+    L.fa_bwd_ws.restype = st
+    L.fa_bwd_ws_workspace_bytes.argtypes = [i, i, i, i]
+    L.fa_bwd_ws_workspace_bytes.restype = ctypes.c_size_t
     L.fa_fwd_host.argtypes = [vp] * 6 + [ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
     L.fa_fwd_host.restype = st
     L.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
@@ -130,6 +136,17 @@ def fa_fwd_ws(Q, K, V, O, LSE, workspace, workspace_bytes, B, H, M, N, D, scale,
 
 def fa_fwd_workspace_bytes(B, H, M, N, D, causal, dtype) -> int:
     return lib().fa_fwd_workspace_bytes(B, H, M, N, D, int(causal), int(dtype))
+
+
+def fa_bwd_ws(Q, K, V, O, dO, LSE, dQ, dK, dV, workspace, workspace_bytes, B, H, M, N, D, scale, causal, dtype,
+              stream=None) -> int:
+    return lib().fa_bwd_ws(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+                           _ptr(workspace), workspace_bytes, B, H, M, N, D, float(scale), int(causal), int(dtype),
+                           _stream(stream))
+
+
+def fa_bwd_ws_workspace_bytes(B, H, M, D) -> int:
+    return lib().fa_bwd_ws_workspace_bytes(B, H, M, D)
 
 
 def fa_fwd_host(hQ, hK, hV, hO, hLSE, dev_ws, dev_ws_bytes, B, H, M, N, D, scale, causal, dtype, stream=None) -> int:
@@ -255,12 +272,21 @@ def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, str
     return out, lse
 
 
-def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=None):
-    """dQ, dK, dV of sum(do * o); also returns the delta workspace (rowsum(dO o O))."""
+def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=None, fused: bool = False):
+    """dQ, dK, dV of sum(do * o); also returns the delta workspace (rowsum(dO o O)).
+
+    fused=True goes through fa_bwd_ws (one dK/dV/dQ pass for D = 64, with an f32 dQ accumulator
+    in the same workspace after delta)."""
     import torch
     B, H, M, D = _dims4(q, "q")
     N = _dims4(k, "k")[2]
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if fused:
+        nbytes = fa_bwd_ws_workspace_bytes(B, H, M, D)
+        ws = torch.empty((max(nbytes, 4) // 4,), dtype=torch.float32, device=q.device)
+        _check(fa_bwd_ws(q, k, v, o, do, lse, dq, dk, dv, ws, nbytes, B, H, M, N, D, scale, causal, fa_dtype(q),
+                         stream), "fa_bwd_ws")
+        return dq, dk, dv, ws[: B * H * M].view(B, H, M)
     ws = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
     _check(fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, B, H, M, N, D, scale, causal, fa_dtype(q), stream),
            "fa_bwd")

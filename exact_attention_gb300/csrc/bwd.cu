@@ -395,6 +395,8 @@ struct OvHdr {
   unsigned long long sig1, sig2;           // compute -> MMA (8 warps each)
   unsigned long long free1, free2;         // MMA -> compute: packed operand regions read
   unsigned long long acc_full, mma_done[2];
+  // fused dK/dV/dQ only: dQ_i computed, dQ_i read from TMEM, dQ_i staged, staging read by the reduce
+  unsigned long long dq_full, dq_free, dq_staged, stg_free;
   uint32_t tmem_base;
   int abort_flag;
   float nlse2[kStagesMax][kT];  // per streamed block: -LSE * log2(e) (dK/dV only)
@@ -410,6 +412,17 @@ struct OvCfg {
   static constexpr int kData = 2 * kTileBytes + kStages * 2 * kTileBytes;
   static constexpr int kSmem = 1024 + static_cast<int>(kOvHdrBytes) + kData;
   static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+// The fused dK/dV/dQ kernel (D = 64): K and V, three Q/dO stages, dS^T (32 KB) and the two dQ
+// staging boxes (32 KB).
+struct FusedCfg {
+  static constexpr int kTileBytes = kChunkB;
+  static constexpr int kStages = 3;
+  static constexpr int kData = 2 * kTileBytes + kStages * 2 * kTileBytes + 2 * kChunkB + 2 * kT * 128;
+  static constexpr int kSmem = 1024 + static_cast<int>(kOvHdrBytes) + kData;
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kStages <= kStagesMax, "LSE/delta staging");
 };
 
 __device__ __forceinline__ void ov_init(OvHdr* hdr, int stages, uint32_t full_count) {
@@ -769,6 +782,437 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   }
 }
 
+// dK, dV and dQ in one pass over (key tile, query block) with D = 64: the dK/dV kernel above
+// with dS^T in shared memory instead of tensor memory. There one buffer serves as the K-major A
+// operand of dK += dS^T Q and, read MN-major, as the A operand of dQ_i = dS K (the tutorial's
+// dQ kernel recomputes S and dP for that product; here it reuses them). dQ_i lands in the tensor
+// memory dS^T had, the compute warps stage it in shared memory as f32 and one thread adds it into
+// an f32 dQ accumulator in global memory with a bulk reduce (cp.reduce.async.bulk .add.f32; a
+// query block's 128 rows of 64 floats are contiguous there). A later kernel scales and converts
+// the accumulator. TMEM: S^T [0,128), dP^T [128,256), P^T packed [256,320), dQ_i [320,384),
+// dV [384,448), dK [448,512).
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kThreadsO, 1)
+    bwd_fused64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
+                       const float* __restrict__ LSE, const float* __restrict__ delta, uint16_t* __restrict__ dK,
+                       uint16_t* __restrict__ dV, const __grid_constant__ CUtensorMap tmQacc, int BH, int M, int N,
+                       float scale,
+                       DevStatus* status, unsigned long long budget_ns) {
+  constexpr int D = 64;
+  using C = FusedCfg;
+  constexpr uint32_t cS = 0, cdP = 128, cP = 256, cdQ = 320, cdV = 384, cdK = 448;
+  extern __shared__ uint8_t smem_raw[];
+  OvHdr* hdr = reinterpret_cast<OvHdr*>(smem_raw);
+  const uint32_t raw = ptx::smem_u32(smem_raw);
+  const uint32_t data = (raw + kOvHdrBytes + 1023u) & ~1023u;
+  const uint32_t sK = data, sV = data + C::kTileBytes;
+  auto sQ = [&](int st) { return data + 2 * C::kTileBytes + st * 2 * C::kTileBytes; };
+  auto sdO = [&](int st) { return sQ(st) + C::kTileBytes; };
+  // dS^T of the current block: [q chunk 0..1][key 0..127][64 q], 128-byte swizzled rows
+  const uint32_t sdS = data + 2 * C::kTileBytes + C::kStages * 2 * C::kTileBytes;
+  // dQ_i staged for the reduce: two boxes [32 d][128 queries] f32 in the tensor map's 128-byte
+  // swizzled layout (box b holds columns [32 b, 32 b + 32))
+  const uint32_t sStg = sdS + 2 * kChunkB;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
+  const int items = BH * nkb;
+  const float sl2 = scale * kLog2eB;
+  auto item = [&](int w) {
+    BwdItem it;
+    // causal: key tiles with the most query blocks (the first ones) go first, all heads of a
+    // key tile together; non-causal: the key tiles of a head are adjacent (shared Q/dO in L2)
+    int kb;
+    if (CAUSAL) {
+      kb = w / BH;
+      it.bh = w - kb * BH;
+    } else {
+      it.bh = w / nkb;
+      kb = w - it.bh * nkb;
+    }
+    it.r0 = kb * kT;
+    it.lo = CAUSAL ? min(it.r0 / kT, nqb) : 0;  // query blocks before the diagonal see no key here
+    it.hi = nqb;
+    return it;
+  };
+
+  if (threadIdx.x == 0) {
+    ov_init(hdr, C::kStages, 2);  // full: TMA bytes + LSE/delta staging
+    ptx::mbar_init(ptx::smem_u32(&hdr->fixed_empty), 2);  // K is read by both issuers here
+    ptx::mbar_init(ptx::smem_u32(&hdr->dq_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->dq_free), 8);
+    ptx::mbar_init(ptx::smem_u32(&hdr->dq_staged), 8);
+    ptx::mbar_init(ptx::smem_u32(&hdr->stg_free), 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == kWarpMmaO) {
+    ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = hdr->tmem_base;
+  ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDkDv};
+
+  if (warp == kWarpProdO) {
+    // ------------------------------------------------------------ producer (whole warp)
+    // Walks (item, query block) in order. -LSE (base 2) and -delta of a block's queries
+    // are read from global memory one block ahead into registers (lane l holds queries
+    // l, l+32, l+64, l+96), so their latency overlaps the wait for the next free stage.
+    constexpr int kQL = kT / 32;
+    float nl_v[kQL], nd_v[kQL];
+    auto fetch = [&](const BwdItem& it, int i) {
+#pragma unroll
+      for (int k = 0; k < kQL; ++k) {
+        const int row = i * kT + lane + 32 * k;
+        const bool in = row < M;  // past M: P = 0 (exp of -inf), delta = 0
+        const size_t g = static_cast<size_t>(it.bh) * M + (in ? row : 0);
+        nl_v[k] = in ? -LSE[g] * kLog2eB : -INFINITY;
+        nd_v[k] = in ? -delta[g] : 0.f;
+      }
+    };
+    uint32_t it_s = 0;
+    int n_item = 0;
+    bool ok = true;
+    int r = 0;
+    int w = item_of_round<CAUSAL>(0, items);
+    BwdItem itm{};
+    // first item that has a query block (items without one need only their fixed tiles)
+    if (w < items) {
+      itm = item(w);
+      if (itm.lo < itm.hi) fetch(itm, itm.lo);
+    }
+    for (; w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
+      itm = item(w);
+      if (lane == 0) {
+        ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10);
+        if (ok) {
+          const uint32_t ff = ptx::smem_u32(&hdr->fixed_full);
+          ptx::mbar_arrive_expect_tx(ff, 2 * C::kTileBytes);
+          ptx::tma_load_3d(sK, &tmK, ff, 0, itm.r0, itm.bh);
+          ptx::tma_load_3d(sV, &tmV, ff, 0, itm.r0, itm.bh);
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      for (int i = itm.lo; i < itm.hi && ok; ++i, ++it_s) {
+        const int st = it_s % C::kStages;
+        if (lane == 0)
+          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / C::kStages) & 1u) ^ 1u, wc, 11);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        const uint32_t fb = ptx::smem_u32(&hdr->full[st]);
+        if (lane == 0) {
+          ptx::mbar_arrive_expect_tx(fb, 2 * C::kTileBytes);
+          ptx::tma_load_3d(sQ(st), &tmQ, fb, 0, i * kT, itm.bh);
+          ptx::tma_load_3d(sdO(st), &tmdO, fb, 0, i * kT, itm.bh);
+        }
+#pragma unroll
+        for (int k = 0; k < kQL; ++k) {
+          hdr->nlse2[st][lane + 32 * k] = nl_v[k];
+          hdr->ndlt[st][lane + 32 * k] = nd_v[k];
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(fb);
+        // next block's values: this item's next block, else the first block of the next
+        // item that has one
+        if (i + 1 < itm.hi) {
+          fetch(itm, i + 1);
+        } else {
+          for (int r2 = r + 1, w2 = item_of_round<CAUSAL>(r2, items); w2 < items; w2 = item_of_round<CAUSAL>(++r2, items)) {
+            const BwdItem nx = item(w2);
+            if (nx.lo < nx.hi) {
+              fetch(nx, nx.lo);
+              break;
+            }
+          }
+        }
+      }
+    }
+    if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
+      for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
+        ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
+    }
+  } else if (warp == kWarpMmaO || warp == kWarpGradO) {
+    // ------------------------------------------------------------ MMA issuers (lane 0)
+    if (lane == 0) {
+      const bool scores = warp == kWarpMmaO;
+      constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
+      constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
+      constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
+      constexpr uint32_t id_q = ptx::idesc_f32acc(kT, D, fmt, fmt, true, true);  // A = dS read MN-major
+      uint32_t it_s = 0, n1 = 0, n2 = 0, nq = 0;
+      int n_item = 0;
+      bool ok = true;
+      auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+        return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
+      };
+      auto commit = [&](unsigned long long* bar) { ptx::tc_commit(ptx::smem_u32(bar)); };
+      auto stage_ready = [&](uint32_t k) { return wait(&hdr->full[k % C::kStages], (k / C::kStages) & 1u, 21); };
+      auto qk = [&](uint32_t k) {  // S^T = K Q^T
+        const int st = k % C::kStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss(tmem + cS, kmajor_desc(sK, ks), kmajor_desc(sQ(st), ks), id_s, ks > 0);
+        commit(&hdr->s_full);
+      };
+      auto vdo = [&](uint32_t k) {  // dP^T = V dO^T
+        const int st = k % C::kStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
+        commit(&hdr->dp_full);
+      };
+      for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
+        const BwdItem itm = item(w);
+        if (scores) {
+          if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
+          if (itm.lo < itm.hi) {
+            ok = stage_ready(it_s);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            qk(it_s);
+            vdo(it_s);
+            // the next block's stage has normally landed long ago: check it while the
+            // compute warps work, not between their signal and the next scores
+            if (itm.lo + 1 < itm.hi && !stage_ready(it_s + 1)) break;
+          }
+        }
+        for (int i = itm.lo; i < itm.hi; ++i, ++it_s) {
+          const int st = it_s % C::kStages;
+          const bool more = i + 1 < itm.hi;
+          const bool acc = i > itm.lo;
+          // S^T(i) read and P^T(i) stored
+          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (scores) {
+            if (more) qk(it_s + 1);
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < kT / 16; ++ks)  // dV += P^T dO
+              ptx::mma_f16_ts(tmem + cdV, tmem + cP + ks * 8, mnmajor_desc(sdO(st), ks), id_g, (acc || ks > 0));
+            commit(&hdr->free1);
+          }
+          // dP^T(i) read and dS^T(i) stored
+          ok = wait(&hdr->sig2, (n2++) & 1u, 23);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (scores) {
+            if (more) vdo(it_s + 1);
+            if (i + 2 < itm.hi && !stage_ready(it_s + 2)) {
+              ok = false;
+              break;
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < kT / 16; ++ks)  // dK += dS^T Q (dS^T K-major in shared memory)
+              ptx::mma_f16_ss(tmem + cdK, kmajor_desc(sdS, ks), mnmajor_desc(sQ(st), ks), id_g, (acc || ks > 0));
+            // dQ_i = dS K (the same buffer read MN-major: M = queries, K = keys), once the compute
+            // warps hold dQ of the previous block
+            if (nq > 0 && !wait(&hdr->dq_free, (nq - 1u) & 1u, 26)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < kT / 16; ++ks)
+              ptx::mma_f16_ss(tmem + cdQ, mnmajor_desc(sdS, ks), mnmajor_desc(sK, ks), id_q, ks > 0);
+            ++nq;
+            commit(&hdr->dq_full);
+            commit(&hdr->free2);  // dS^T has been read by both products
+            commit(&hdr->empty[st]);
+          }
+        }
+        if (!ok) break;
+        if (!scores) commit(&hdr->acc_full);
+        commit(&hdr->fixed_empty);  // K and V read by this thread's products of the item
+      }
+      const int me = scores ? 0 : 1;
+      commit(&hdr->mma_done[me]);
+      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[me]), 0u, 1000000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ compute warps: one key row per thread
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's query columns [c0, c0 + 64)
+    uint32_t it_s = 0, nb = 0;  // blocks processed (all items): s_full/dp_full/free phases
+    int n_item = 0;
+    bool ok = true;
+    auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+      const bool r = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site));
+      ptx::tc_fence_after();
+      return r;
+    };
+    auto signal = [&](unsigned long long* bar) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
+    };
+    // dQ_i of query block `qb`: TMEM -> the staging boxes (then the TMEM columns are free for the
+    // next product) -> warp 0's lane 0 adds both boxes into the accumulator. Warp-uniform result.
+    uint32_t nq = 0;  // dQ blocks read back (all items)
+    const bool reducer = warp == 0 && lane == 0;
+    auto dq_readout = [&](int bh, int qb) {
+      if (!wait_all(&hdr->dq_full, nq & 1u, 36)) return false;
+      uint32_t a[32];
+      ptx::tmem_ld32(tmem + lane_sel + cdQ + 32 * half, a);
+      ptx::tmem_wait_ld32(a);
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_free));
+      // the previous reduce has read the staging boxes
+      if (reducer && nq > 0) {
+        ptx::bulk_wait_read();
+        ptx::mbar_arrive(ptx::smem_u32(&hdr->stg_free));
+      }
+      if (nq > 0 && !wait_all(&hdr->stg_free, (nq - 1u) & 1u, 37)) return false;
+      {
+        const int rr = quarter * 32 + lane;  // query row within the block
+        uint8_t* srow = smem_raw + (sStg - raw) + half * (kT * 128) + rr * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(srow + ((u ^ (rr & 7)) << 4)) =
+              make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+      }
+      ptx::fence_proxy_async_smem();  // staging writes -> the TMA engine
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_staged));
+      bool good = true;
+      if (reducer) {
+        good = ptx::mbar_wait(ptx::smem_u32(&hdr->dq_staged), nq & 1u, wc, 38);
+        if (good) {
+          ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, qb * kT, bh);
+          ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, qb * kT, bh);
+          ptx::bulk_commit();
+        }
+      }
+      ++nq;
+      return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+    };
+    for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
+      const BwdItem itm = item(w);
+      const int key = itm.r0 + quarter * 32 + lane;
+      for (int i = itm.lo; i < itm.hi; ++i, ++it_s, ++nb) {
+        const int st = it_s % C::kStages;
+        // S^T(i) computed; the stage's -LSE/-delta were staged before its full barrier
+        ok = wait_all(&hdr->s_full, nb & 1u, 30) &&
+             wait_all(&hdr->full[st], (it_s / C::kStages) & 1u, 31);
+        if (!ok) break;
+        const float* nl = hdr->nlse2[st] + c0;
+        const float* nd = hdr->ndlt[st] + c0;
+        const int qb = i * kT + static_cast<int>(c0);  // first query of this warp's columns
+        const bool diag = CAUSAL && qb < key;          // some of these queries precede the key
+        float p[64];
+        {
+          uint32_t s[64];
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0, s);
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
+          ptx::tmem_wait_ld32(s);
+          ptx::tmem_wait_ld32(s + 32);
+          const float2 c2 = make_float2(sl2, sl2);
+#pragma unroll
+          for (int q = 0; q < 64; q += 2) {
+            const float2 nlq = *reinterpret_cast<const float2*>(nl + q);
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(s[q]), __uint_as_float(s[q + 1])), c2, nlq);
+            p[q] = ptx::ex2(x.x);
+            p[q + 1] = ptx::ex2(x.y);
+            if (diag) {  // key j is visible to query i iff j <= i
+              if (qb + q < key) p[q] = 0.f;
+              if (qb + q + 1 < key) p[q + 1] = 0.f;
+            }
+          }
+        }
+        // P^T(i-1) has been read by dV's MMA before P^T(i) overwrites it
+        if (nb > 0) {
+          ok = wait_all(&hdr->free1, (nb - 1u) & 1u, 32);
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) pk[k] = pack2<BF16>(p[c + 2 * k], p[c + 2 * k + 1]);
+          ptx::tmem_st16(tmem + lane_sel + cP + (c0 + c) / 2, pk);
+        }
+        ptx::tmem_wait_st();
+        signal(&hdr->sig1);
+        // dP^T(i) computed; dS^T = P^T o (dP^T - delta)
+        ok = wait_all(&hdr->dp_full, nb & 1u, 33);
+        if (ok && nb > 0) ok = wait_all(&hdr->free2, (nb - 1u) & 1u, 34);
+        if (!ok) break;
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t dp[32];
+          ptx::tmem_ld32(tmem + lane_sel + cdP + c0 + c, dp);
+          ptx::tmem_wait_ld32(dp);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 ndq = *reinterpret_cast<const float2*>(nd + c + 2 * k);
+            const float2 t = ptx::fadd2(make_float2(__uint_as_float(dp[2 * k]), __uint_as_float(dp[2 * k + 1])), ndq);
+            const float2 ds = ptx::fmul2(make_float2(p[c + 2 * k], p[c + 2 * k + 1]), t);
+            pk[k] = pack2<BF16>(ds.x, ds.y);
+          }
+          // row `key` of dS^T, queries [c0 + c, c0 + c + 32): four 16-byte chunks of chunk `half`
+          {
+            const int rr = quarter * 32 + lane;
+            uint8_t* drow = smem_raw + (sdS - raw) + half * kChunkB + rr * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int v = c / 8 + u;
+              *reinterpret_cast<uint4*>(drow + ((v ^ (rr & 7)) << 4)) =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            }
+          }
+        }
+        ptx::fence_proxy_async_smem();  // the generic-proxy writes of dS^T -> the tensor core
+        signal(&hdr->sig2);
+        // dQ of the previous block (its product was issued after the previous sig2)
+        if (i > itm.lo) {
+          ok = dq_readout(itm.bh, i - 1);
+          if (!ok) break;
+        }
+      }
+      if (ok && itm.lo < itm.hi) ok = dq_readout(itm.bh, itm.hi - 1);  // the item's last block
+      if (!ok) break;
+      // epilogue: this warp writes columns [32 * half, 32 * half + 32) of dV and scale * dK
+      ok = wait_all(&hdr->acc_full, n_item & 1, 35);
+      if (!ok) break;
+      const bool valid = key < N;
+      const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t a[32];
+        ptx::tmem_ld32(tmem + lane_sel + (part == 0 ? cdV : cdK) + 32 * half, a);
+        ptx::tmem_wait_ld32(a);
+        const float f = part == 0 ? 1.f : scale;
+        uint32_t h[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          h[k] = none ? 0u : pack2<BF16>(__uint_as_float(a[2 * k]) * f, __uint_as_float(a[2 * k + 1]) * f);
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>((part == 0 ? dV : dK) + g);
+#pragma unroll
+          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+    }
+  }
+
+  if (warp == 0 && lane == 0) ptx::bulk_wait_all();  // the reduces have completed
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMmaO) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
 // dQ. TMEM: S [0,128), dP [128,256), dS packed [256,320), dQ [320, 320+D).
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsO, 1)
@@ -1024,10 +1468,21 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   }
 }
 
+// dQ = scale * the f32 accumulator of the fused kernel, rounded to the I/O type.
+template <bool BF16>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dQ,
+                                                             long long n4, float scale) {
+  for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n4;
+       i += static_cast<long long>(gridDim.x) * 256) {
+    const float4 a = acc[i];
+    dQ[i] = make_uint2(pack2<BF16>(a.x * scale, a.y * scale), pack2<BF16>(a.z * scale, a.w * scale));
+  }
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                         void* dQ, void* dK, void* dV, float* delta, int BH, int M, int N, float scale, int dtype,
-                         const LaunchCtx& ctx) {
+                         void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, float scale,
+                         int dtype, const LaunchCtx& ctx) {
   using C = BwdCfg<D>;
   // delta = rowsum(dO o O)
   {
@@ -1047,6 +1502,32 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       !make_tmap_3d(&mv, V, dtype, D, N, BH, 64, kT) || !make_tmap_3d(&mdo, dO, dtype, D, M, BH, 64, kT))
     return cudaErrorInvalidValue;
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
+  if constexpr (D == 64) {
+    if (dQacc != nullptr) {  // one pass for dK, dV and dQ (dQ accumulated in f32, then converted)
+      const size_t n = static_cast<size_t>(BH) * M * D;
+      cudaError_t e = cudaMemsetAsync(dQacc, 0, n * sizeof(float), ctx.stream);
+      if (e != cudaSuccess) return e;
+      CUtensorMap macc;
+      if (!make_tmap_3d(&macc, dQacc, kF32, D, M, BH, 32, kT)) return cudaErrorInvalidValue;
+      const long long items = static_cast<long long>(BH) * nkb;
+      const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
+      auto kern = bwd_fused64_kernel<BF16, CAUSAL>;
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedCfg::kSmem);
+      if (e != cudaSuccess) return e;
+      kern<<<grid, kThreadsO, FusedCfg::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dK),
+                                                              static_cast<uint16_t*>(dV), macc, BH, M, N, scale,
+                                                              ctx.status, ctx.wait_budget_ns);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      const long long n4 = static_cast<long long>(n / 4);
+      long long blocks = (n4 + 255) / 256;
+      const long long cap = static_cast<long long>(ctx.num_sms) * 8;
+      if (blocks > cap) blocks = cap;
+      bwd_dq_convert_kernel<BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
+          reinterpret_cast<const float4*>(dQacc), static_cast<uint2*>(dQ), n4, scale);
+      return cudaGetLastError();
+    }
+  }
   {
     const long long items = static_cast<long long>(BH) * nkb;
     const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
@@ -1084,12 +1565,12 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
 }  // namespace
 
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                       void* dQ, void* dK, void* dV, float* delta, int BH, int M, int N, int D, float scale,
-                       bool causal, int dtype, const LaunchCtx& ctx) {
+                       void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, int D,
+                       float scale, bool causal, int dtype, const LaunchCtx& ctx) {
   const bool bf = dtype == kBF16;
 #define FA_B(DD, BB, CC)                                                                                       \
   if (D == DD && bf == BB && causal == CC)                                                                     \
-    return launch_bwd_t<DD, BB, CC>(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, BH, M, N, scale, dtype, ctx);
+    return launch_bwd_t<DD, BB, CC>(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, dQacc, BH, M, N, scale, dtype, ctx);
   FA_B(64, false, false)
   FA_B(64, false, true)
   FA_B(64, true, false)

@@ -292,6 +292,37 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   return FA_OK;
 }
 
+// fa_bwd / fa_bwd_ws: delta_ws holds delta (B*H*M f32); dQacc, when not null, the fused path's f32
+// dQ accumulator (B*H*M*64).
+fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                   void* dQ, void* dK, void* dV, float* delta_ws, float* dQacc, int B, int H, int M, int N, int D,
+                   float scale, int causal, fa_dtype dtype, void* stream, const char* name) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, M, N, D));
+  if (dtype == FA_F32) return fail(FA_ERR_UNSUPPORTED, "%s supports FA_F16 and FA_BF16", name);
+  FA_TRY(check_scale(scale, true));
+  if (B * H == 0 || M == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  FA_TRY(check_ptr(Q, "Q"));
+  FA_TRY(check_ptr(K, "K"));
+  FA_TRY(check_ptr(V, "V"));
+  FA_TRY(check_ptr(O, "O"));
+  FA_TRY(check_ptr(dO, "dO"));
+  FA_TRY(check_ptr(LSE, "LSE"));
+  FA_TRY(check_ptr(dQ, "dQ"));
+  FA_TRY(check_ptr(dK, "dK"));
+  FA_TRY(check_ptr(dV, "dV"));
+  FA_TRY(check_ptr(delta_ws, "delta_ws"));
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  cudaError_t e =
+      launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, dQacc, B * H, M, N, D, scale, causal != 0, dtype, ctx);
+  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
+  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "%s: TMA descriptor rejected by the driver", name);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -358,32 +389,37 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
                   "fa_fwd_ws");
 }
 
+
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                  void* dQ, void* dK, void* dV, float* delta_ws, int B, int H, int M, int N, int D, float scale,
                  int causal, fa_dtype dtype, void* stream) {
-  FA_TRY(check_dtype(dtype));
-  FA_TRY(check_sizes(B, H, M, N, D));
-  if (dtype == FA_F32) return fail(FA_ERR_UNSUPPORTED, "fa_bwd supports FA_F16 and FA_BF16");
-  FA_TRY(check_scale(scale, true));
-  if (B * H == 0 || M == 0) return FA_OK;
-  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
-  FA_TRY(check_ptr(Q, "Q"));
-  FA_TRY(check_ptr(K, "K"));
-  FA_TRY(check_ptr(V, "V"));
-  FA_TRY(check_ptr(O, "O"));
-  FA_TRY(check_ptr(dO, "dO"));
-  FA_TRY(check_ptr(LSE, "LSE"));
-  FA_TRY(check_ptr(dQ, "dQ"));
-  FA_TRY(check_ptr(dK, "dK"));
-  FA_TRY(check_ptr(dV, "dV"));
-  FA_TRY(check_ptr(delta_ws, "delta_ws"));
-  LaunchCtx ctx{};
-  FA_TRY(make_ctx(&ctx, stream));
-  cudaError_t e = launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, B * H, M, N, D, scale, causal != 0, dtype, ctx);
-  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_bwd: configuration not supported");
-  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "fa_bwd: TMA descriptor rejected by the driver");
-  if (e != cudaSuccess) return cuda_fail(e, "fa_bwd launch");
-  return FA_OK;
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, nullptr, B, H, M, N, D, scale, causal, dtype, stream,
+                  "fa_bwd");
+}
+
+// workspace of fa_bwd_ws: delta, then (D = 64) the f32 dQ accumulator, 256-byte aligned
+size_t fa_bwd_ws_workspace_bytes(int B, int H, int M, int D) {
+  if (B <= 0 || H <= 0 || M <= 0 || D <= 0) return 0;
+  const size_t rows = static_cast<size_t>(B) * H * M;
+  const size_t delta = (rows * sizeof(float) + 255u) & ~static_cast<size_t>(255u);
+  return D == 64 ? delta + rows * 64 * sizeof(float) : delta;
+}
+
+fa_status fa_bwd_ws(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                    void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int M, int N,
+                    int D, float scale, int causal, fa_dtype dtype, void* stream) {
+  const size_t need = fa_bwd_ws_workspace_bytes(B, H, M, D);
+  if (B * H > 0 && M > 0 && (workspace == nullptr || workspace_bytes < need))
+    return fail(FA_ERR_INVALID, "fa_bwd_ws: workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  float* delta = static_cast<float*>(workspace);
+  float* acc = nullptr;
+  if (D == 64 && B * H > 0 && M > 0) {
+    const size_t rows = static_cast<size_t>(B) * H * M;
+    acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                   ((rows * sizeof(float) + 255u) & ~static_cast<size_t>(255u)));
+  }
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, acc, B, H, M, N, D, scale, causal, dtype, stream,
+                  "fa_bwd_ws");
 }
 
 fa_status fa_decode(const void* q, const void* Kcache, const void* Vcache, void* O, float* partial_ws, int B, int H,

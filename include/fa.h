@@ -165,6 +165,34 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 size_t fa_bwd_workspace_bytes(int B, int H, int M);
 
 /*
+ * fa_bwd with a caller-owned workspace that also holds an f32 dQ accumulator;
+ * same arguments as fa_bwd (delta_ws replaced by workspace), same results.
+ *
+ * The pages' backward recomputes S and dP in a separate dQ kernel. With D = 64
+ * this call instead forms dQ in the dK/dV pass: dS, already in shared memory
+ * for dK += dS^T Q, also gives dQ_i = dS K, whose 128x64 block is added into an
+ * f32 accumulator in global memory (a bulk reduce-add in L2); a last kernel
+ * writes dQ = scale * accumulator in the I/O dtype. Five matrix products per
+ * (query block, key block) instead of seven. For D = 128 it runs the three
+ * kernels of fa_bwd.
+ *
+ *   workspace        device pointer, 16-byte aligned, at least
+ *                    fa_bwd_ws_workspace_bytes(B,H,M,D) bytes: delta
+ *                    (B*H*M float32, rowsum(dO o O) on return), then for
+ *                    D = 64 the accumulator (B*H*M*64 float32, 256-byte
+ *                    aligned). Zeroed by the call itself; caller-owned.
+ *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
+ * The summation order of dQ's key blocks follows the SMs' timing, so dQ can
+ * differ between runs in the last bits of the f32 accumulator (dK, dV do not).
+ */
+fa_status fa_bwd_ws(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                    void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int M,
+                    int N, int D, float scale, int causal, fa_dtype dtype, void* stream);
+
+/* Bytes of workspace fa_bwd_ws needs (0 on bad sizes). */
+size_t fa_bwd_ws_workspace_bytes(int B, int H, int M, int D);
+
+/*
  * Decode (flash decoding): one query row per (batch, head) against a KV cache
  * (fa_decode_ex below takes up to four rows and returns the LSE too).
  *

@@ -15,11 +15,11 @@ from helpers import TOL_GRAD, assert_close, f64, to_device, to_f64
 pytestmark = pytest.mark.gpu
 
 
-def run_bwd(B, H, M, N, D, dtype, causal, scale, seed=0, std=1.0):
+def run_bwd(B, H, M, N, D, dtype, causal, scale, seed=0, std=1.0, fused=False):
     q, k, v, do = synth.attention_inputs(B, H, M, N, D, dtype, seed=seed, std=std, with_dout=True)
     qd, kd, vd, dod = (to_device(x, dtype) for x in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, scale, causal)
-    dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
+    dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal, fused=fused)
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
     return (q, k, v, do), to_f64(o), (to_f64(dq), to_f64(dk), to_f64(dv)), to_f64(delta)
 
@@ -42,11 +42,16 @@ def check(inputs, o_gpu, grads, delta, dtype, causal, scale, heads=None):
     return worst
 
 
+# fused: fa_bwd_ws (dQ formed in the dK/dV pass and accumulated in f32 for D = 64) instead of fa_bwd
+FUSED = pytest.mark.parametrize("fused", [False, True], ids=["3kernels", "fused"])
+
+
+@FUSED
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("std", [1.0, 0.5])
-def test_backward_tutorial_shape(causal, std):
+def test_backward_tutorial_shape(causal, std, fused):
     """Z=1, H=2, N_CTX=1024, D=64, sm_scale 0.5, fp16, N(0,1) and N(0, 0.5^2)."""
-    inputs, o, grads, delta = run_bwd(1, 2, 1024, 1024, 64, "f16", causal, 0.5, seed=20, std=std)
+    inputs, o, grads, delta = run_bwd(1, 2, 1024, 1024, 64, "f16", causal, 0.5, seed=20, std=std, fused=fused)
     check(inputs, o, grads, delta, "f16", causal, 0.5)
 
 
@@ -61,13 +66,14 @@ SHAPES = [
 ]
 
 
+@FUSED
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,M,N", SHAPES)
-def test_backward_matches_oracle(dtype, D, causal, B, H, M, N):
+def test_backward_matches_oracle(dtype, D, causal, B, H, M, N, fused):
     scale = 1.0 / math.sqrt(D)
-    inputs, o, grads, delta = run_bwd(B, H, M, N, D, dtype, causal, scale, seed=M * 7 + N)
+    inputs, o, grads, delta = run_bwd(B, H, M, N, D, dtype, causal, scale, seed=M * 7 + N, fused=fused)
     check(inputs, o, grads, delta, dtype, causal, scale)
 
 
@@ -79,9 +85,26 @@ def test_backward_gradient_identities():
     assert np.max(np.abs(dv.sum(axis=2) - do.sum(axis=2))) < 0.05
 
 
+@FUSED
 @pytest.mark.parametrize("causal", [False, True])
-def test_backward_full_workload_sampled_heads(causal):
+def test_backward_full_workload_sampled_heads(causal, fused):
     """B4 H12 M=N=2048 D64 fp16 (the measured workload): every gradient entry of three heads
     spread over the batch against the oracle."""
-    inputs, o, grads, delta = run_bwd(4, 12, 2048, 2048, 64, "f16", causal, 0.125, seed=5)
+    inputs, o, grads, delta = run_bwd(4, 12, 2048, 2048, 64, "f16", causal, 0.125, seed=5, fused=fused)
     check(inputs, o, grads, delta, "f16", causal, 0.125, heads=[(0, 0), (1, 7), (3, 11)])
+
+
+def test_backward_fused_matches_three_kernels():
+    """The fused pass gives dK and dV identical to the three kernels (same products, same order)
+    and dQ equal up to the f32 summation order of its key blocks."""
+    import torch
+    for causal in (False, True):
+        q, k, v, do = synth.attention_inputs(2, 3, 700, 900, 64, "f16", seed=11, with_dout=True)
+        qd, kd, vd, dod = (to_device(x, "f16") for x in (q, k, v, do))
+        o, lse = fa.forward(qd, kd, vd, 0.125, causal)
+        a = fa.backward(qd, kd, vd, o, dod, lse, 0.125, causal)
+        b = fa.backward(qd, kd, vd, o, dod, lse, 0.125, causal, fused=True)
+        assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+        assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]), causal
+        assert torch.equal(a[3], b[3])  # delta
+        assert float((a[0].float() - b[0].float()).abs().max()) <= 4e-3, causal
