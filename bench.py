@@ -236,7 +236,9 @@ def run_ours(args):
     od = torch.empty_like(qd)
     lse = torch.empty((c["B"], c["H"], c["M"]), dtype=torch.float32, device="cuda")
     dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-    delta = torch.empty((c["B"], c["H"], c["M"]), dtype=torch.float32, device="cuda")
+    # backward workspace: delta, then the f32 dQ accumulator of the fused dK/dV/dQ pass (fa_bwd_ws)
+    bws_bytes = fa.fa_bwd_ws_workspace_bytes(c["B"], c["H"], c["M"], c["D"])
+    bws = torch.empty(bws_bytes, dtype=torch.uint8, device="cuda")
     BHMND = (c["B"], c["H"], c["M"], c["N"], c["D"])
 
     d = DEC
@@ -268,12 +270,12 @@ def run_ours(args):
         nonlocal have_bwd
         if not have_bwd:
             return
-        s = fa.fa_bwd(qd, kd, vd, od, dod, lse, dq, dk, dv, delta, *BHMND, c["scale"], c["causal"], fa.FA_F16,
-                      stream)
+        s = fa.fa_bwd_ws(qd, kd, vd, od, dod, lse, dq, dk, dv, bws, bws_bytes, *BHMND, c["scale"], c["causal"],
+                         fa.FA_F16, stream)
         if s == fa.FA_ERR_UNSUPPORTED:
             have_bwd = False
             return
-        check(s, "fa_bwd")
+        check(s, "fa_bwd_ws")
 
     def run_dec():
         check(fa.fa_decode(qdec, kc, vc, odec, ws, d["B"], d["H"], d["N"], d["D"], 1 / math.sqrt(d["D"]),
@@ -511,13 +513,13 @@ def run_ours(args):
         "backward": None if bwd_tflops is None else {
             "value": round(bwd_tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(t_bwd / K * 1e3, 4),
             "flops": "2.5 x forward",
-            # the whole call (delta, dK/dV, dQ) against the tensor peak; traffic is the dK/dV
-            # kernel's (the larger share of the call) from one ncu capture of this workload
-            "roofline": {"kernel": "bwd_dkdv64_kernel<f16,non-causal> + bwd_dq_kernel<64,f16,non-causal>",
+            # the whole call (delta, the fused dK/dV/dQ pass, dQ's conversion) against the tensor
+            # peak; traffic is the fused kernel's from one ncu capture of this workload
+            "roofline": {"kernel": "bwd_fused64_kernel<f16,non-causal> (+ delta, dQ conversion)",
                          "bound": "tensor", "achieved": round(bwd_tflops / world, 2), "peak": peak_tf,
                          "unit": "TFLOP/s", "frac": round(bwd_tflops / world / peak_tf, 4),
                          "peak_source": f"{peaks_src} bf16 burst (fp16 dense rate equals bf16)",
-                         "traffic": traffic.get("bwd_dkdv")}},
+                         "traffic": traffic.get("bwd_fused")}},
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,

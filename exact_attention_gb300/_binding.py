@@ -272,11 +272,12 @@ def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, str
     return out, lse
 
 
-def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=None, fused: bool = False):
-    """dQ, dK, dV of sum(do * o); also returns the delta workspace (rowsum(dO o O)).
+def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=None, fused: bool = True):
+    """dQ, dK, dV of sum(do * o); also returns delta (rowsum(dO o O)).
 
-    fused=True goes through fa_bwd_ws (one dK/dV/dQ pass for D = 64, with an f32 dQ accumulator
-    in the same workspace after delta)."""
+    fused=True (default) goes through fa_bwd_ws (one dK/dV/dQ pass for D = 64, with an f32 dQ
+    accumulator in the same workspace after delta); fused=False through fa_bwd (the three kernels:
+    delta, dK/dV, dQ)."""
     import torch
     B, H, M, D = _dims4(q, "q")
     N = _dims4(k, "k")[2]
