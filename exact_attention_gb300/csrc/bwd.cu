@@ -46,7 +46,8 @@ constexpr int kMinSmem = 120 * 1024;  // keeps one CTA per SM (each allocates al
 // ------------------------------------------------------------------------- delta
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
-                                                        float* __restrict__ delta, long long rows) {
+                                                        float* __restrict__ delta, float* __restrict__ acc_zero,
+                                                        long long rows) {
   constexpr int kLPR = D * 2 / 16;          // lanes per row (16-byte vectors)
   constexpr int kRPW = 32 / kLPR;           // rows per warp pass
   const int lane = threadIdx.x & 31;
@@ -71,6 +72,11 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
 #pragma unroll
     for (int o = kLPR / 2; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
     if (sl == 0 && r < rows) delta[r] = acc;
+    if (acc_zero != nullptr && r < rows) {  // the row's D f32 of the dQ accumulator start at zero
+      float4* z = reinterpret_cast<float4*>(acc_zero + r * D);
+#pragma unroll
+      for (int k = 0; k < D / 4 / kLPR; ++k) z[sl + k * kLPR] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
   }
 }
 
@@ -852,6 +858,9 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // launched behind the delta kernel, which also zeroes the dQ accumulator: the set-up above
+  // overlaps its tail
+  ptx::grid_dep_wait();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDkDv};
 
@@ -1472,6 +1481,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
 template <bool BF16>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __restrict__ acc, uint2* __restrict__ dQ,
                                                              long long n4, float scale) {
+  ptx::grid_dep_wait();  // launched behind the fused kernel
   for (long long i = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x; i < n4;
        i += static_cast<long long>(gridDim.x) * 256) {
     const float4 a = acc[i];
@@ -1492,8 +1502,10 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     const long long cap = static_cast<long long>(ctx.num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
+    // the fused D = 64 pass accumulates dQ into dQacc, which this kernel zeroes on the way
+    float* zero = D == 64 ? dQacc : nullptr;
     bwd_delta_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
-        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, rows);
+        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1505,27 +1517,39 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
   if constexpr (D == 64) {
     if (dQacc != nullptr) {  // one pass for dK, dV and dQ (dQ accumulated in f32, then converted)
       const size_t n = static_cast<size_t>(BH) * M * D;
-      cudaError_t e = cudaMemsetAsync(dQacc, 0, n * sizeof(float), ctx.stream);
-      if (e != cudaSuccess) return e;
       CUtensorMap macc;
       if (!make_tmap_3d(&macc, dQacc, kF32, D, M, BH, 32, kT)) return cudaErrorInvalidValue;
       const long long items = static_cast<long long>(BH) * nkb;
       const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
       auto kern = bwd_fused64_kernel<BF16, CAUSAL>;
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedCfg::kSmem);
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedCfg::kSmem);
       if (e != cudaSuccess) return e;
-      kern<<<grid, kThreadsO, FusedCfg::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dK),
-                                                              static_cast<uint16_t*>(dV), macc, BH, M, N, scale,
-                                                              ctx.status, ctx.wait_budget_ns);
-      e = cudaGetLastError();
+      // Both later kernels are launched as programmatic dependents: each starts its set-up
+      // while the kernel before it drains and waits (griddepcontrol.wait) before touching
+      // that kernel's results.
+      cudaLaunchAttribute pdl[1];
+      pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      pdl[0].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(grid));
+      cfg.blockDim = dim3(kThreadsO);
+      cfg.dynamicSmemBytes = FusedCfg::kSmem;
+      cfg.stream = ctx.stream;
+      cfg.attrs = pdl;
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, LSE, static_cast<const float*>(delta),
+                             static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), macc, BH, M, N, scale,
+                             ctx.status, ctx.wait_budget_ns);
       if (e != cudaSuccess) return e;
       const long long n4 = static_cast<long long>(n / 4);
       long long blocks = (n4 + 255) / 256;
       const long long cap = static_cast<long long>(ctx.num_sms) * 8;
       if (blocks > cap) blocks = cap;
-      bwd_dq_convert_kernel<BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
-          reinterpret_cast<const float4*>(dQacc), static_cast<uint2*>(dQ), n4, scale);
-      return cudaGetLastError();
+      cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+      cfg.blockDim = dim3(256);
+      cfg.dynamicSmemBytes = 0;
+      return cudaLaunchKernelEx(&cfg, bwd_dq_convert_kernel<BF16>, reinterpret_cast<const float4*>(dQacc),
+                                static_cast<uint2*>(dQ), n4, scale);
     }
   }
   {
