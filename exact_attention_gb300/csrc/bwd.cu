@@ -47,7 +47,10 @@ constexpr int kMinSmem = 120 * 1024;  // keeps one CTA per SM (each allocates al
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
                                                         float* __restrict__ delta, float* __restrict__ acc_zero,
-                                                        long long rows) {
+                                                        uint32_t* __restrict__ flags_zero, int n_flags, long long rows) {
+  // the fused pass's ready flags (split schedule) start at zero
+  if (blockIdx.x == 0)
+    for (int k = threadIdx.x; k < n_flags; k += blockDim.x) flags_zero[k] = 0u;
   constexpr int kLPR = D * 2 / 16;          // lanes per row (16-byte vectors)
   constexpr int kRPW = 32 / kLPR;           // rows per warp pass
   const int lane = threadIdx.x & 31;
@@ -788,6 +791,64 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   }
 }
 
+// Which pieces of work a CTA of the fused pass takes. A piece is an item (key tile of a head)
+// with a range of its query blocks.
+//  * Classic: whole items, one per round (item_of_round).
+//  * Split (non-causal): the contiguous range [c U / G, (c+1) U / G) of the U = items x nqb
+//    (item, query block) units, so every CTA streams the same number of blocks and no part-full
+//    last round is left. An item cut by a range boundary is finished by the CTA holding its
+//    first block, which reaches that piece last (a range ends with it) and adds in the partial
+//    dK / dV of the CTAs holding the rest; those reach theirs first (a range starts with it) and
+//    publish it in the workspace.
+struct FusedPiece {
+  BwdItem it;
+  int w;     // item index
+  int kind;  // 0: the whole item; 1: its first blocks, finished here; 2: later blocks, a partial
+};
+template <bool CAUSAL>
+struct FusedSched {
+  bool split;
+  int r;          // classic: next round
+  uint32_t u, e;  // split: the remaining unit range
+  __device__ static uint32_t start(uint32_t c, uint32_t units) {
+    return static_cast<uint32_t>(static_cast<uint64_t>(c) * units / gridDim.x);
+  }
+  __device__ FusedSched(bool sp, uint32_t units) : split(sp), r(0), u(0), e(0) {
+    if (split) {
+      u = start(blockIdx.x, units);
+      e = start(blockIdx.x + 1, units);
+    }
+  }
+  template <class ItemFn>
+  __device__ bool next(FusedPiece& pc, int items, int nqb, const ItemFn& item) {
+    if (!split) {
+      const int w = item_of_round<CAUSAL>(r, items);
+      if (w >= items) return false;
+      ++r;
+      pc.it = item(w);
+      pc.w = w;
+      pc.kind = 0;
+      return true;
+    }
+    if (u >= e) return false;
+    const int w = static_cast<int>(u / static_cast<uint32_t>(nqb));
+    const int i0 = static_cast<int>(u - static_cast<uint32_t>(w) * static_cast<uint32_t>(nqb));
+    const uint32_t left = e - u;
+    const int i1 = left < static_cast<uint32_t>(nqb - i0) ? i0 + static_cast<int>(left) : nqb;
+    pc.it = item(w);
+    pc.it.lo = i0;
+    pc.it.hi = i1;
+    pc.w = w;
+    pc.kind = (i0 == 0 && i1 == nqb) ? 0 : (i0 == 0 ? 1 : 2);
+    u += static_cast<uint32_t>(i1 - i0);
+    return true;
+  }
+};
+
+// Partial dK / dV of a split item, one slot per CTA: [dV, dK][64 columns][128 key rows] f32
+// (unscaled); plus one ready flag per compute warp, zeroed by the delta kernel of the call.
+constexpr int kFusedSlotFloats = 2 * 64 * kT;
+
 // dK, dV and dQ in one pass over (key tile, query block) with D = 64: the dK/dV kernel above
 // with dS^T in shared memory instead of tensor memory. There one buffer serves as the K-major A
 // operand of dK += dS^T Q and, read MN-major, as the A operand of dQ_i = dS K (the tutorial's
@@ -803,7 +864,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const float* __restrict__ LSE, const float* __restrict__ delta, uint16_t* __restrict__ dK,
                        uint16_t* __restrict__ dV, const __grid_constant__ CUtensorMap tmQacc, int BH, int M, int N,
-                       float scale,
+                       float scale, float* __restrict__ part_ws, uint32_t* __restrict__ flags,
                        DevStatus* status, unsigned long long budget_ns) {
   constexpr int D = 64;
   using C = FusedCfg;
@@ -824,6 +885,8 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
   const float sl2 = scale * kLog2eB;
+  const bool split = !CAUSAL && part_ws != nullptr;  // the host checks items * nqb < 2^31
+  const uint32_t units = split ? static_cast<uint32_t>(items) * static_cast<uint32_t>(nqb) : 0u;
   auto item = [&](int w) {
     BwdItem it;
     // causal: key tiles with the most query blocks (the first ones) go first, all heads of a
@@ -884,16 +947,13 @@ __global__ void __launch_bounds__(kThreadsO, 1)
     uint32_t it_s = 0;
     int n_item = 0;
     bool ok = true;
-    int r = 0;
-    int w = item_of_round<CAUSAL>(0, items);
-    BwdItem itm{};
-    // first item that has a query block (items without one need only their fixed tiles)
-    if (w < items) {
-      itm = item(w);
-      if (itm.lo < itm.hi) fetch(itm, itm.lo);
-    }
-    for (; w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
-      itm = item(w);
+    FusedSched<CAUSAL> sch(split, units);
+    FusedPiece pc;
+    bool have = sch.next(pc, items, nqb, item);
+    // first piece that has a query block (items without one need only their fixed tiles)
+    if (have && pc.it.lo < pc.it.hi) fetch(pc.it, pc.it.lo);
+    for (; have && ok; have = sch.next(pc, items, nqb, item), ++n_item) {
+      const BwdItem itm = pc.it;
       if (lane == 0) {
         ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10);
         if (ok) {
@@ -923,15 +983,16 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(fb);
-        // next block's values: this item's next block, else the first block of the next
-        // item that has one
+        // next block's values: this piece's next block, else the first block of the next
+        // piece that has one
         if (i + 1 < itm.hi) {
           fetch(itm, i + 1);
         } else {
-          for (int r2 = r + 1, w2 = item_of_round<CAUSAL>(r2, items); w2 < items; w2 = item_of_round<CAUSAL>(++r2, items)) {
-            const BwdItem nx = item(w2);
-            if (nx.lo < nx.hi) {
-              fetch(nx, nx.lo);
+          FusedSched<CAUSAL> peek = sch;
+          FusedPiece nx;
+          while (peek.next(nx, items, nqb, item)) {
+            if (nx.it.lo < nx.it.hi) {
+              fetch(nx.it, nx.it.lo);
               break;
             }
           }
@@ -972,8 +1033,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
         commit(&hdr->dp_full);
       };
-      for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
-        const BwdItem itm = item(w);
+      FusedSched<CAUSAL> sch(split, units);
+      FusedPiece pc;
+      for (; ok && sch.next(pc, items, nqb, item); ++n_item) {
+        const BwdItem itm = pc.it;
         if (scores) {
           if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
           if (itm.lo < itm.hi) {
@@ -1100,8 +1163,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       ++nq;
       return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
     };
-    for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
-      const BwdItem itm = item(w);
+    FusedSched<CAUSAL> sch(split, units);
+    FusedPiece pc;
+    for (; ok && sch.next(pc, items, nqb, item); ++n_item) {
+      const BwdItem itm = pc.it;
       const int key = itm.r0 + quarter * 32 + lane;
       for (int i = itm.lo; i < itm.hi; ++i, ++it_s, ++nb) {
         const int st = it_s % C::kStages;
@@ -1186,29 +1251,82 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       }
       if (ok && itm.lo < itm.hi) ok = dq_readout(itm.bh, itm.hi - 1);  // the item's last block
       if (!ok) break;
-      // epilogue: this warp writes columns [32 * half, 32 * half + 32) of dV and scale * dK
+      // epilogue: this warp's columns [32 * half, 32 * half + 32) of dV and dK, for key row rr
       ok = wait_all(&hdr->acc_full, n_item & 1, 35);
       if (!ok) break;
-      const bool valid = key < N;
-      const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
-      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+      const int rr = quarter * 32 + lane;
+      float g2[2][32];
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t a[32];
         ptx::tmem_ld32(tmem + lane_sel + (part == 0 ? cdV : cdK) + 32 * half, a);
         ptx::tmem_wait_ld32(a);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) g2[part][k] = __uint_as_float(a[k]);
+      }
+      ptx::tc_fence_before();
+      // slot element (part, column, key row); a warp's 32 rows of one column are one 128-byte line
+      auto slot_at = [&](uint32_t c, int part, int k) {
+        return part_ws + static_cast<size_t>(c) * kFusedSlotFloats + (part * 64 + 32 * half + k) * kT + rr;
+      };
+      if (pc.kind == 2) {
+        // later blocks of a split item: the raw sums go to this CTA's slot, then this warp's flag
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int k = 0; k < 32; ++k) *slot_at(blockIdx.x, part, k) = g2[part][k];
+        __threadfence();  // every lane's slot writes, at gpu scope, before the flag
+        __syncwarp();
+        if (lane == 0) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + warp, 1u);
+        continue;
+      }
+      if (pc.kind == 1) {
+        // first blocks of a split item: add the partials of the CTAs that took the rest (they
+        // reached those pieces first, so they are normally long published)
+        const uint32_t end_u = static_cast<uint32_t>(pc.w + 1) * static_cast<uint32_t>(nqb);
+        for (uint32_t c2 = blockIdx.x + 1;
+             c2 < gridDim.x && FusedSched<CAUSAL>::start(c2, units) < end_u && ok; ++c2) {
+          // a CTA with an empty range (more CTAs than units) writes no partial
+          if (FusedSched<CAUSAL>::start(c2 + 1, units) == FusedSched<CAUSAL>::start(c2, units)) continue;
+          const uint32_t* f = flags + static_cast<size_t>(c2) * 8 + warp;
+          bool got = true;
+          if (lane == 0) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            got = false;
+            for (uint32_t k = 0; k < (1u << 30); ++k) {
+              if (ptx::ld_acquire_u32(f) == 1u) {
+                got = true;
+                break;
+              }
+              if ((k & 255u) == 255u && (*wc.abort_flag || ptx::globaltimer_ns() - t0 > wc.budget_ns)) break;
+            }
+            if (!got) ptx::raise_error(wc, kStatusTimeout, 39);
+          }
+          ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
+          if (!ok) break;
+          (void)ptx::ld_acquire_u32(f);  // orders this lane's reads of the slot after the flag
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int k = 0; k < 32; ++k) g2[part][k] += *slot_at(c2, part, k);
+        }
+        if (!ok) break;
+      }
+      const bool valid = key < N;
+      const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
         const float f = part == 0 ? 1.f : scale;
         uint32_t h[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          h[k] = none ? 0u : pack2<BF16>(__uint_as_float(a[2 * k]) * f, __uint_as_float(a[2 * k + 1]) * f);
+        for (int k = 0; k < 16; ++k) h[k] = none ? 0u : pack2<BF16>(g2[part][2 * k] * f, g2[part][2 * k + 1] * f);
         if (valid) {
           uint4* d4 = reinterpret_cast<uint4*>((part == 0 ? dV : dK) + g);
 #pragma unroll
           for (int v = 0; v < 4; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
         }
       }
-      ptx::tc_fence_before();
     }
   }
 
@@ -1492,8 +1610,11 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __res
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                          void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, float scale,
-                         int dtype, const LaunchCtx& ctx) {
+                         int dtype, const BwdSplit& sp, const LaunchCtx& ctx) {
   using C = BwdCfg<D>;
+  const bool split = D == 64 && !CAUSAL && dQacc != nullptr && sp.ws != nullptr;
+  uint32_t* flags =
+      split ? reinterpret_cast<uint32_t*>(sp.ws + static_cast<size_t>(ctx.num_sms) * kFusedSlotFloats) : nullptr;
   // delta = rowsum(dO o O)
   {
     const long long rows = static_cast<long long>(BH) * M;
@@ -1502,10 +1623,12 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     const long long cap = static_cast<long long>(ctx.num_sms) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    // the fused D = 64 pass accumulates dQ into dQacc, which this kernel zeroes on the way
+    // the fused D = 64 pass accumulates dQ into dQacc, which this kernel zeroes on the way, and
+    // its split schedule's ready flags start at zero
     float* zero = D == 64 ? dQacc : nullptr;
     bwd_delta_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
-        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, rows);
+        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, flags,
+        split ? ctx.num_sms * 8 : 0, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1520,27 +1643,32 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       CUtensorMap macc;
       if (!make_tmap_3d(&macc, dQacc, kF32, D, M, BH, 32, kT)) return cudaErrorInvalidValue;
       const long long items = static_cast<long long>(BH) * nkb;
-      const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
       auto kern = bwd_fused64_kernel<BF16, CAUSAL>;
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedCfg::kSmem);
       if (e != cudaSuccess) return e;
-      // Both later kernels are launched as programmatic dependents: each starts its set-up
-      // while the kernel before it drains and waits (griddepcontrol.wait) before touching
-      // that kernel's results.
+      // The later kernels are launched as programmatic dependents: each starts its set-up while
+      // the kernel before it drains and waits (griddepcontrol.wait) before touching that
+      // kernel's results. The split schedule instead needs every CTA resident at once (a CTA
+      // may wait for the partial of a later one): a cooperative launch of one CTA per SM.
       cudaLaunchAttribute pdl[1];
       pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       pdl[0].val.programmaticStreamSerializationAllowed = 1;
+      cudaLaunchAttribute coop[1];
+      coop[0].id = cudaLaunchAttributeCooperative;
+      coop[0].val.cooperative = 1;
       cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(static_cast<unsigned>(grid));
+      cfg.gridDim = dim3(static_cast<unsigned>(split ? ctx.num_sms : (items < ctx.num_sms ? items : ctx.num_sms)));
       cfg.blockDim = dim3(kThreadsO);
       cfg.dynamicSmemBytes = FusedCfg::kSmem;
       cfg.stream = ctx.stream;
-      cfg.attrs = pdl;
+      cfg.attrs = split ? coop : pdl;
       cfg.numAttrs = 1;
       e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, LSE, static_cast<const float*>(delta),
                              static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), macc, BH, M, N, scale,
-                             ctx.status, ctx.wait_budget_ns);
+                             split ? sp.ws : static_cast<float*>(nullptr), flags, ctx.status, ctx.wait_budget_ns);
       if (e != cudaSuccess) return e;
+      cfg.attrs = pdl;
+      cfg.numAttrs = split ? 0 : 1;  // behind the cooperative launch: an ordinary one
       const long long n4 = static_cast<long long>(n / 4);
       long long blocks = (n4 + 255) / 256;
       const long long cap = static_cast<long long>(ctx.num_sms) * 8;
@@ -1588,13 +1716,17 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
 
 }  // namespace
 
+size_t bwd_fused_split_bytes(int num_sms) {
+  return static_cast<size_t>(num_sms) * (kFusedSlotFloats * sizeof(float) + 8 * sizeof(uint32_t));
+}
+
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                        void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, int D,
-                       float scale, bool causal, int dtype, const LaunchCtx& ctx) {
+                       float scale, bool causal, int dtype, const BwdSplit& sp, const LaunchCtx& ctx) {
   const bool bf = dtype == kBF16;
 #define FA_B(DD, BB, CC)                                                                                       \
   if (D == DD && bf == BB && causal == CC)                                                                     \
-    return launch_bwd_t<DD, BB, CC>(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, dQacc, BH, M, N, scale, dtype, ctx);
+    return launch_bwd_t<DD, BB, CC>(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, dQacc, BH, M, N, scale, dtype, sp, ctx);
   FA_B(64, false, false)
   FA_B(64, false, true)
   FA_B(64, true, false)

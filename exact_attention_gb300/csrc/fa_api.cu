@@ -211,6 +211,23 @@ bool use_split(int BH, int M, int N, int causal, int num_sms) {
   return pairs * 10 < rounds * num_sms * 9;
 }
 
+// Whether the fused backward (fa_bwd_ws, D = 64) runs its split schedule: non-causal calls
+// whose whole key tiles would leave the last round of CTAs less than 90 % full.
+// FA_BWD_SPLIT=0 / 1 forces it off / on (non-causal only; tests use it).
+bool use_bwd_split(int BH, int M, int N, int D, int causal, int num_sms) {
+  if (D != 64 || causal) return false;
+  const long long items = static_cast<long long>(BH) * ((N + 127) / 128);
+  const long long units = items * ((M + 127) / 128);
+  if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
+  if (const char* e = std::getenv("FA_BWD_SPLIT")) {
+    if (e[0] == '0') return false;
+    if (e[0] == '1') return true;
+  }
+  if (units < 4ll * num_sms) return false;
+  const long long rounds = (items + num_sms - 1) / num_sms;
+  return items * 10 < rounds * num_sms * 9;
+}
+
 std::atomic<uint32_t> g_epoch{0};
 std::atomic<int> g_inject{0};  // fa_debug_inject: consumed by the next decode launch
 
@@ -295,8 +312,8 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
 // fa_bwd / fa_bwd_ws: delta_ws holds delta (B*H*M f32); dQacc, when not null, the fused path's f32
 // dQ accumulator (B*H*M*64).
 fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                   void* dQ, void* dK, void* dV, float* delta_ws, float* dQacc, int B, int H, int M, int N, int D,
-                   float scale, int causal, fa_dtype dtype, void* stream, const char* name) {
+                   void* dQ, void* dK, void* dV, float* delta_ws, float* dQacc, float* split_ws, int B, int H, int M,
+                   int N, int D, float scale, int causal, fa_dtype dtype, void* stream, const char* name) {
   FA_TRY(check_dtype(dtype));
   FA_TRY(check_sizes(B, H, M, N, D));
   if (dtype == FA_F32) return fail(FA_ERR_UNSUPPORTED, "%s supports FA_F16 and FA_BF16", name);
@@ -315,8 +332,10 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   FA_TRY(check_ptr(delta_ws, "delta_ws"));
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
+  BwdSplit sp{nullptr};
+  if (dQacc != nullptr && split_ws != nullptr && use_bwd_split(B * H, M, N, D, causal, ctx.num_sms)) sp.ws = split_ws;
   cudaError_t e =
-      launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, dQacc, B * H, M, N, D, scale, causal != 0, dtype, ctx);
+      launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, dQacc, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
   if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "%s: TMA descriptor rejected by the driver", name);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
@@ -393,16 +412,20 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                  void* dQ, void* dK, void* dV, float* delta_ws, int B, int H, int M, int N, int D, float scale,
                  int causal, fa_dtype dtype, void* stream) {
-  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, nullptr, B, H, M, N, D, scale, causal, dtype, stream,
-                  "fa_bwd");
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, nullptr, nullptr, B, H, M, N, D, scale, causal, dtype,
+                  stream, "fa_bwd");
 }
 
-// workspace of fa_bwd_ws: delta, then (D = 64) the f32 dQ accumulator, 256-byte aligned
+// workspace of fa_bwd_ws: delta, then (D = 64) the f32 dQ accumulator and the split schedule's
+// partial slots and flags, each 256-byte aligned
 size_t fa_bwd_ws_workspace_bytes(int B, int H, int M, int D) {
   if (B <= 0 || H <= 0 || M <= 0 || D <= 0) return 0;
   const size_t rows = static_cast<size_t>(B) * H * M;
   const size_t delta = (rows * sizeof(float) + 255u) & ~static_cast<size_t>(255u);
-  return D == 64 ? delta + rows * 64 * sizeof(float) : delta;
+  if (D != 64) return delta;
+  DevState* st = nullptr;
+  if (device_state(&st) != FA_OK) return 0;
+  return delta + rows * 64 * sizeof(float) + bwd_fused_split_bytes(st->num_sms);
 }
 
 fa_status fa_bwd_ws(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
@@ -413,12 +436,14 @@ fa_status fa_bwd_ws(const void* Q, const void* K, const void* V, const void* O, 
     return fail(FA_ERR_INVALID, "fa_bwd_ws: workspace of %zu bytes, %zu needed", workspace_bytes, need);
   float* delta = static_cast<float*>(workspace);
   float* acc = nullptr;
+  float* split = nullptr;
   if (D == 64 && B * H > 0 && M > 0) {
     const size_t rows = static_cast<size_t>(B) * H * M;
     acc = reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                    ((rows * sizeof(float) + 255u) & ~static_cast<size_t>(255u)));
+    split = acc + rows * 64;  // rows * 256 bytes past a 256-byte boundary
   }
-  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, acc, B, H, M, N, D, scale, causal, dtype, stream,
+  return bwd_impl(Q, K, V, O, dO, LSE, dQ, dK, dV, delta, acc, split, B, H, M, N, D, scale, causal, dtype, stream,
                   "fa_bwd_ws");
 }
 

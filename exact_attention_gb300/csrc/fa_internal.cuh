@@ -70,11 +70,18 @@ size_t fwd_f32_split_bytes(int BH, int M, int parts);
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                            int D, float scale, bool causal, int parts, float* ws, const LaunchCtx& ctx);
 
+// Split schedule of the fused backward (non-causal, D = 64): ws holds bwd_fused_split_bytes of
+// partial dK/dV slots then num_sms * 8 ready flags; ws == nullptr runs whole key tiles.
+struct BwdSplit {
+  float* ws;
+};
+size_t bwd_fused_split_bytes(int num_sms);
+
 // dQacc == nullptr: delta, dK/dV and dQ kernels; else (D = 64) delta, one fused dK/dV/dQ kernel
 // that accumulates dQ in dQacc (B*H*M*D f32), and a conversion of dQacc into dQ.
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                        void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, int D,
-                       float scale, bool causal, int dtype, const LaunchCtx& ctx);
+                       float scale, bool causal, int dtype, const BwdSplit& sp, const LaunchCtx& ctx);
 
 // Encodes a 3-D TMA tensor map over a contiguous [outer, rows, inner] tensor
 // (inner = head dimension) with a box of [box_inner, box_rows, 1] elements and

@@ -108,3 +108,61 @@ def test_backward_fused_matches_three_kernels():
         assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]), causal
         assert torch.equal(a[3], b[3])  # delta
         assert float((a[0].float() - b[0].float()).abs().max()) <= 4e-3, causal
+
+
+SPLIT_SHAPES = [
+    # B, H, M, N
+    (1, 2, 1024, 1024),  # the tutorial's shape
+    (2, 3, 384, 256),
+    (1, 2, 300, 700),    # ragged M and N
+    (1, 1, 8192, 256),   # 128 units for more CTAs: empty ranges, one key tile over many CTAs
+    (3, 5, 640, 1000),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("B,H,M,N", SPLIT_SHAPES)
+def test_backward_fused_split_schedule_matches_oracle(monkeypatch, dtype, B, H, M, N):
+    """The fused pass's split schedule forced on: every SM an equal share of the (key tile,
+    query block) units; a key tile cut by a share boundary gets the partial dK/dV of the SMs
+    holding its later query blocks added in by the SM holding its first ones."""
+    monkeypatch.setenv("FA_BWD_SPLIT", "1")
+    inputs, o, grads, delta = run_bwd(B, H, M, N, 64, dtype, False, 0.125, seed=M + N, fused=True)
+    check(inputs, o, grads, delta, dtype, False, 0.125)
+
+
+def test_backward_fused_split_agrees_with_whole_tiles(monkeypatch):
+    """Split and whole key tiles run the same products; dK and dV differ only in the f32
+    order in which a cut tile's two sums meet, dQ in the order of its reduce-adds."""
+    import torch
+    q, k, v, do = synth.attention_inputs(2, 3, 1000, 900, 64, "f16", seed=12, with_dout=True)
+    qd, kd, vd, dod = (to_device(x, "f16") for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, 0.125, False)
+    monkeypatch.setenv("FA_BWD_SPLIT", "0")
+    a = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False)
+    monkeypatch.setenv("FA_BWD_SPLIT", "1")
+    b = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False)
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    for n in range(3):
+        assert float((a[n].float() - b[n].float()).abs().max()) <= 4e-3, n
+    assert torch.equal(a[3], b[3])  # delta
+
+
+def test_backward_fused_split_reused_workspace(monkeypatch):
+    """Three calls on one workspace: the ready flags the previous call left set are cleared by
+    the next call's delta kernel before its fused pass reads them."""
+    import torch
+    monkeypatch.setenv("FA_BWD_SPLIT", "1")
+    B, H, M, N, D = 1, 3, 512, 640, 64
+    nbytes = fa.fa_bwd_ws_workspace_bytes(B, H, M, D)
+    ws = torch.empty((nbytes // 4,), dtype=torch.float32, device="cuda")
+    for seed in (1, 2, 3):
+        q, k, v, do = synth.attention_inputs(B, H, M, N, D, "f16", seed=seed, with_dout=True)
+        qd, kd, vd, dod = (to_device(x, "f16") for x in (q, k, v, do))
+        o, lse = fa.forward(qd, kd, vd, 0.125, False)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+        st = fa.fa_bwd_ws(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, nbytes, B, H, M, N, D, 0.125, False, fa.FA_F16)
+        assert st == fa.FA_OK, fa.fa_last_error_message()
+        torch.cuda.synchronize()
+        check((q, k, v, do), to_f64(o), (to_f64(dq), to_f64(dk), to_f64(dv)), to_f64(ws[: B * H * M].view(B, H, M)),
+              "f16", False, 0.125)
