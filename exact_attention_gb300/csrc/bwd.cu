@@ -862,8 +862,9 @@ template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsO, 1)
     bwd_fused64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                       const float* __restrict__ LSE, const float* __restrict__ delta, uint16_t* __restrict__ dK,
-                       uint16_t* __restrict__ dV, const __grid_constant__ CUtensorMap tmQacc, int BH, int M, int N,
+                       const float* __restrict__ LSE, const float* __restrict__ delta,
+                       const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
+                       const __grid_constant__ CUtensorMap tmQacc, int BH, int M, int N,
                        float scale, float* __restrict__ part_ws, uint32_t* __restrict__ flags,
                        DevStatus* status, unsigned long long budget_ns) {
   constexpr int D = 64;
@@ -1122,10 +1123,36 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
     };
-    // dQ_i of query block `qb`: TMEM -> the staging boxes (then the TMEM columns are free for the
-    // next product) -> warp 0's lane 0 adds both boxes into the accumulator. Warp-uniform result.
+    // The 32 KB staging area after dS^T is filled by the eight compute warps and drained by bulk
+    // tensor operations that warp 0's lane 0 issues once every warp has written its part: the
+    // dQ_i blocks (added into the accumulator) and each piece's dV / dK tiles (stored). A fill
+    // first waits until the previous drain has read the area. Warp-uniform result.
     uint32_t nq = 0;  // dQ blocks read back (all items)
+    uint32_t ns = 0;  // fills of the staging area
     const bool reducer = warp == 0 && lane == 0;
+    auto stage = [&](const auto& fill, const auto& drain) {
+      if (reducer && ns > 0) {
+        ptx::bulk_wait_read();
+        ptx::mbar_arrive(ptx::smem_u32(&hdr->stg_free));
+      }
+      if (ns > 0 && !wait_all(&hdr->stg_free, (ns - 1u) & 1u, 37)) return false;
+      fill();
+      ptx::fence_proxy_async_smem();  // staging writes -> the TMA engine
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_staged));
+      bool good = true;
+      if (reducer) {
+        good = ptx::mbar_wait(ptx::smem_u32(&hdr->dq_staged), ns & 1u, wc, 38);
+        if (good) {
+          drain();
+          ptx::bulk_commit();
+        }
+      }
+      ++ns;
+      return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+    };
+    // dQ_i of query block `qb`: TMEM -> two f32 boxes [32 d][128 queries] (then the TMEM columns
+    // are free for the next product) -> added into the accumulator
     auto dq_readout = [&](int bh, int qb) {
       if (!wait_all(&hdr->dq_full, nq & 1u, 36)) return false;
       uint32_t a[32];
@@ -1134,34 +1161,20 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_free));
-      // the previous reduce has read the staging boxes
-      if (reducer && nq > 0) {
-        ptx::bulk_wait_read();
-        ptx::mbar_arrive(ptx::smem_u32(&hdr->stg_free));
-      }
-      if (nq > 0 && !wait_all(&hdr->stg_free, (nq - 1u) & 1u, 37)) return false;
-      {
-        const int rr = quarter * 32 + lane;  // query row within the block
-        uint8_t* srow = smem_raw + (sStg - raw) + half * (kT * 128) + rr * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(srow + ((u ^ (rr & 7)) << 4)) =
-              make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-      }
-      ptx::fence_proxy_async_smem();  // staging writes -> the TMA engine
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_staged));
-      bool good = true;
-      if (reducer) {
-        good = ptx::mbar_wait(ptx::smem_u32(&hdr->dq_staged), nq & 1u, wc, 38);
-        if (good) {
-          ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, qb * kT, bh);
-          ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, qb * kT, bh);
-          ptx::bulk_commit();
-        }
-      }
       ++nq;
-      return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+      return stage(
+          [&] {
+            const int rr = quarter * 32 + lane;  // query row within the block
+            uint8_t* srow = smem_raw + (sStg - raw) + half * (kT * 128) + rr * 128;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4*>(srow + ((u ^ (rr & 7)) << 4)) =
+                  make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+          },
+          [&] {
+            ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, qb * kT, bh);
+            ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, qb * kT, bh);
+          });
     };
     FusedSched<CAUSAL> sch(split, units);
     FusedPiece pc;
@@ -1312,25 +1325,35 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         }
         if (!ok) break;
       }
-      const bool valid = key < N;
-      const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
+      // dV and scale * dK in the I/O type, as the two 128 x 64 output tiles (128-byte swizzled
+      // rows, the tensor maps' layout; rows past N are clipped by the maps), stored by TMA
       const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+      uint32_t hv[16], hk[16];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const float f = part == 0 ? 1.f : scale;
-        uint32_t h[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) h[k] = none ? 0u : pack2<BF16>(g2[part][2 * k] * f, g2[part][2 * k + 1] * f);
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>((part == 0 ? dV : dK) + g);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-        }
+      for (int k = 0; k < 16; ++k) {
+        hv[k] = none ? 0u : pack2<BF16>(g2[0][2 * k], g2[0][2 * k + 1]);
+        hk[k] = none ? 0u : pack2<BF16>(g2[1][2 * k] * scale, g2[1][2 * k + 1] * scale);
       }
+      ok = stage(
+          [&] {
+            uint8_t* row = smem_raw + (sStg - raw) + rr * 128;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int v = 4 * half + u;  // this warp's 16-byte chunks of the row
+              *reinterpret_cast<uint4*>(row + ((v ^ (rr & 7)) << 4)) =
+                  make_uint4(hv[4 * u], hv[4 * u + 1], hv[4 * u + 2], hv[4 * u + 3]);
+              *reinterpret_cast<uint4*>(row + kChunkB + ((v ^ (rr & 7)) << 4)) =
+                  make_uint4(hk[4 * u], hk[4 * u + 1], hk[4 * u + 2], hk[4 * u + 3]);
+            }
+          },
+          [&] {
+            ptx::tma_store_3d(&tmdV, sStg, 0, itm.r0, itm.bh);
+            ptx::tma_store_3d(&tmdK, sStg + kChunkB, 0, itm.r0, itm.bh);
+          });
     }
   }
 
-  if (warp == 0 && lane == 0) ptx::bulk_wait_all();  // the reduces have completed
+  if (warp == 0 && lane == 0) ptx::bulk_wait_all();  // the reduces and stores have completed
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kWarpMmaO) {
@@ -1640,35 +1663,34 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
   if constexpr (D == 64) {
     if (dQacc != nullptr) {  // one pass for dK, dV and dQ (dQ accumulated in f32, then converted)
       const size_t n = static_cast<size_t>(BH) * M * D;
-      CUtensorMap macc;
-      if (!make_tmap_3d(&macc, dQacc, kF32, D, M, BH, 32, kT)) return cudaErrorInvalidValue;
+      CUtensorMap macc, mdk, mdv;
+      if (!make_tmap_3d(&macc, dQacc, kF32, D, M, BH, 32, kT) || !make_tmap_3d(&mdk, dK, dtype, D, N, BH, 64, kT) ||
+          !make_tmap_3d(&mdv, dV, dtype, D, N, BH, 64, kT))
+        return cudaErrorInvalidValue;
       const long long items = static_cast<long long>(BH) * nkb;
       auto kern = bwd_fused64_kernel<BF16, CAUSAL>;
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FusedCfg::kSmem);
       if (e != cudaSuccess) return e;
       // The later kernels are launched as programmatic dependents: each starts its set-up while
       // the kernel before it drains and waits (griddepcontrol.wait) before touching that
-      // kernel's results. The split schedule instead needs every CTA resident at once (a CTA
-      // may wait for the partial of a later one): a cooperative launch of one CTA per SM.
+      // kernel's results. Under the split schedule a CTA may wait for the partial of a later
+      // CTA; with one CTA per SM and nothing else on the device they are all resident once the
+      // delta kernel's blocks retire, and the wait is bounded in any case (a cooperative launch,
+      // which would guarantee residency, measured 6 us slower per call).
       cudaLaunchAttribute pdl[1];
       pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       pdl[0].val.programmaticStreamSerializationAllowed = 1;
-      cudaLaunchAttribute coop[1];
-      coop[0].id = cudaLaunchAttributeCooperative;
-      coop[0].val.cooperative = 1;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(split ? ctx.num_sms : (items < ctx.num_sms ? items : ctx.num_sms)));
       cfg.blockDim = dim3(kThreadsO);
       cfg.dynamicSmemBytes = FusedCfg::kSmem;
       cfg.stream = ctx.stream;
-      cfg.attrs = split ? coop : pdl;
-      cfg.numAttrs = 1;
-      e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, LSE, static_cast<const float*>(delta),
-                             static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), macc, BH, M, N, scale,
-                             split ? sp.ws : static_cast<float*>(nullptr), flags, ctx.status, ctx.wait_budget_ns);
-      if (e != cudaSuccess) return e;
       cfg.attrs = pdl;
-      cfg.numAttrs = split ? 0 : 1;  // behind the cooperative launch: an ordinary one
+      cfg.numAttrs = 1;
+      e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, LSE, static_cast<const float*>(delta), mdk, mdv, macc, BH,
+                             M, N, scale, split ? sp.ws : static_cast<float*>(nullptr), flags, ctx.status,
+                             ctx.wait_budget_ns);
+      if (e != cudaSuccess) return e;
       const long long n4 = static_cast<long long>(n / 4);
       long long blocks = (n4 + 255) / 256;
       const long long cap = static_cast<long long>(ctx.num_sms) * 8;

@@ -190,7 +190,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int M);
  * leave the last round of SMs under 90 % busy run a split schedule: every SM
  * takes an equal share of the (key tile, query block) pairs, and a key tile
  * cut between two SMs has the partial dK/dV of the later one added in by the
- * earlier one (a cooperative launch, one CTA per SM).
+ * earlier one (one CTA per SM; an SM that waits longer than the wait budget for
+ * a partial, which takes another job holding SMs for that long, ends the call
+ * with FA_ERR_TIMEOUT).
  * The summation order of dQ's key blocks follows the SMs' timing, so dQ can
  * differ between runs in the last bits of the f32 accumulator (dK, dV do not).
  */
