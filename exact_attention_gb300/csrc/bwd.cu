@@ -858,8 +858,12 @@ constexpr int kFusedSlotFloats = 2 * 64 * kT;
 // query block's 128 rows of 64 floats are contiguous there). A later kernel scales and converts
 // the accumulator. TMEM: S^T [0,128), dP^T [128,256), P^T packed [256,320), dQ_i [320,384),
 // dV [384,448), dK [448,512).
+// Warps: compute 0-7, producer 8, MMA issuers 9 (scores) and 10 (gradients), and 11, which drains
+// the staging area (the bulk reduce-adds of dQ_i and the stores of dV / dK).
+constexpr int kThreadsF = 384;
+constexpr int kWarpDrainF = 11;
 template <bool BF16, bool CAUSAL>
-__global__ void __launch_bounds__(kThreadsO, 1)
+__global__ void __launch_bounds__(kThreadsF, 1)
     bwd_fused64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                        const float* __restrict__ LSE, const float* __restrict__ delta,
@@ -1105,6 +1109,41 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       commit(&hdr->mma_done[me]);
       ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[me]), 0u, 1000000000ull);
     }
+  } else if (warp == kWarpDrainF) {
+    // ------------------------------------------------------------ staging drain (lane 0)
+    // Walks the fills of the staging area in the compute warps' order: per piece, the dQ_i of each
+    // of its blocks, then (unless the piece ends in a partial) its dV / dK tiles. Per fill: wait
+    // until the eight compute warps have written it, issue the bulk operations, wait until they
+    // have read the area and release it for the next fill.
+    if (lane == 0) {
+      uint32_t ns = 0;
+      bool ok = true;
+      auto drain = [&](auto&& issue) {
+        if (!ptx::mbar_wait(ptx::smem_u32(&hdr->dq_staged), ns & 1u, wc, 38)) return false;
+        issue();
+        ptx::bulk_commit();
+        ptx::bulk_wait_read();
+        ptx::mbar_arrive(ptx::smem_u32(&hdr->stg_free));
+        ++ns;
+        return true;
+      };
+      FusedSched<CAUSAL> sch(split, units);
+      FusedPiece pc;
+      while (ok && sch.next(pc, items, nqb, item)) {
+        const BwdItem itm = pc.it;
+        for (int i = itm.lo; i < itm.hi && ok; ++i)
+          ok = drain([&] {
+            ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, i * kT, itm.bh);
+            ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, i * kT, itm.bh);
+          });
+        if (ok && pc.kind != 2)
+          ok = drain([&] {
+            ptx::tma_store_3d(&tmdV, sStg, 0, itm.r0, itm.bh);
+            ptx::tma_store_3d(&tmdK, sStg + kChunkB, 0, itm.r0, itm.bh);
+          });
+      }
+      ptx::bulk_wait_all();  // the reduces and stores have completed
+    }
   } else {
     // ------------------------------------------------------------ compute warps: one key row per thread
     const int quarter = warp & 3, half = warp >> 2;
@@ -1123,37 +1162,24 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
     };
-    // The 32 KB staging area after dS^T is filled by the eight compute warps and drained by bulk
-    // tensor operations that warp 0's lane 0 issues once every warp has written its part: the
-    // dQ_i blocks (added into the accumulator) and each piece's dV / dK tiles (stored). A fill
-    // first waits until the previous drain has read the area. Warp-uniform result.
+    // The 32 KB staging area after dS^T is filled by the eight compute warps and drained by the
+    // drain warp's bulk tensor operations: the dQ_i blocks (added into the accumulator) and each
+    // piece's dV / dK tiles (stored). A fill first waits until the previous drain has read the
+    // area. Warp-uniform result.
     uint32_t nq = 0;  // dQ blocks read back (all items)
     uint32_t ns = 0;  // fills of the staging area
-    const bool reducer = warp == 0 && lane == 0;
-    auto stage = [&](const auto& fill, const auto& drain) {
-      if (reducer && ns > 0) {
-        ptx::bulk_wait_read();
-        ptx::mbar_arrive(ptx::smem_u32(&hdr->stg_free));
-      }
+    auto stage = [&](const auto& fill) {
       if (ns > 0 && !wait_all(&hdr->stg_free, (ns - 1u) & 1u, 37)) return false;
       fill();
       ptx::fence_proxy_async_smem();  // staging writes -> the TMA engine
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_staged));
-      bool good = true;
-      if (reducer) {
-        good = ptx::mbar_wait(ptx::smem_u32(&hdr->dq_staged), ns & 1u, wc, 38);
-        if (good) {
-          drain();
-          ptx::bulk_commit();
-        }
-      }
       ++ns;
-      return __shfl_sync(0xFFFFFFFFu, good, 0) != 0;
+      return true;
     };
-    // dQ_i of query block `qb`: TMEM -> two f32 boxes [32 d][128 queries] (then the TMEM columns
-    // are free for the next product) -> added into the accumulator
-    auto dq_readout = [&](int bh, int qb) {
+    // dQ_i of the previous block: TMEM -> two f32 boxes [32 d][128 queries] (then the TMEM columns
+    // are free for the next product), which the drain warp adds into the accumulator
+    auto dq_readout = [&]() {
       if (!wait_all(&hdr->dq_full, nq & 1u, 36)) return false;
       uint32_t a[32];
       ptx::tmem_ld32(tmem + lane_sel + cdQ + 32 * half, a);
@@ -1162,19 +1188,14 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_free));
       ++nq;
-      return stage(
-          [&] {
-            const int rr = quarter * 32 + lane;  // query row within the block
-            uint8_t* srow = smem_raw + (sStg - raw) + half * (kT * 128) + rr * 128;
+      return stage([&] {
+        const int rr = quarter * 32 + lane;  // query row within the block
+        uint8_t* srow = smem_raw + (sStg - raw) + half * (kT * 128) + rr * 128;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-              *reinterpret_cast<uint4*>(srow + ((u ^ (rr & 7)) << 4)) =
-                  make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
-          },
-          [&] {
-            ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, qb * kT, bh);
-            ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, qb * kT, bh);
-          });
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(srow + ((u ^ (rr & 7)) << 4)) =
+              make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+      });
     };
     FusedSched<CAUSAL> sch(split, units);
     FusedPiece pc;
@@ -1258,11 +1279,11 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         signal(&hdr->sig2);
         // dQ of the previous block (its product was issued after the previous sig2)
         if (i > itm.lo) {
-          ok = dq_readout(itm.bh, i - 1);
+          ok = dq_readout();
           if (!ok) break;
         }
       }
-      if (ok && itm.lo < itm.hi) ok = dq_readout(itm.bh, itm.hi - 1);  // the item's last block
+      if (ok && itm.lo < itm.hi) ok = dq_readout();  // the piece's last block
       if (!ok) break;
       // epilogue: this warp's columns [32 * half, 32 * half + 32) of dV and dK, for key row rr
       ok = wait_all(&hdr->acc_full, n_item & 1, 35);
@@ -1334,26 +1355,20 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         hv[k] = none ? 0u : pack2<BF16>(g2[0][2 * k], g2[0][2 * k + 1]);
         hk[k] = none ? 0u : pack2<BF16>(g2[1][2 * k] * scale, g2[1][2 * k + 1] * scale);
       }
-      ok = stage(
-          [&] {
-            uint8_t* row = smem_raw + (sStg - raw) + rr * 128;
+      ok = stage([&] {
+        uint8_t* row = smem_raw + (sStg - raw) + rr * 128;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int v = 4 * half + u;  // this warp's 16-byte chunks of the row
-              *reinterpret_cast<uint4*>(row + ((v ^ (rr & 7)) << 4)) =
-                  make_uint4(hv[4 * u], hv[4 * u + 1], hv[4 * u + 2], hv[4 * u + 3]);
-              *reinterpret_cast<uint4*>(row + kChunkB + ((v ^ (rr & 7)) << 4)) =
-                  make_uint4(hk[4 * u], hk[4 * u + 1], hk[4 * u + 2], hk[4 * u + 3]);
-            }
-          },
-          [&] {
-            ptx::tma_store_3d(&tmdV, sStg, 0, itm.r0, itm.bh);
-            ptx::tma_store_3d(&tmdK, sStg + kChunkB, 0, itm.r0, itm.bh);
-          });
+        for (int u = 0; u < 4; ++u) {
+          const int v = 4 * half + u;  // this warp's 16-byte chunks of the row
+          *reinterpret_cast<uint4*>(row + ((v ^ (rr & 7)) << 4)) =
+              make_uint4(hv[4 * u], hv[4 * u + 1], hv[4 * u + 2], hv[4 * u + 3]);
+          *reinterpret_cast<uint4*>(row + kChunkB + ((v ^ (rr & 7)) << 4)) =
+              make_uint4(hk[4 * u], hk[4 * u + 1], hk[4 * u + 2], hk[4 * u + 3]);
+        }
+      });
     }
   }
 
-  if (warp == 0 && lane == 0) ptx::bulk_wait_all();  // the reduces and stores have completed
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kWarpMmaO) {
@@ -1682,7 +1697,7 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       pdl[0].val.programmaticStreamSerializationAllowed = 1;
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(static_cast<unsigned>(split ? ctx.num_sms : (items < ctx.num_sms ? items : ctx.num_sms)));
-      cfg.blockDim = dim3(kThreadsO);
+      cfg.blockDim = dim3(kThreadsF);
       cfg.dynamicSmemBytes = FusedCfg::kSmem;
       cfg.stream = ctx.stream;
       cfg.attrs = pdl;
