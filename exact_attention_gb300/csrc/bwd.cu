@@ -408,8 +408,8 @@ struct OvHdr {
   unsigned long long dq_full, dq_free, dq_staged, stg_free;
   uint32_t tmem_base;
   int abort_flag;
-  float nlse2[kStagesMax][kT];  // per streamed block: -LSE * log2(e) (dK/dV only)
-  float ndlt[kStagesMax][kT];   // per streamed block: -delta (dK/dV only)
+  alignas(16) float nlse2[kStagesMax][kT];  // per streamed block: -LSE * log2(e) (dK/dV only)
+  alignas(16) float ndlt[kStagesMax][kT];   // per streamed block: -delta (dK/dV only)
 };
 constexpr uint32_t kOvHdrBytes = (sizeof(OvHdr) + 127u) & ~127u;
 
@@ -1220,15 +1220,22 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           ptx::tmem_wait_ld32(s);
           ptx::tmem_wait_ld32(s + 32);
           const float2 c2 = make_float2(sl2, sl2);
+          // the block's -LSE values are read four at a time: every lane reads the same 16 bytes
 #pragma unroll
-          for (int q = 0; q < 64; q += 2) {
-            const float2 nlq = *reinterpret_cast<const float2*>(nl + q);
-            const float2 x = ptx::ffma2(make_float2(__uint_as_float(s[q]), __uint_as_float(s[q + 1])), c2, nlq);
-            p[q] = ptx::ex2(x.x);
-            p[q + 1] = ptx::ex2(x.y);
+          for (int q = 0; q < 64; q += 4) {
+            const float4 n4 = *reinterpret_cast<const float4*>(nl + q);
+            const float2 x0 = ptx::ffma2(make_float2(__uint_as_float(s[q]), __uint_as_float(s[q + 1])), c2,
+                                         make_float2(n4.x, n4.y));
+            const float2 x1 = ptx::ffma2(make_float2(__uint_as_float(s[q + 2]), __uint_as_float(s[q + 3])), c2,
+                                         make_float2(n4.z, n4.w));
+            p[q] = ptx::ex2(x0.x);
+            p[q + 1] = ptx::ex2(x0.y);
+            p[q + 2] = ptx::ex2(x1.x);
+            p[q + 3] = ptx::ex2(x1.y);
             if (diag) {  // key j is visible to query i iff j <= i
-              if (qb + q < key) p[q] = 0.f;
-              if (qb + q + 1 < key) p[q + 1] = 0.f;
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (qb + q + e < key) p[q + e] = 0.f;
             }
           }
         }
@@ -1257,11 +1264,17 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           ptx::tmem_wait_ld32(dp);
           uint32_t pk[16];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float2 ndq = *reinterpret_cast<const float2*>(nd + c + 2 * k);
-            const float2 t = ptx::fadd2(make_float2(__uint_as_float(dp[2 * k]), __uint_as_float(dp[2 * k + 1])), ndq);
-            const float2 ds = ptx::fmul2(make_float2(p[c + 2 * k], p[c + 2 * k + 1]), t);
-            pk[k] = pack2<BF16>(ds.x, ds.y);
+          for (int k = 0; k < 16; k += 2) {
+            const float4 n4 = *reinterpret_cast<const float4*>(nd + c + 2 * k);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const float2 ndq = e == 0 ? make_float2(n4.x, n4.y) : make_float2(n4.z, n4.w);
+              const int kk = k + e;
+              const float2 t =
+                  ptx::fadd2(make_float2(__uint_as_float(dp[2 * kk]), __uint_as_float(dp[2 * kk + 1])), ndq);
+              const float2 ds = ptx::fmul2(make_float2(p[c + 2 * kk], p[c + 2 * kk + 1]), t);
+              pk[kk] = pack2<BF16>(ds.x, ds.y);
+            }
           }
           // row `key` of dS^T, queries [c0 + c, c0 + c + 32): four 16-byte chunks of chunk `half`
           {
