@@ -858,10 +858,17 @@ constexpr int kFusedSlotFloats = 2 * 64 * kT;
 // query block's 128 rows of 64 floats are contiguous there). A later kernel scales and converts
 // the accumulator. TMEM: S^T [0,128), dP^T [128,256), P^T packed [256,320), dQ_i [320,384),
 // dV [384,448), dK [448,512).
-// Warps: compute 0-7, producer 8, MMA issuers 9 (scores) and 10 (gradients), and 11, which drains
-// the staging area (the bulk reduce-adds of dQ_i and the stores of dV / dK).
-constexpr int kThreadsF = 384;
-constexpr int kWarpDrainF = 11;
+// Warps: kCwF compute warps (kCwF / 4 per TMEM lane quarter: each thread takes kQcF of its key
+// row's 128 query columns and kDcF of its 64 gradient columns), then the producer, the MMA
+// issuers of the scores and of the gradients, and a warp that drains the staging area (the bulk
+// reduce-adds of dQ_i and the stores of dV / dK).
+constexpr int kCwF = 8;
+constexpr int kSlicesF = kCwF / 4;
+constexpr int kQcF = kT / kSlicesF;
+constexpr int kDcF = 64 / kSlicesF;
+constexpr int kWarpProdF = kCwF, kWarpMmaF = kCwF + 1, kWarpGradF = kCwF + 2, kWarpDrainF = kCwF + 3;
+constexpr int kThreadsF = (kCwF + 4) * 32;
+static_assert(kQcF % 32 == 0 && (kDcF == 16 || kDcF == 32), "compute-warp slicing");
 template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsF, 1)
     bwd_fused64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -914,12 +921,14 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     ov_init(hdr, C::kStages, 2);  // full: TMA bytes + LSE/delta staging
     ptx::mbar_init(ptx::smem_u32(&hdr->fixed_empty), 2);  // K is read by both issuers here
     ptx::mbar_init(ptx::smem_u32(&hdr->dq_full), 1);
-    ptx::mbar_init(ptx::smem_u32(&hdr->dq_free), 8);
-    ptx::mbar_init(ptx::smem_u32(&hdr->dq_staged), 8);
+    ptx::mbar_init(ptx::smem_u32(&hdr->sig1), kCwF);
+    ptx::mbar_init(ptx::smem_u32(&hdr->sig2), kCwF);
+    ptx::mbar_init(ptx::smem_u32(&hdr->dq_free), kCwF);
+    ptx::mbar_init(ptx::smem_u32(&hdr->dq_staged), kCwF);
     ptx::mbar_init(ptx::smem_u32(&hdr->stg_free), 1);
     ptx::fence_mbar_init();
   }
-  if (warp == kWarpMmaO) {
+  if (warp == kWarpMmaF) {
     ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
     ptx::tmem_relinquish();
   }
@@ -932,7 +941,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDkDv};
 
-  if (warp == kWarpProdO) {
+  if (warp == kWarpProdF) {
     // ------------------------------------------------------------ producer (whole warp)
     // Walks (item, query block) in order. -LSE (base 2) and -delta of a block's queries
     // are read from global memory one block ahead into registers (lane l holds queries
@@ -1008,10 +1017,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
         ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
     }
-  } else if (warp == kWarpMmaO || warp == kWarpGradO) {
+  } else if (warp == kWarpMmaF || warp == kWarpGradF) {
     // ------------------------------------------------------------ MMA issuers (lane 0)
     if (lane == 0) {
-      const bool scores = warp == kWarpMmaO;
+      const bool scores = warp == kWarpMmaF;
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
       constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
@@ -1146,9 +1155,20 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     }
   } else {
     // ------------------------------------------------------------ compute warps: one key row per thread
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, slice = warp >> 2;
     const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's query columns [c0, c0 + 64)
+    const uint32_t c0 = static_cast<uint32_t>(slice * kQcF);  // this warp's query columns [c0, c0 + kQcF)
+    const int d0 = slice * kDcF;                              // and gradient columns [d0, d0 + kDcF)
+    // kDcF gradient columns of this thread's TMEM lane
+    auto ld_grad = [&](uint32_t col, uint32_t* a) {
+      if constexpr (kDcF == 32) {
+        ptx::tmem_ld32(tmem + lane_sel + col, a);
+        ptx::tmem_wait_ld32(a);
+      } else {
+        ptx::tmem_ld16(tmem + lane_sel + col, a);
+        ptx::tmem_wait_ld16(a);
+      }
+    };
     uint32_t it_s = 0, nb = 0;  // blocks processed (all items): s_full/dp_full/free phases
     int n_item = 0;
     bool ok = true;
@@ -1162,7 +1182,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(bar));
     };
-    // The 32 KB staging area after dS^T is filled by the eight compute warps and drained by the
+    // The 32 KB staging area after dS^T is filled by the compute warps and drained by the
     // drain warp's bulk tensor operations: the dQ_i blocks (added into the accumulator) and each
     // piece's dV / dK tiles (stored). A fill first waits until the previous drain has read the
     // area. Warp-uniform result.
@@ -1181,20 +1201,22 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     // are free for the next product), which the drain warp adds into the accumulator
     auto dq_readout = [&]() {
       if (!wait_all(&hdr->dq_full, nq & 1u, 36)) return false;
-      uint32_t a[32];
-      ptx::tmem_ld32(tmem + lane_sel + cdQ + 32 * half, a);
-      ptx::tmem_wait_ld32(a);
+      uint32_t a[kDcF];
+      ld_grad(cdQ + d0, a);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->dq_free));
       ++nq;
       return stage([&] {
         const int rr = quarter * 32 + lane;  // query row within the block
-        uint8_t* srow = smem_raw + (sStg - raw) + half * (kT * 128) + rr * 128;
+        // columns [d0, d0 + kDcF) sit in box d0 / 32 from its 16-byte chunk (d0 % 32) / 4
+        uint8_t* srow = smem_raw + (sStg - raw) + (d0 / 32) * (kT * 128) + rr * 128;
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(srow + ((u ^ (rr & 7)) << 4)) =
+        for (int u = 0; u < kDcF / 4; ++u) {
+          const int v = (d0 % 32) / 4 + u;
+          *reinterpret_cast<uint4*>(srow + ((v ^ (rr & 7)) << 4)) =
               make_uint4(a[4 * u], a[4 * u + 1], a[4 * u + 2], a[4 * u + 3]);
+        }
       });
     };
     FusedSched<CAUSAL> sch(split, units);
@@ -1212,17 +1234,17 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const float* nd = hdr->ndlt[st] + c0;
         const int qb = i * kT + static_cast<int>(c0);  // first query of this warp's columns
         const bool diag = CAUSAL && qb < key;          // some of these queries precede the key
-        float p[64];
+        float p[kQcF];
         {
-          uint32_t s[64];
-          ptx::tmem_ld32(tmem + lane_sel + cS + c0, s);
-          ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
-          ptx::tmem_wait_ld32(s);
-          ptx::tmem_wait_ld32(s + 32);
+          uint32_t s[kQcF];
+#pragma unroll
+          for (int c = 0; c < kQcF; c += 32) ptx::tmem_ld32(tmem + lane_sel + cS + c0 + c, s + c);
+#pragma unroll
+          for (int c = 0; c < kQcF; c += 32) ptx::tmem_wait_ld32(s + c);
           const float2 c2 = make_float2(sl2, sl2);
           // the block's -LSE values are read four at a time: every lane reads the same 16 bytes
 #pragma unroll
-          for (int q = 0; q < 64; q += 4) {
+          for (int q = 0; q < kQcF; q += 4) {
             const float4 n4 = *reinterpret_cast<const float4*>(nl + q);
             const float2 x0 = ptx::ffma2(make_float2(__uint_as_float(s[q]), __uint_as_float(s[q + 1])), c2,
                                          make_float2(n4.x, n4.y));
@@ -1245,7 +1267,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           if (!ok) break;
         }
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kQcF; c += 32) {
           uint32_t pk[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) pk[k] = pack2<BF16>(p[c + 2 * k], p[c + 2 * k + 1]);
@@ -1258,7 +1280,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         if (ok && nb > 0) ok = wait_all(&hdr->free2, (nb - 1u) & 1u, 34);
         if (!ok) break;
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) {
+        for (int c = 0; c < kQcF; c += 32) {
           uint32_t dp[32];
           ptx::tmem_ld32(tmem + lane_sel + cdP + c0 + c, dp);
           ptx::tmem_wait_ld32(dp);
@@ -1276,13 +1298,15 @@ __global__ void __launch_bounds__(kThreadsF, 1)
               pk[kk] = pack2<BF16>(ds.x, ds.y);
             }
           }
-          // row `key` of dS^T, queries [c0 + c, c0 + c + 32): four 16-byte chunks of chunk `half`
+          // row `key` of dS^T, queries [c0 + c, c0 + c + 32): four 16-byte chunks of the
+          // 64-query chunk (c0 + c) / 64
           {
             const int rr = quarter * 32 + lane;
-            uint8_t* drow = smem_raw + (sdS - raw) + half * kChunkB + rr * 128;
+            const int qc = static_cast<int>(c0) + c;
+            uint8_t* drow = smem_raw + (sdS - raw) + (qc / 64) * kChunkB + rr * 128;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int v = c / 8 + u;
+              const int v = (qc % 64) / 8 + u;
               *reinterpret_cast<uint4*>(drow + ((v ^ (rr & 7)) << 4)) =
                   make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
             }
@@ -1298,33 +1322,32 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
       if (ok && itm.lo < itm.hi) ok = dq_readout();  // the piece's last block
       if (!ok) break;
-      // epilogue: this warp's columns [32 * half, 32 * half + 32) of dV and dK, for key row rr
+      // epilogue: this warp's columns [d0, d0 + kDcF) of dV and dK, for key row rr
       ok = wait_all(&hdr->acc_full, n_item & 1, 35);
       if (!ok) break;
       const int rr = quarter * 32 + lane;
-      float g2[2][32];
+      float g2[2][kDcF];
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
-        uint32_t a[32];
-        ptx::tmem_ld32(tmem + lane_sel + (part == 0 ? cdV : cdK) + 32 * half, a);
-        ptx::tmem_wait_ld32(a);
+        uint32_t a[kDcF];
+        ld_grad((part == 0 ? cdV : cdK) + d0, a);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) g2[part][k] = __uint_as_float(a[k]);
+        for (int k = 0; k < kDcF; ++k) g2[part][k] = __uint_as_float(a[k]);
       }
       ptx::tc_fence_before();
       // slot element (part, column, key row); a warp's 32 rows of one column are one 128-byte line
       auto slot_at = [&](uint32_t c, int part, int k) {
-        return part_ws + static_cast<size_t>(c) * kFusedSlotFloats + (part * 64 + 32 * half + k) * kT + rr;
+        return part_ws + static_cast<size_t>(c) * kFusedSlotFloats + (part * 64 + d0 + k) * kT + rr;
       };
       if (pc.kind == 2) {
         // later blocks of a split item: the raw sums go to this CTA's slot, then this warp's flag
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int k = 0; k < 32; ++k) *slot_at(blockIdx.x, part, k) = g2[part][k];
+          for (int k = 0; k < kDcF; ++k) *slot_at(blockIdx.x, part, k) = g2[part][k];
         __threadfence();  // every lane's slot writes, at gpu scope, before the flag
         __syncwarp();
-        if (lane == 0) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + warp, 1u);
+        if (lane == 0) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * kCwF + warp, 1u);
         continue;
       }
       if (pc.kind == 1) {
@@ -1335,7 +1358,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
              c2 < gridDim.x && FusedSched<CAUSAL>::start(c2, units) < end_u && ok; ++c2) {
           // a CTA with an empty range (more CTAs than units) writes no partial
           if (FusedSched<CAUSAL>::start(c2 + 1, units) == FusedSched<CAUSAL>::start(c2, units)) continue;
-          const uint32_t* f = flags + static_cast<size_t>(c2) * 8 + warp;
+          const uint32_t* f = flags + static_cast<size_t>(c2) * kCwF + warp;
           bool got = true;
           if (lane == 0) {
             const uint64_t t0 = ptx::globaltimer_ns();
@@ -1355,24 +1378,24 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int k = 0; k < 32; ++k) g2[part][k] += *slot_at(c2, part, k);
+            for (int k = 0; k < kDcF; ++k) g2[part][k] += *slot_at(c2, part, k);
         }
         if (!ok) break;
       }
       // dV and scale * dK in the I/O type, as the two 128 x 64 output tiles (128-byte swizzled
       // rows, the tensor maps' layout; rows past N are clipped by the maps), stored by TMA
       const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
-      uint32_t hv[16], hk[16];
+      uint32_t hv[kDcF / 2], hk[kDcF / 2];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < kDcF / 2; ++k) {
         hv[k] = none ? 0u : pack2<BF16>(g2[0][2 * k], g2[0][2 * k + 1]);
         hk[k] = none ? 0u : pack2<BF16>(g2[1][2 * k] * scale, g2[1][2 * k + 1] * scale);
       }
       ok = stage([&] {
         uint8_t* row = smem_raw + (sStg - raw) + rr * 128;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int v = 4 * half + u;  // this warp's 16-byte chunks of the row
+        for (int u = 0; u < kDcF / 8; ++u) {
+          const int v = d0 / 8 + u;  // this warp's 16-byte chunks of the row
           *reinterpret_cast<uint4*>(row + ((v ^ (rr & 7)) << 4)) =
               make_uint4(hv[4 * u], hv[4 * u + 1], hv[4 * u + 2], hv[4 * u + 3]);
           *reinterpret_cast<uint4*>(row + kChunkB + ((v ^ (rr & 7)) << 4)) =
@@ -1384,7 +1407,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
 
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == kWarpMmaO) {
+  if (warp == kWarpMmaF) {
     __syncwarp();
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
@@ -1679,7 +1702,7 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     float* zero = D == 64 ? dQacc : nullptr;
     bwd_delta_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
         static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, flags,
-        split ? ctx.num_sms * 8 : 0, rows);
+        split ? ctx.num_sms * kCwF : 0, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -1767,7 +1790,7 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
 }  // namespace
 
 size_t bwd_fused_split_bytes(int num_sms) {
-  return static_cast<size_t>(num_sms) * (kFusedSlotFloats * sizeof(float) + 8 * sizeof(uint32_t));
+  return static_cast<size_t>(num_sms) * (kFusedSlotFloats * sizeof(float) + kCwF * sizeof(uint32_t));
 }
 
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
