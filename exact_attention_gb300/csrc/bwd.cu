@@ -47,10 +47,11 @@ constexpr int kMinSmem = 120 * 1024;  // keeps one CTA per SM (each allocates al
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restrict__ O, const uint16_t* __restrict__ dO,
                                                         float* __restrict__ delta, float* __restrict__ acc_zero,
-                                                        uint32_t* __restrict__ flags_zero, int n_flags, long long rows) {
-  // the fused pass's ready flags (split schedule) start at zero
+                                                        uint32_t* __restrict__ counters_zero, int n_counters,
+                                                        long long rows) {
+  // the fused pass's counters (split schedule) start at zero
   if (blockIdx.x == 0)
-    for (int k = threadIdx.x; k < n_flags; k += blockDim.x) flags_zero[k] = 0u;
+    for (int k = threadIdx.x; k < n_counters; k += blockDim.x) counters_zero[k] = 0u;
   constexpr int kLPR = D * 2 / 16;          // lanes per row (16-byte vectors)
   constexpr int kRPW = 32 / kLPR;           // rows per warp pass
   const int lane = threadIdx.x & 31;
@@ -845,8 +846,9 @@ struct FusedSched {
   }
 };
 
-// Partial dK / dV of a split item, one slot per CTA: [dV, dK][64 columns][128 key rows] f32
-// (unscaled); plus one ready flag per compute warp, zeroed by the delta kernel of the call.
+// Partial dK / dV of a split item: two slots per CTA (a CTA's range can cut an item at each end),
+// each [dV, dK][64 columns][128 key rows] f32 (unscaled); then, per CTA, one counter per compute
+// warp for the items whose first block it holds, zeroed by the delta kernel of the call.
 constexpr int kFusedSlotFloats = 2 * 64 * kT;
 
 // dK, dV and dQ in one pass over (key tile, query block) with D = 64: the dK/dV kernel above
@@ -876,7 +878,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                        const float* __restrict__ LSE, const float* __restrict__ delta,
                        const __grid_constant__ CUtensorMap tmdK, const __grid_constant__ CUtensorMap tmdV,
                        const __grid_constant__ CUtensorMap tmQacc, int BH, int M, int N,
-                       float scale, float* __restrict__ part_ws, uint32_t* __restrict__ flags,
+                       float scale, float* __restrict__ part_ws, uint32_t* __restrict__ counters,
+                       uint16_t* __restrict__ dK, uint16_t* __restrict__ dV,
                        DevStatus* status, unsigned long long budget_ns) {
   constexpr int D = 64;
   using C = FusedCfg;
@@ -1145,7 +1148,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, i * kT, itm.bh);
             ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, i * kT, itm.bh);
           });
-        if (ok && pc.kind != 2)
+        if (ok && pc.kind == 0)
           ok = drain([&] {
             ptx::tma_store_3d(&tmdV, sStg, 0, itm.r0, itm.bh);
             ptx::tma_store_3d(&tmdK, sStg + kChunkB, 0, itm.r0, itm.bh);
@@ -1335,52 +1338,63 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         for (int k = 0; k < kDcF; ++k) g2[part][k] = __uint_as_float(a[k]);
       }
       ptx::tc_fence_before();
-      // slot element (part, column, key row); a warp's 32 rows of one column are one 128-byte line
-      auto slot_at = [&](uint32_t c, int part, int k) {
-        return part_ws + static_cast<size_t>(c) * kFusedSlotFloats + (part * 64 + d0 + k) * kT + rr;
-      };
-      if (pc.kind == 2) {
-        // later blocks of a split item: the raw sums go to this CTA's slot, then this warp's flag
+      if (pc.kind != 0) {
+        // A piece of a split item. Every CTA holding one adds it up the same way: it writes its
+        // raw sums into its slot for that piece and counts itself in on the item's counter (one
+        // per compute warp, kept by the CTA holding the item's first block); the warp that
+        // counts in last adds the others' slots to its own sums and writes that part of dV and
+        // dK. No CTA waits for another.
+        using S = FusedSched<CAUSAL>;
+        const uint32_t u0 = static_cast<uint32_t>(pc.w) * static_cast<uint32_t>(nqb);  // the item's units
+        const uint32_t u1 = u0 + static_cast<uint32_t>(nqb);
+        uint32_t ca = static_cast<uint32_t>(static_cast<uint64_t>(u0) * gridDim.x / units);  // holder of u0
+        while (ca + 1u < gridDim.x && S::start(ca + 1u, units) <= u0) ++ca;
+        while (ca > 0u && S::start(ca, units) > u0) --ca;
+        // CTA c's slot for this item: its second (last) one if its range starts before the item
+        auto slot_of = [&](uint32_t c) { return 2u * c + (S::start(c, units) < u0 ? 1u : 0u); };
+        // slot element (part, column, key row); a warp's 32 rows of one column are one 128-byte line
+        auto slot_at = [&](uint32_t sl, int part, int k) {
+          return part_ws + static_cast<size_t>(sl) * kFusedSlotFloats + (part * 64 + d0 + k) * kT + rr;
+        };
+        uint32_t holders = 0;
+        for (uint32_t c = ca; c < gridDim.x && S::start(c, units) < u1; ++c)
+          if (S::start(c + 1u, units) > S::start(c, units)) ++holders;
+        const uint32_t mine = slot_of(blockIdx.x);
 #pragma unroll
         for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int k = 0; k < kDcF; ++k) *slot_at(blockIdx.x, part, k) = g2[part][k];
-        __threadfence();  // every lane's slot writes, at gpu scope, before the flag
+          for (int k = 0; k < kDcF; ++k) __stcg(slot_at(mine, part, k), g2[part][k]);
+        __threadfence();  // every lane's slot writes, at gpu scope, before the count
         __syncwarp();
-        if (lane == 0) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * kCwF + warp, 1u);
-        continue;
-      }
-      if (pc.kind == 1) {
-        // first blocks of a split item: add the partials of the CTAs that took the rest (they
-        // reached those pieces first, so they are normally long published)
-        const uint32_t end_u = static_cast<uint32_t>(pc.w + 1) * static_cast<uint32_t>(nqb);
-        for (uint32_t c2 = blockIdx.x + 1;
-             c2 < gridDim.x && FusedSched<CAUSAL>::start(c2, units) < end_u && ok; ++c2) {
-          // a CTA with an empty range (more CTAs than units) writes no partial
-          if (FusedSched<CAUSAL>::start(c2 + 1, units) == FusedSched<CAUSAL>::start(c2, units)) continue;
-          const uint32_t* f = flags + static_cast<size_t>(c2) * kCwF + warp;
-          bool got = true;
-          if (lane == 0) {
-            const uint64_t t0 = ptx::globaltimer_ns();
-            got = false;
-            for (uint32_t k = 0; k < (1u << 30); ++k) {
-              if (ptx::ld_acquire_u32(f) == 1u) {
-                got = true;
-                break;
-              }
-              if ((k & 255u) == 255u && (*wc.abort_flag || ptx::globaltimer_ns() - t0 > wc.budget_ns)) break;
-            }
-            if (!got) ptx::raise_error(wc, kStatusTimeout, 39);
-          }
-          ok = __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
-          if (!ok) break;
-          (void)ptx::ld_acquire_u32(f);  // orders this lane's reads of the slot after the flag
+        uint32_t before = 0;
+        if (lane == 0) before = atomicAdd(counters + static_cast<size_t>(ca) * kCwF + warp, 1u);
+        before = __shfl_sync(0xFFFFFFFFu, before, 0);
+        if (before + 1u < holders) continue;  // a later holder finishes this part of the item
+        __threadfence();  // the other holders' slot writes, counted in before this warp, are visible
+        for (uint32_t c = ca; c < gridDim.x && S::start(c, units) < u1; ++c) {
+          if (c == blockIdx.x || S::start(c + 1u, units) == S::start(c, units)) continue;
+          const uint32_t sl = slot_of(c);
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
-            for (int k = 0; k < kDcF; ++k) g2[part][k] += *slot_at(c2, part, k);
+            for (int k = 0; k < kDcF; ++k) g2[part][k] += __ldcg(slot_at(sl, part, k));
         }
-        if (!ok) break;
+        // this thread's row of dV and scale * dK, columns [d0, d0 + kDcF)
+        const int key_row = itm.r0 + rr;
+        if (key_row < N) {
+          const size_t g = (static_cast<size_t>(itm.bh) * N + key_row) * D + d0;
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const float f = part == 0 ? 1.f : scale;
+            uint32_t h[kDcF / 2];
+#pragma unroll
+            for (int k = 0; k < kDcF / 2; ++k) h[k] = pack2<BF16>(g2[part][2 * k] * f, g2[part][2 * k + 1] * f);
+            uint4* d4 = reinterpret_cast<uint4*>((part == 0 ? dV : dK) + g);
+#pragma unroll
+            for (int v = 0; v < kDcF / 8; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+          }
+        }
+        continue;
       }
       // dV and scale * dK in the I/O type, as the two 128 x 64 output tiles (128-byte swizzled
       // rows, the tensor maps' layout; rows past N are clipped by the maps), stored by TMA
@@ -1687,8 +1701,8 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
                          int dtype, const BwdSplit& sp, const LaunchCtx& ctx) {
   using C = BwdCfg<D>;
   const bool split = D == 64 && !CAUSAL && dQacc != nullptr && sp.ws != nullptr;
-  uint32_t* flags =
-      split ? reinterpret_cast<uint32_t*>(sp.ws + static_cast<size_t>(ctx.num_sms) * kFusedSlotFloats) : nullptr;
+  uint32_t* counters =
+      split ? reinterpret_cast<uint32_t*>(sp.ws + static_cast<size_t>(ctx.num_sms) * 2 * kFusedSlotFloats) : nullptr;
   // delta = rowsum(dO o O)
   {
     const long long rows = static_cast<long long>(BH) * M;
@@ -1698,10 +1712,10 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     // the fused D = 64 pass accumulates dQ into dQacc, which this kernel zeroes on the way, and
-    // its split schedule's ready flags start at zero
+    // its split schedule's counters start at zero
     float* zero = D == 64 ? dQacc : nullptr;
     bwd_delta_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
-        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, flags,
+        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, counters,
         split ? ctx.num_sms * kCwF : 0, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1724,10 +1738,8 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       if (e != cudaSuccess) return e;
       // The later kernels are launched as programmatic dependents: each starts its set-up while
       // the kernel before it drains and waits (griddepcontrol.wait) before touching that
-      // kernel's results. Under the split schedule a CTA may wait for the partial of a later
-      // CTA; with one CTA per SM and nothing else on the device they are all resident once the
-      // delta kernel's blocks retire, and the wait is bounded in any case (a cooperative launch,
-      // which would guarantee residency, measured 6 us slower per call).
+      // kernel's results. No CTA waits for another (the split schedule's partials are added by
+      // whichever holder of a cut key tile finishes last), so none has to be resident at once.
       cudaLaunchAttribute pdl[1];
       pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       pdl[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1739,7 +1751,8 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       cfg.attrs = pdl;
       cfg.numAttrs = 1;
       e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, LSE, static_cast<const float*>(delta), mdk, mdv, macc, BH,
-                             M, N, scale, split ? sp.ws : static_cast<float*>(nullptr), flags, ctx.status,
+                             M, N, scale, split ? sp.ws : static_cast<float*>(nullptr), counters,
+                             static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), ctx.status,
                              ctx.wait_budget_ns);
       if (e != cudaSuccess) return e;
       const long long n4 = static_cast<long long>(n / 4);
@@ -1790,7 +1803,7 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
 }  // namespace
 
 size_t bwd_fused_split_bytes(int num_sms) {
-  return static_cast<size_t>(num_sms) * (kFusedSlotFloats * sizeof(float) + kCwF * sizeof(uint32_t));
+  return static_cast<size_t>(num_sms) * (2 * kFusedSlotFloats * sizeof(float) + kCwF * sizeof(uint32_t));
 }
 
 cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,

@@ -71,7 +71,7 @@ cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O,
                            int D, float scale, bool causal, int parts, float* ws, const LaunchCtx& ctx);
 
 // Split schedule of the fused backward (non-causal, D = 64): ws holds bwd_fused_split_bytes of
-// partial dK/dV slots then num_sms * 8 ready flags; ws == nullptr runs whole key tiles.
+// partial dK/dV slots (two per SM) then num_sms * 8 counters; ws == nullptr runs whole key tiles.
 struct BwdSplit {
   float* ws;
 };

@@ -180,21 +180,20 @@ size_t fa_bwd_workspace_bytes(int B, int H, int M);
  *                    fa_bwd_ws_workspace_bytes(B,H,M,D) bytes: delta
  *                    (B*H*M float32, rowsum(dO o O) on return), then for
  *                    D = 64 the accumulator (B*H*M*64 float32, 256-byte
- *                    aligned), then per SM of the current device one slot
- *                    of partial dK/dV (2*64*128 float32) and, after all
- *                    slots, 8 ready flags (uint32) per SM. The call writes
+ *                    aligned), then per SM of the current device two slots
+ *                    of partial dK/dV (2*64*128 float32 each) and, after all
+ *                    slots, 8 counters (uint32) per SM. The call writes
  *                    every part it reads (no zero-fill needed); caller-owned,
  *                    one call at a time.
  *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
  * Non-causal calls with D = 64 whose key tiles (B*H*ceil(N/128)) would
  * leave the last round of SMs under 90 % busy run a split schedule: every SM
- * takes an equal share of the (key tile, query block) pairs, and a key tile
- * cut between two SMs has the partial dK/dV of the later one added in by the
- * earlier one (one CTA per SM; an SM that waits longer than the wait budget for
- * a partial, which takes another job holding SMs for that long, ends the call
- * with FA_ERR_TIMEOUT).
+ * takes an equal share of the (key tile, query block) pairs, and each SM
+ * holding part of a cut key tile writes its partial dK/dV; whichever finishes
+ * last adds the others' and writes the tile (no SM waits for another).
  * The summation order of dQ's key blocks follows the SMs' timing, so dQ can
- * differ between runs in the last bits of the f32 accumulator (dK, dV do not).
+ * differ between runs in the last bits of the f32 accumulator, and so can dK
+ * and dV of a key tile the split schedule cuts (otherwise they do not).
  */
 fa_status fa_bwd_ws(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                     void* dQ, void* dK, void* dV, void* workspace, size_t workspace_bytes, int B, int H, int M,
