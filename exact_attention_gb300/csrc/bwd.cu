@@ -1368,6 +1368,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         __syncwarp();
         uint32_t before = 0;
         if (lane == 0) before = atomicAdd(counters + static_cast<size_t>(ca) * kCwF + warp, 1u);
+        __syncwarp();  // the other lanes' reads below follow lane 0's count
         before = __shfl_sync(0xFFFFFFFFu, before, 0);
         if (before + 1u < holders) continue;  // a later holder finishes this part of the item
         __threadfence();  // the other holders' slot writes, counted in before this warp, are visible

@@ -299,10 +299,16 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
     }
   }
   cudaError_t e;
-  if (dtype == FA_F32)
-    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, parts, static_cast<float*>(ws), ctx);
-  else
+  if (dtype == FA_F32) {
+    uint32_t ep = 0;
+    if (parts > 1) {
+      ep = ++g_epoch;
+      if (ep == 0u) ep = ++g_epoch;  // 0 is what a fresh workspace holds
+    }
+    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, parts, static_cast<float*>(ws), ep, ctx);
+  } else {
     e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
+  }
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
   if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "%s: TMA descriptor rejected by the driver", name);
   if (e != cudaSuccess) return cuda_fail(e, name);

@@ -64,11 +64,14 @@ cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O
                             int D, float scale, bool causal, int dtype, const FwdSplit& sp, const LaunchCtx& ctx);
 
 // f32 forward; with few query tiles (under half the SMs) each tile's key blocks are shared by
-// `parts` CTAs whose partials a second launch merges (ws: fwd_f32_split_bytes floats' worth).
+// `parts` CTAs, and the one that finishes last merges the others' partials (ws:
+// fwd_f32_split_bytes bytes of partial slots and per-tile counters; epoch: nonzero, new per
+// launch, so counts an earlier launch left behind read as zero).
 int fwd_f32_parts(int BH, int M, int N, int num_sms);
 size_t fwd_f32_split_bytes(int BH, int M, int parts);
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                           int D, float scale, bool causal, int parts, float* ws, const LaunchCtx& ctx);
+                           int D, float scale, bool causal, int parts, float* ws, uint32_t epoch,
+                           const LaunchCtx& ctx);
 
 // Split schedule of the fused backward (non-causal, D = 64): ws holds bwd_fused_split_bytes of
 // partial dK/dV slots (two per SM) then num_sms * 8 counters; ws == nullptr runs whole key tiles.

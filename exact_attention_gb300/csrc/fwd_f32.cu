@@ -104,7 +104,8 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads32, 1)
     fwd_f32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, float* __restrict__ O, float* __restrict__ LSE, int BH,
-                   int M, int N, float scale_log2, int parts, float* __restrict__ ws, DevStatus* status,
+                   int M, int N, float scale_log2, int parts, float* __restrict__ ws,
+                   unsigned long long* __restrict__ counters, uint32_t epoch, DevStatus* status,
                    unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
   F32Hdr* hdr = reinterpret_cast<F32Hdr*>(smem_raw);
@@ -124,8 +125,10 @@ __global__ void __launch_bounds__(kThreads32, 1)
   const int tiles = BH * nqt;
 
   // Unit w = (tile w / parts, part w % parts): the tile's key blocks [jb, jb + nb) of its part.
-  // With parts > 1 each part leaves an unnormalised partial that fwd_f32_combine merges;
-  // empty parts (causal tiles with fewer blocks than parts) are skipped by every role.
+  // With parts > 1 each part leaves an unnormalised partial and counts itself in on its tile;
+  // the part that counts in last merges the others into its own and writes O and LSE (no CTA
+  // waits for another). Empty parts (causal tiles with fewer blocks than parts) are skipped by
+  // every role.
   const int units = tiles * parts;
   auto tile_of = [&](int w, int& bh, int& q0, int& jb, int& nb) {
     const int tile = w / parts, part = w - tile * parts;
@@ -373,14 +376,62 @@ __global__ void __launch_bounds__(kThreads32, 1)
       if (parts > 1) {
         // unnormalised partial of this part, column-major (a warp's 32 rows of a column are
         // one contiguous line): O [64][128], m [128], l [128]
-        float* slot = ws + static_cast<size_t>(w) * kF32Slot;
+        const int tile = w / parts, part = w - tile * parts;
+        const int nbt = CAUSAL ? min(nkb, (q0 + kBM32 - 1) / kBN32 + 1) : nkb;
+        auto nonempty = [&](int p) { return (p + 1) * nbt / parts > p * nbt / parts; };
+        auto slot_of = [&](int p) { return ws + (static_cast<size_t>(tile) * parts + p) * kF32Slot; };
         const int r = warp * 32 + lane;
+        float* slot = slot_of(part);
 #pragma unroll
-        for (int c = 0; c < kD32; ++c) slot[c * kBM32 + r] = oacc[c];
-        slot[kD32 * kBM32 + r] = m2;
-        slot[kD32 * kBM32 + kBM32 + r] = l;
+        for (int c = 0; c < kD32; ++c) __stcg(slot + c * kBM32 + r, oacc[c]);
+        __stcg(slot + kD32 * kBM32 + r, m2);
+        __stcg(slot + kD32 * kBM32 + kBM32 + r, l);
         ptx::tc_fence_before();
-        continue;
+        __threadfence();  // every lane's partial, at gpu scope, before the count
+        __syncwarp();
+        int holders = 0;
+        for (int p = 0; p < parts; ++p) holders += nonempty(p) ? 1 : 0;
+        // count in on (tile, warp): the 64-bit word holds (epoch << 32) | count, so whatever an
+        // earlier launch left there (another epoch) reads as a count of zero
+        uint32_t count = 0;
+        if (lane == 0) {
+          unsigned long long* cw = counters + static_cast<size_t>(tile) * 4 + warp;
+          const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
+          unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cw);
+          for (uint32_t it = 0; it < (1u << 20); ++it) {
+            const unsigned long long nv = (cur >> 32) == epoch ? cur + 1ull : (tag | 1ull);
+            const unsigned long long seen = atomicCAS(cw, cur, nv);
+            if (seen == cur) {
+              count = static_cast<uint32_t>(nv);
+              break;
+            }
+            cur = seen;
+          }
+          if (count == 0u) ptx::raise_error(wc, kStatusTimeout, 39);
+        }
+        __syncwarp();  // the other lanes' reads below follow lane 0's count
+        count = __shfl_sync(0xFFFFFFFFu, count, 0);
+        if (count == 0u) break;
+        if (static_cast<int>(count) < holders) continue;  // a later part finishes the tile
+        __threadfence();  // the other parts' partials, counted in before this one, are visible
+        // merge: m = max_s m_s, weights 2^(m_s - m) (the online-softmax rescaling)
+        float mm = m2;
+        for (int p = 0; p < parts; ++p)
+          if (p != part && nonempty(p)) mm = fmaxf(mm, __ldcg(slot_of(p) + kD32 * kBM32 + r));
+        const float a = m2 == -INFINITY ? 0.f : ptx::ex2(m2 - mm);
+        l *= a;
+#pragma unroll
+        for (int c = 0; c < kD32; ++c) oacc[c] *= a;
+        for (int p = 0; p < parts; ++p) {
+          if (p == part || !nonempty(p)) continue;
+          const float* sp = slot_of(p);
+          const float mp = __ldcg(sp + kD32 * kBM32 + r);
+          const float b = mp == -INFINITY ? 0.f : ptx::ex2(mp - mm);
+          l = fmaf(b, __ldcg(sp + kD32 * kBM32 + kBM32 + r), l);
+#pragma unroll
+          for (int c = 0; c < kD32; ++c) oacc[c] = fmaf(b, __ldcg(sp + c * kBM32 + r), oacc[c]);
+        }
+        m2 = mm;
       }
       const float inv = 1.f / l;
       const bool valid = row < M;
@@ -405,61 +456,20 @@ __global__ void __launch_bounds__(kThreads32, 1)
   }
 }
 
-// Merges the parts of each row: m = max_s m_s, w_s = 2^(m_s - m), O = sum_s w_s O_s / sum_s w_s l_s
-// (the online-softmax rescaling between key blocks), LSE = m + log sum_s w_s l_s. Empty parts
-// (no key blocks) wrote nothing and are skipped. One thread per (row, 4 columns).
-template <bool CAUSAL>
-__global__ void __launch_bounds__(256)
-    fwd_f32_combine(const float* __restrict__ ws, float* __restrict__ O, float* __restrict__ LSE, int BH, int M,
-                    int N, int parts) {
-  const long long gid = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);  // global row
-  const int c4 = threadIdx.x & 15;
-  if (gid >= static_cast<long long>(BH) * M) return;
-  const int bh = static_cast<int>(gid / M), row = static_cast<int>(gid - static_cast<long long>(bh) * M);
-  const int nqt = (M + kBM32 - 1) / kBM32, nkb = (N + kBN32 - 1) / kBN32;
-  const int qt = row / kBM32, r = row - qt * kBM32;
-  const int qt_rev = CAUSAL ? nqt - 1 - qt : qt;
-  const int tile = qt_rev * BH + bh;
-  const int nbt = CAUSAL ? min(nkb, (qt * kBM32 + kBM32 - 1) / kBN32 + 1) : nkb;
-  float m = -INFINITY;
-  for (int p = 0; p < parts; ++p) {
-    if ((p + 1) * nbt / parts == p * nbt / parts) continue;
-    const float* slot = ws + (static_cast<size_t>(tile) * parts + p) * kF32Slot;
-    m = fmaxf(m, slot[kD32 * kBM32 + r]);
-  }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lsum = 0.f;
-  for (int p = 0; p < parts; ++p) {
-    if ((p + 1) * nbt / parts == p * nbt / parts) continue;
-    const float* slot = ws + (static_cast<size_t>(tile) * parts + p) * kF32Slot;
-    const float wgt = ptx::ex2(slot[kD32 * kBM32 + r] - m);
-    lsum = fmaf(wgt, slot[kD32 * kBM32 + kBM32 + r], lsum);
-    acc.x = fmaf(wgt, slot[(4 * c4 + 0) * kBM32 + r], acc.x);
-    acc.y = fmaf(wgt, slot[(4 * c4 + 1) * kBM32 + r], acc.y);
-    acc.z = fmaf(wgt, slot[(4 * c4 + 2) * kBM32 + r], acc.z);
-    acc.w = fmaf(wgt, slot[(4 * c4 + 3) * kBM32 + r], acc.w);
-  }
-  const float inv = 1.f / lsum;
-  reinterpret_cast<float4*>(O + static_cast<size_t>(gid) * kD32)[c4] =
-      make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-  if (c4 == 0 && LSE != nullptr) LSE[gid] = (m + __log2f(lsum)) * kLn2_32;
-}
-
 template <bool CAUSAL>
 cudaError_t launch32(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, void* O, float* LSE, int BH,
-                     int M, int N, float scale, int parts, float* ws, const LaunchCtx& ctx) {
+                     int M, int N, float scale, int parts, float* ws, uint32_t epoch, const LaunchCtx& ctx) {
   auto kern = fwd_f32_kernel<CAUSAL>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem32);
   if (e != cudaSuccess) return e;
   const long long units = static_cast<long long>((M + kBM32 - 1) / kBM32) * BH * parts;
   const int grid = static_cast<int>(units < ctx.num_sms ? units : ctx.num_sms);
+  // the tiles' counters follow the partial slots
+  unsigned long long* counters =
+      parts > 1 ? reinterpret_cast<unsigned long long*>(ws + static_cast<size_t>(units) * kF32Slot) : nullptr;
   kern<<<grid, kThreads32, kSmem32, ctx.stream>>>(mq, mk, mv, static_cast<float*>(O), LSE, BH, M, N,
-                                                  scale * kLog2e32, parts, ws, ctx.status, ctx.wait_budget_ns);
-  e = cudaGetLastError();
-  if (e != cudaSuccess || parts == 1) return e;
-  const long long rows = static_cast<long long>(BH) * M;
-  fwd_f32_combine<CAUSAL><<<static_cast<unsigned>((rows + 15) / 16), 256, 0, ctx.stream>>>(
-      ws, static_cast<float*>(O), LSE, BH, M, N, parts);
+                                                  scale * kLog2e32, parts, ws, counters, epoch, ctx.status,
+                                                  ctx.wait_budget_ns);
   return cudaGetLastError();
 }
 
@@ -476,19 +486,21 @@ int fwd_f32_parts(int BH, int M, int N, int num_sms) {
 
 size_t fwd_f32_split_bytes(int BH, int M, int parts) {
   if (parts <= 1) return 0;
-  return static_cast<size_t>((M + kBM32 - 1) / kBM32) * BH * parts * kF32Slot * sizeof(float);
+  const size_t tiles = static_cast<size_t>((M + kBM32 - 1) / kBM32) * BH;
+  return tiles * parts * kF32Slot * sizeof(float) + tiles * 4 * sizeof(unsigned long long);  // slots, counters
 }
 
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
-                           int D, float scale, bool causal, int parts, float* ws, const LaunchCtx& ctx) {
+                           int D, float scale, bool causal, int parts, float* ws, uint32_t epoch,
+                           const LaunchCtx& ctx) {
   if (D != kD32) return cudaErrorNotSupported;
   if (parts < 1 || (parts > 1 && ws == nullptr)) parts = 1;
   CUtensorMap mq, mk, mv;
   if (!make_tmap_3d(&mq, Q, kF32, D, M, BH, 32, kBM32) || !make_tmap_3d(&mk, K, kF32, D, N, BH, 32, kBN32) ||
       !make_tmap_3d(&mv, V, kF32, D, N, BH, 32, kBN32))
     return cudaErrorInvalidValue;
-  return causal ? launch32<true>(mq, mk, mv, O, LSE, BH, M, N, scale, parts, ws, ctx)
-                : launch32<false>(mq, mk, mv, O, LSE, BH, M, N, scale, parts, ws, ctx);
+  return causal ? launch32<true>(mq, mk, mv, O, LSE, BH, M, N, scale, parts, ws, epoch, ctx)
+                : launch32<false>(mq, mk, mv, O, LSE, BH, M, N, scale, parts, ws, epoch, ctx);
 }
 
 }  // namespace fa

@@ -240,3 +240,15 @@ def test_forward_host_buffers_without_lse_and_checks():
     assert fa.fa_fwd_host(hq, None, hv, ho, None, ws, nbytes, B, H, M, N, D, 0.125, 0, fa.FA_F16) == fa.FA_ERR_INVALID
     assert fa.fa_fwd_host(hq, hk, hv, ho, None, ws, nbytes, B, H, M, N, 96, 0.125, 0, fa.FA_F16) == \
         fa.FA_ERR_UNSUPPORTED
+
+
+def test_forward_f32_and_half_splits_share_the_workspace(monkeypatch):
+    """The cached forward workspace serves, in turn, the f32 key-range split (partial slots and
+    epoch-tagged counters, merged by the part that finishes last) and the half-precision split
+    schedule (partials and epoch flags); neither is misled by what the other left there, and a
+    repeated f32 call is not misled by its own earlier counts."""
+    monkeypatch.setenv("FA_FWD_SPLIT", "1")
+    for seed in (1, 2):
+        for dtype in ("f32", "f16", "f32"):
+            inputs, out, lse = run_fwd(1, 2, 512, 768, 64, dtype, seed == 2, 0.125, seed=seed)
+            check_heads(inputs, out, lse, dtype, seed == 2, 0.125, rel_l2=REL_L2_F32 if dtype == "f32" else None)
