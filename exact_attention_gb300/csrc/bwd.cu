@@ -855,10 +855,10 @@ constexpr int kFusedSlotFloats = 2 * 64 * kT;
 // with dS^T in shared memory instead of tensor memory. There one buffer serves as the K-major A
 // operand of dK += dS^T Q and, read MN-major, as the A operand of dQ_i = dS K (the tutorial's
 // dQ kernel recomputes S and dP for that product; here it reuses them). dQ_i lands in the tensor
-// memory dS^T had, the compute warps stage it in shared memory as f32 and one thread adds it into
-// an f32 dQ accumulator in global memory with a bulk reduce (cp.reduce.async.bulk .add.f32; a
-// query block's 128 rows of 64 floats are contiguous there). A later kernel scales and converts
-// the accumulator. TMEM: S^T [0,128), dP^T [128,256), P^T packed [256,320), dQ_i [320,384),
+// memory dS^T had, the compute warps stage it in shared memory as f32 and the drain warp adds it
+// into an f32 dQ accumulator in global memory with a bulk tensor reduce (.add; a query block's
+// 128 rows of 64 floats are contiguous there). A later kernel scales and converts the
+// accumulator. TMEM: S^T [0,128), dP^T [128,256), P^T packed [256,320), dQ_i [320,384),
 // dV [384,448), dK [448,512).
 // Warps: kCwF compute warps (kCwF / 4 per TMEM lane quarter: each thread takes kQcF of its key
 // row's 128 query columns and kDcF of its 64 gradient columns), then the producer, the MMA

@@ -71,7 +71,8 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, float* LS
  * 256x64 f32 block and three 256-float statistics) plus eight 32-bit flags per
  * SM. f32 with D = 64 when its 128-row query tiles fill fewer than half the SMs:
  * one 128x64 f32 block plus two 128-float statistics per (tile, part), where the
- * key blocks of a tile are shared by `parts` SMs. Otherwise, or on bad sizes, 0.
+ * key blocks of a tile are shared by `parts` SMs, then four 64-bit counters per
+ * tile. Otherwise, or on bad sizes, 0.
  */
 size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_dtype dtype);
 
@@ -97,8 +98,10 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  * The split is used when the call is not causal, every SM gets at least four key
  * blocks and the last wave would be less than 90 % full (causal pairs, whose key
  * ranges differ in length, are dealt whole in a serpentine order, which measured
- * faster); FA_FWD_SPLIT=0 or 1 in the environment turns it off or on regardless. For f32 (few query tiles) the parts of a tile write
- * unnormalised partials that a second launch on `stream` merges the same way.
+ * faster); FA_FWD_SPLIT=0 or 1 in the environment turns it off or on regardless.
+ * For f32 with few query tiles, several CTAs share each tile's keys: each writes
+ * an unnormalised partial and counts itself in on the tile, and the one that
+ * counts in last merges the partials the same way and writes O and LSE.
  */
 fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE, void* workspace,
                     size_t workspace_bytes, int B, int H, int M, int N, int D, float scale, int causal, fa_dtype dtype,
