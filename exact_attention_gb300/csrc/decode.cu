@@ -306,10 +306,15 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
         if (kk < nk) {
           float kf[C::kEPL];
           Elem<DT>::unpack(*reinterpret_cast<const uint4*>(sk + kk * C::kRow + sl * 16), kf);
+          // pairs of elements on the f32x2 FMA (half the instructions: this path is issue-bound)
 #pragma unroll
-          for (int r = 0; r < R; ++r)
+          for (int r = 0; r < R; ++r) {
+            float2 p2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < C::kEPL; ++e) part[r] = fmaf(qv[r][e], kf[e], part[r]);
+            for (int e = 0; e < C::kEPL; e += 2)
+              p2 = ptx::ffma2(make_float2(qv[r][e], qv[r][e + 1]), make_float2(kf[e], kf[e + 1]), p2);
+            part[r] = p2.x + p2.y;
+          }
         }
         float c;
         if constexpr (R == 2) {
@@ -346,7 +351,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
       for (int r = 0; r < R; ++r) {
         const float cr = __shfl_sync(0xFFFFFFFFu, corr, group0 + row_lane(r));
 #pragma unroll
-        for (int e = 0; e < C::kEPL; ++e) acc[r][e] *= cr;
+        for (int e = 0; e < C::kEPL; e += 2) {
+          const float2 a = ptx::fmul2(make_float2(acc[r][e], acc[r][e + 1]), make_float2(cr, cr));
+          acc[r][e] = a.x;
+          acc[r][e + 1] = a.y;
+        }
       }
 #pragma unroll
       for (int g = 0; g < C::kG; ++g) {
@@ -360,7 +369,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
 #pragma unroll
           for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int e = 0; e < C::kEPL; ++e) acc[r][e] = fmaf(pr[r], vf[e], acc[r][e]);
+            for (int e = 0; e < C::kEPL; e += 2) {
+              const float2 a = ptx::ffma2(make_float2(pr[r], pr[r]), make_float2(vf[e], vf[e + 1]),
+                                          make_float2(acc[r][e], acc[r][e + 1]));
+              acc[r][e] = a.x;
+              acc[r][e + 1] = a.y;
+            }
         }
       }
     }
