@@ -306,7 +306,12 @@ __global__ void __launch_bounds__(kThreads32, 1)
           ptx::tmem_ld32(tO + c, t);
           ptx::tmem_wait_ld32(t);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) oacc[c + i] += __uint_as_float(t[i]);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 a = ptx::fadd2(make_float2(oacc[c + i], oacc[c + i + 1]),
+                                        make_float2(__uint_as_float(t[i]), __uint_as_float(t[i + 1])));
+            oacc[c + i] = a.x;
+            oacc[c + i + 1] = a.y;
+          }
         }
       };
       for (int j = 0; j < nb; ++j) {
@@ -329,39 +334,61 @@ __global__ void __launch_bounds__(kThreads32, 1)
             }
           }
         };
-        float mx = -INFINITY;
+        // the block maximum in four independent chains of three-input max
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < kBN32; c += 32) {
           uint32_t r[32];
           load_s(c, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(r[i]));
+          for (int i = 0; i < 32; i += 8) {
+            mx0 = ptx::fmax3(mx0, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+            mx1 = ptx::fmax3(mx1, __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+            mx2 = ptx::fmax3(mx2, __uint_as_float(r[i + 4]), __uint_as_float(r[i + 5]));
+            mx3 = ptx::fmax3(mx3, __uint_as_float(r[i + 6]), __uint_as_float(r[i + 7]));
+          }
         }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
         const float m_new = fmaxf(m2, mx * scale_log2);
         const float m_safe = m_new == -INFINITY ? 0.f : m_new;
         const float corr = ptx::ex2(m2 - m_safe);  // m2 = -inf on the first block: corr = 0
         if (j > 0 && corr != 1.f) {
 #pragma unroll
-          for (int i = 0; i < kD32; ++i) oacc[i] *= corr;
+          for (int i = 0; i < kD32; i += 2) {
+            const float2 a = ptx::fmul2(make_float2(oacc[i], oacc[i + 1]), make_float2(corr, corr));
+            oacc[i] = a.x;
+            oacc[i + 1] = a.y;
+          }
         }
         m2 = m_new;
-        float sum = 0.f;
+        // P = 2^(s c - m) by pairs on the f32x2 pipe, its sum in two independent chains, and its
+        // split into the tf32 hi part and the remainder
+        const float2 c2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_safe, -m_safe);
+        float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kBN32; c += 32) {
           uint32_t r[32], plo[32];
           load_s(c, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const float p = ptx::ex2(fmaf(__uint_as_float(r[i]), scale_log2, -m_safe));
-            sum += p;
-            const float h = tf32_hi(p);
-            r[i] = __float_as_uint(h);
-            plo[i] = __float_as_uint(p - h);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), c2, nm2);
+            const float2 p = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
+            if (i & 2)
+              sum_b = ptx::fadd2(sum_b, p);
+            else
+              sum_a = ptx::fadd2(sum_a, p);
+            const float2 h = make_float2(tf32_hi(p.x), tf32_hi(p.y));
+            const float2 lo = ptx::fsub2(p, h);
+            r[i] = __float_as_uint(h.x);
+            r[i + 1] = __float_as_uint(h.y);
+            plo[i] = __float_as_uint(lo.x);
+            plo[i + 1] = __float_as_uint(lo.y);
           }
           ptx::tmem_st32(tS + c, r);
           ptx::tmem_st32(tPl + c, plo);
         }
-        l = fmaf(l, corr, sum);
+        const float2 sum2 = ptx::fadd2(sum_a, sum_b);
+        l = fmaf(l, corr, sum2.x + sum2.y);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
