@@ -797,14 +797,12 @@ __global__ void __launch_bounds__(kThreadsO, 1)
 //  * Classic: whole items, one per round (item_of_round).
 //  * Split (non-causal): the contiguous range [c U / G, (c+1) U / G) of the U = items x nqb
 //    (item, query block) units, so every CTA streams the same number of blocks and no part-full
-//    last round is left. An item cut by a range boundary is finished by the CTA holding its
-//    first block, which reaches that piece last (a range ends with it) and adds in the partial
-//    dK / dV of the CTAs holding the rest; those reach theirs first (a range starts with it) and
-//    publish it in the workspace.
+//    last round is left. The pieces of an item cut by range boundaries each leave a partial
+//    dK / dV; whichever CTA finishes its piece last adds the others in (see the epilogue).
 struct FusedPiece {
   BwdItem it;
   int w;     // item index
-  int kind;  // 0: the whole item; 1: its first blocks, finished here; 2: later blocks, a partial
+  int kind;  // 0: the whole item; 1: its first blocks; 2: later blocks (1 and 2: a cut item)
 };
 template <bool CAUSAL>
 struct FusedSched {
