@@ -592,7 +592,8 @@ PROFILE_CASES = {
     # inputs larger than L2 (129 MB) so DRAM counters mean something, a few GB at most
     "fwd": dict(B=16, H=16, M=4096, N=4096, D=64, dtype="f16"),     # Q/K/V 0.4 GB
     "decode": dict(B=8, H=8, N=32768, D=128, n_splits=64, dtype="bf16"),  # K/V 1.07 GB
-    "bwd": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # Q/K/V/O/dO 0.34 GB
+    "bwd": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # Q/K/V/O/dO 0.34 GB (fused pass)
+    "bwd3": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # the same through the three kernels
     "decode_rows": dict(B=8, H=8, N=32768, D=128, n_splits=64, rows=4, dtype="bf16"),  # K/V 1.07 GB
 }
 
@@ -616,12 +617,12 @@ def run_profile(kind: str, launches: int = 5):
         lse = torch.empty(shp[:3], device="cuda")
         for _ in range(launches):
             fa.forward(q, k, v, 0.125, False, out=o, lse=lse)
-    elif kind == "bwd":
+    elif kind in ("bwd", "bwd3"):
         shp = (c["B"], c["H"], c["M"], c["D"])
         q, k, v, do = (torch.randn(shp, generator=g, device="cuda").half() for _ in range(4))
         o, lse = fa.forward(q, k, v, 0.125, False)
         for _ in range(launches):
-            fa.backward(q, k, v, o, do, lse, 0.125, False)
+            fa.backward(q, k, v, o, do, lse, 0.125, False, fused=kind == "bwd")
     else:
         q = torch.randn((c["B"], c["H"], c.get("rows", 1), c["D"]), generator=g, device="cuda").bfloat16()
         kc = torch.randn((c["B"], c["H"], c["N"], c["D"]), generator=g, device="cuda").bfloat16()
