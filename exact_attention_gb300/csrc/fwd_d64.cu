@@ -244,6 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
+    // whole pairs (the schedule of small problems, where the start weighs most): the first
+    // pair's Q tiles and first key blocks start towards L2 while the CTA sets up
+    Schedule<CAUSAL> first(split, BH, num_pairs, nkb);
+    Piece p0;
+    if (!split && first.next(p0, split, BH, num_pairs, nkb)) {
+      for (int t = 0; t < 2; ++t) ptx::tma_prefetch_l2_3d(&tmQ, 0, p0.q0 + t * kBM, p0.bh);
+      const int nb = p0.nb1 < kStages ? p0.nb1 : kStages;
+      for (int j = 0; j < nb; ++j) {
+        ptx::tma_prefetch_l2_3d(&tmK, 0, (p0.jb + j) * kBN, p0.bh);
+        ptx::tma_prefetch_l2_3d(&tmV, 0, (p0.jb + j) * kBN, p0.bh);
+      }
+    }
   }
   if (warp == kWarpEpi && lane == 0) ptx::prefetch_tmap(&tmO);
   ptx::tc_fence_before();
