@@ -3,15 +3,19 @@
 A step is one pass of the hot path over synthetic inputs already resident in
 device memory:
   * forward, fp16, B=4, H=12, M=N=2048, D=64, scale 0.125, non-causal
-    (the workload the headline TFLOP/s is quoted on); L2 is flushed before it;
+    (the workload the headline TFLOP/s is quoted on);
   * backward at the same shape, when the library provides it;
   * flash decoding, bf16, B=8, H=32, N=32768, D=128, n_splits=64 (the K/V cache,
     4.29 GB, is far larger than L2).
-Each part is timed with CUDA events on the stream it runs on. `value` is the
-forward's TFLOP/s (4*B*H*M*N*D per call); the decode GB/s (K+V bytes read per
-call) is reported in the `decode` object. `e2e` repeats the forward through the
-C ABI on pinned host buffers (fa_fwd_host: the inputs copied in and O/LSE copied
-back inside the timed region, overlapped with the kernels chunk by chunk).
+Step i runs the forward and the backward on input set i % 4 of four seeded sets
+(4 x 63 MB, larger than L2, so every call reads its inputs from HBM). The K
+calls of each part run back to back on one stream between one pair of CUDA
+events. `value` is the forward's TFLOP/s (4*B*H*M*N*D per call); the decode
+GB/s (K+V bytes read per call) is reported in the `decode` object. `configs`
+times every configuration of the workload list on its own (one call between
+two events, L2 flushed before it). `e2e` repeats the forward through the C ABI
+on pinned host buffers (fa_fwd_host: the inputs copied in and O/LSE copied back
+inside the timed region, overlapped with the kernels chunk by chunk).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -38,6 +42,7 @@ METRIC = "attn fwd TFLOP/s & % tensor peak (B4 H12 N2048 D64); decode KV GB/s & 
 FWD = dict(B=4, H=12, M=2048, N=2048, D=64, scale=0.125, causal=False, dtype="f16")
 DEC = dict(B=8, H=32, N=32768, D=128, n_splits=64, dtype="bf16")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
+ROTATE = 4  # input sets of the forward/backward workload used in turn: 4 x 63 MB > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -230,12 +235,18 @@ def run_ours(args):
         return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
     c = FWD
-    q, k, v, do = synth.attention_inputs(c["B"], c["H"], c["M"], c["N"], c["D"], c["dtype"], seed=rank,
-                                         with_dout=True)
-    qd, kd, vd, dod = dev(q, "f16"), dev(k, "f16"), dev(v, "f16"), dev(do, "f16")
-    od = torch.empty_like(qd)
-    lse = torch.empty((c["B"], c["H"], c["M"]), dtype=torch.float32, device="cuda")
-    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    # ROTATE input sets of the forward/backward workload, used in turn by consecutive steps: together
+    # they are larger than L2 (129 MB), so every call reads its inputs from HBM
+    sets = []
+    for r in range(ROTATE):
+        q, k, v, do = synth.attention_inputs(c["B"], c["H"], c["M"], c["N"], c["D"], c["dtype"],
+                                             seed=rank * ROTATE + r, with_dout=True)
+        qd, kd, vd, dod = dev(q, "f16"), dev(k, "f16"), dev(v, "f16"), dev(do, "f16")
+        sets.append(dict(q=qd, k=kd, v=vd, do=dod, o=torch.empty_like(qd),
+                         lse=torch.empty((c["B"], c["H"], c["M"]), dtype=torch.float32, device="cuda"),
+                         dq=torch.empty_like(qd), dk=torch.empty_like(kd), dv=torch.empty_like(vd)))
+    qd, kd, vd, dod = (sets[0][n] for n in ("q", "k", "v", "do"))
+    od, lse = sets[0]["o"], sets[0]["lse"]
     # backward workspace: delta, then the f32 dQ accumulator of the fused dK/dV/dQ pass (fa_bwd_ws)
     bws_bytes = fa.fa_bwd_ws_workspace_bytes(c["B"], c["H"], c["M"], c["D"])
     bws = torch.empty(bws_bytes, dtype=torch.uint8, device="cuda")
@@ -260,18 +271,20 @@ def run_ours(args):
         if s != fa.FA_OK:
             raise RuntimeError(f"{what}: {fa.fa_status_string(s)}: {fa.fa_last_error_message()}")
 
-    def run_fwd():
-        check(fa.fa_fwd_ws(qd, kd, vd, od, lse, fws if fws_bytes else None, fws_bytes, *BHMND, c["scale"], c["causal"],
-                           fa.FA_F16, stream), "fa_fwd_ws")
+    def run_fwd(i=0):
+        t = sets[i % ROTATE]
+        check(fa.fa_fwd_ws(t["q"], t["k"], t["v"], t["o"], t["lse"], fws if fws_bytes else None, fws_bytes, *BHMND,
+                           c["scale"], c["causal"], fa.FA_F16, stream), "fa_fwd_ws")
 
     have_bwd = True
 
-    def run_bwd():
+    def run_bwd(i=0):
         nonlocal have_bwd
         if not have_bwd:
             return
-        s = fa.fa_bwd_ws(qd, kd, vd, od, dod, lse, dq, dk, dv, bws, bws_bytes, *BHMND, c["scale"], c["causal"],
-                         fa.FA_F16, stream)
+        t = sets[i % ROTATE]
+        s = fa.fa_bwd_ws(t["q"], t["k"], t["v"], t["o"], t["do"], t["lse"], t["dq"], t["dk"], t["dv"], bws, bws_bytes,
+                         *BHMND, c["scale"], c["causal"], fa.FA_F16, stream)
         if s == fa.FA_ERR_UNSUPPORTED:
             have_bwd = False
             return
@@ -283,48 +296,41 @@ def run_ours(args):
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    def step(record):
-        flush.zero_()
-        e0, e1 = ev(), ev()
-        e0.record(stream)
-        run_fwd()
-        e1.record(stream)
-        flush.zero_()
-        e2, e3 = ev(), ev()
-        e2.record(stream)
-        run_bwd()
-        e3.record(stream)
-        e4, e5 = ev(), ev()
-        e4.record(stream)
-        run_dec()
-        e5.record(stream)
-        if record is not None:
-            record.append((e0, e1, e2, e3, e4, e5))
+    def steps(n):
+        """n steps: step i runs the forward and the backward on input set i % ROTATE and one decode.
+        Each part's n calls run back to back between one pair of CUDA events; returns their times."""
+        e = [ev() for _ in range(6)]
+        e[0].record(stream)
+        for i in range(n):
+            run_fwd(i)
+        e[1].record(stream)
+        e[2].record(stream)
+        for i in range(n):
+            run_bwd(i)
+        e[3].record(stream)
+        e[4].record(stream)
+        for _ in range(n):
+            run_dec()
+        e[5].record(stream)
+        return e
 
-    for _ in range(args.warmup):
-        step(None)
+    steps(args.warmup)
     check(fa.fa_last_status(stream), "warm-up")
     torch.cuda.synchronize()
 
-    recs = []
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        w0 = ev()
-        w0.record(stream)
-        for _ in range(args.steps):
-            step(recs)
-        w1 = ev()
-        w1.record(stream)
+        e = steps(args.steps)
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - t0
     check(fa.fa_last_status(stream), "timed steps")
-    t_fwd = sum(r[0].elapsed_time(r[1]) for r in recs) / 1e3
-    t_bwd = sum(r[2].elapsed_time(r[3]) for r in recs) / 1e3
-    t_dec = sum(r[4].elapsed_time(r[5]) for r in recs) / 1e3
-    t_step = w0.elapsed_time(w1) / 1e3  # includes the untimed L2 flushes
+    t_fwd = e[0].elapsed_time(e[1]) / 1e3
+    t_bwd = e[2].elapsed_time(e[3]) / 1e3
+    t_dec = e[4].elapsed_time(e[5]) / 1e3
+    t_step = e[0].elapsed_time(e[5]) / 1e3
     t_fwd = max_over_ranks(t_fwd, world)
     t_bwd = max_over_ranks(t_bwd, world)
     t_dec = max_over_ranks(t_dec, world)
@@ -456,6 +462,10 @@ def run_ours(args):
                                  "frac": round(gbs_r / peak_bw, 4), "peak_source": f"{peaks_src} copy bandwidth",
                                  "traffic": None}}
 
+    configs = None
+    if world == 1 and not args.no_configs:
+        configs = bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_src)
+
     launches_per_step = 1 + (3 if have_bwd else 0) + 2
     traffic = load_traffic()
     line = {
@@ -479,7 +489,8 @@ def run_ours(args):
             "head_dim": FWD["D"],
             "heads": FWD["H"],
             "parallelism": f"replicas{world}",
-            "l2": "flushed (512 MB write) before the forward and the backward; decode cache 4.29 GB > L2",
+            "l2": "inputs larger than L2: forward and backward rotate over 4 input sets (4 x 63 MB > 129 MB), "
+                  "calls back to back; decode cache 4.29 GB > L2; configs: L2 flushed (512 MB write) before each call",
         },
         "roofline": {
             "kernel": "fwd_d64_kernel<f16,non-causal>",
@@ -510,6 +521,7 @@ def run_ours(args):
         },
         "f32": f32,
         "decode_rows": dec_rows,
+        "configs": configs,
         "backward": None if bwd_tflops is None else {
             "value": round(bwd_tflops, 2), "unit": "TFLOP/s", "ms_per_call": round(t_bwd / K * 1e3, 4),
             "flops": "2.5 x forward",
@@ -536,6 +548,131 @@ def run_ours(args):
         }
     barrier(world)
     print(json.dumps(line), flush=True)
+
+
+def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_src, calls=20):
+    """Every configuration of the workload list, each timed on its own: one call between a pair of
+    CUDA events with L2 flushed before it (decode: its 4.29 GB cache is larger than L2, calls back to
+    back), averaged over `calls` calls after 3 untimed ones."""
+    import numpy as np
+    import torch
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    out = {}
+
+    def timed(fn, flushed=True):
+        for _ in range(3):
+            fn()
+        recs = []
+        for _ in range(calls):
+            if flushed:
+                flush.zero_()
+            a, b = ev(), ev()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            recs.append((a, b))
+        torch.cuda.synchronize()
+        check(fa.fa_last_status(stream), "configuration sweep")
+        return sum(a.elapsed_time(b) for a, b in recs) / len(recs) / 1e3
+
+    def tensor_entry(desc, flops, t, kernel, peak=peak_tf, peak_note=None):
+        tf = flops / t / 1e12
+        return {"config": desc, "value": round(tf, 2), "unit": "TFLOP/s", "us_per_call": round(t * 1e6, 2),
+                "l2": "flushed before each call",
+                "roofline": {"kernel": kernel, "bound": "tensor", "achieved": round(tf, 2), "peak": round(peak, 1),
+                             "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                             "peak_source": peak_note or f"{peaks_src} bf16 burst (fp16 dense rate equals bf16)",
+                             "traffic": None}}
+
+    def attn(B, H, M, N, D, dtype, seed, with_dout=False):
+        arrs = synth.attention_inputs(B, H, M, N, D, dtype, seed=seed, with_dout=with_dout)
+        return [dev(a, dtype) for a in arrs]
+
+    code = {"f32": fa.FA_F32, "f16": fa.FA_F16, "bf16": fa.FA_BF16}
+
+    def forward_entry(name, B, H, M, N, D, dtype, causal, scale, desc, kernel):
+        q, k, v = attn(B, H, M, N, D, dtype, seed=M + N)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
+        nb = fa.fa_fwd_workspace_bytes(B, H, M, N, D, causal, code[dtype])
+        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
+        t = timed(lambda: check(fa.fa_fwd_ws(q, k, v, o, lse, ws if nb else None, nb, B, H, M, N, D, scale, causal,
+                                             code[dtype], stream), name))
+        flops = 4.0 * B * H * M * N * D / (2 if causal else 1)
+        peak, note = peak_tf, None
+        if dtype == "f32":
+            peak = peak_tf * 1.1 / 2.25 / 3.0
+            note = f"{peaks_src} bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products"
+        out[name] = tensor_entry(desc, flops, t, kernel, peak, note)
+
+    # fp16 forward, B4 H12 D64, M = N over {512, 1024, 2048}; bf16 and causal at 2048
+    for n in (512, 1024, 2048):
+        forward_entry(f"fwd_f16_N{n}", 4, 12, n, n, 64, "f16", False, 0.125,
+                      f"fp16 forward B4 H12 M=N={n} D64 scale 0.125 non-causal (fa_fwd_ws)",
+                      "fwd_d64_kernel<f16,non-causal>")
+    forward_entry("fwd_bf16_N2048", 4, 12, 2048, 2048, 64, "bf16", False, 0.125,
+                  "bf16 forward B4 H12 M=N=2048 D64 scale 0.125 non-causal", "fwd_d64_kernel<bf16,non-causal>")
+    forward_entry("fwd_f16_N2048_causal", 4, 12, 2048, 2048, 64, "f16", True, 0.125,
+                  "fp16 forward B4 H12 M=N=2048 D64 scale 0.125 causal (FLOP halved)", "fwd_d64_kernel<f16,causal>")
+    # f32, one head, 256^2 and 4096^2 (3xTF32)
+    forward_entry("fwd_f32_N256", 1, 1, 256, 256, 64, "f32", False, 0.125,
+                  "f32 forward 1 head Nq=Nk=256 D64 scale 0.125 (3xTF32)", "fwd_f32_kernel<non-causal>")
+    # fp16 forward + backward, Z1 H2 N1024 D64, sm_scale 0.5, causal and not
+    for causal in (False, True):
+        tag = "causal" if causal else "noncausal"
+        forward_entry(f"cfg4_fwd_{tag}", 1, 2, 1024, 1024, 64, "f16", causal, 0.5,
+                      f"fp16 forward Z1 H2 N1024 D64 sm_scale 0.5 {tag}", f"fwd_d64_kernel<f16,{tag}>")
+    for causal in (False, True):
+        for M, B, H, name0 in ((1024, 1, 2, "cfg4"), (2048, 4, 12, "bwd")):
+            if name0 == "bwd" and causal:
+                continue
+            q, k, v, do = attn(B, H, M, M, 64, "f16", seed=20, with_dout=True)
+            o = torch.empty_like(q)
+            lse = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
+            check(fa.fa_fwd(q, k, v, o, lse, B, H, M, M, 64, 0.5, causal, fa.FA_F16, stream), "fa_fwd")
+            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            flops = 2.5 * 4.0 * B * H * M * M * 64 / (2 if causal else 1)
+            tag = "causal" if causal else "noncausal"
+            nb = fa.fa_bwd_ws_workspace_bytes(B, H, M, 64)
+            ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+            t = timed(lambda: check(fa.fa_bwd_ws(q, k, v, o, do, lse, dq, dk, dv, ws, nb, B, H, M, M, 64, 0.5, causal,
+                                                 fa.FA_F16, stream), "fa_bwd_ws"))
+            desc = f"fp16 backward B{B} H{H} N{M} D64 scale 0.5 {tag}"
+            out[f"{name0}_bwd_fused_{tag}"] = tensor_entry(
+                desc + " through fa_bwd_ws (delta, fused dK/dV/dQ, dQ conversion; FLOP = 2.5 x forward)", flops, t,
+                f"bwd_fused64_kernel<f16,{tag}>")
+            dws = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
+            t = timed(lambda: check(fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, dws, B, H, M, M, 64, 0.5, causal,
+                                              fa.FA_F16, stream), "fa_bwd"))
+            out[f"{name0}_bwd_3kernels_{tag}"] = tensor_entry(
+                desc + " through fa_bwd (delta, dK/dV, dQ kernels; FLOP = 2.5 x forward)", flops, t,
+                f"bwd_dkdv64_kernel + bwd_dq_kernel<f16,{tag}>")
+    # bf16 decode B8 H32 N32768 D128 at n_splits 16 and 256 (64 is the main line's)
+    d = DEC
+    qdec = dev(synth.decode_query(d["B"], d["H"], d["D"], d["dtype"], 0), "bf16")
+    kc = torch.empty((d["B"], d["H"], d["N"], d["D"]), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    g = torch.Generator(device="cuda").manual_seed(0)
+    kc.normal_(generator=g)
+    vc.normal_(generator=g)
+    odec = torch.empty_like(qdec)
+    for ns in (16, 256):
+        ws = torch.empty(fa.fa_decode_workspace_bytes(d["B"], d["H"], d["D"], ns) // 4, dtype=torch.float32,
+                         device="cuda")
+        t = timed(lambda: check(fa.fa_decode(qdec, kc, vc, odec, ws, d["B"], d["H"], d["N"], d["D"],
+                                             1 / math.sqrt(d["D"]), ns, fa.FA_BF16, stream), "fa_decode"),
+                  flushed=False)
+        gbs = dec_bytes() / t / 1e9
+        out[f"decode_splits{ns}"] = {
+            "config": f"bf16 decode B8 H32 N32768 D128 n_splits {ns} (cache 4.29 GB > L2, calls back to back)",
+            "value": round(gbs, 1), "unit": "GB/s", "us_per_call": round(t * 1e6, 2),
+            "roofline": {"kernel": "decode_split_kernel<128,bf16> + decode_combine_kernel", "bound": "hbm",
+                         "achieved": round(gbs, 1), "peak": peak_bw, "unit": "GB/s", "frac": round(gbs / peak_bw, 4),
+                         "peak_source": f"{peaks_src} copy bandwidth", "traffic": None}}
+    del kc, vc
+    torch.cuda.empty_cache()
+    return out
 
 
 def load_traffic():
@@ -650,6 +787,7 @@ def main():
     ap.add_argument("--decode-e2e", action="store_true", default=True)
     ap.add_argument("--no-decode-e2e", dest="decode_e2e", action="store_false")
     ap.add_argument("--profile", choices=sorted(PROFILE_CASES), help="run a few launches of one kernel and exit")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration sweep")
     args = ap.parse_args()
     if args.profile:
         run_profile(args.profile)

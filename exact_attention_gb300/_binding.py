@@ -18,6 +18,7 @@ from typing import Optional
 
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_F32, FA_F16, FA_BF16 = 0, 1, 2
+FA_SCHED_FWD_SPLIT, FA_SCHED_BWD_SPLIT, FA_SCHED_HOST_CHUNKS = 1, 2, 3
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 
@@ -41,6 +42,7 @@ EXPORTS = (
     "fa_status_string",
     "fa_last_error_message",
     "fa_set_wait_budget_ns",
+    "fa_set_schedule",
     "fa_debug_inject",
 )
 
@@ -101,6 +103,8 @@ def lib() -> ctypes.CDLL:
     L.fa_last_error_message.restype = ctypes.c_char_p
     L.fa_set_wait_budget_ns.argtypes = [ctypes.c_ulonglong]
     L.fa_set_wait_budget_ns.restype = st
+    L.fa_set_schedule.argtypes = [i, i]
+    L.fa_set_schedule.restype = st
     L.fa_debug_inject.argtypes = [i]
     L.fa_debug_inject.restype = st
     _lib = L
@@ -206,6 +210,25 @@ def fa_last_error_message() -> str:
 
 def fa_set_wait_budget_ns(ns: int) -> int:
     return lib().fa_set_wait_budget_ns(int(ns))
+
+def fa_set_schedule(key: int, value: int) -> int:
+    return lib().fa_set_schedule(int(key), int(value))
+
+
+class schedule:
+    """Context manager: fa_set_schedule(key, value) inside the block, automatic (-1) after it."""
+
+    def __init__(self, key: int, value: int):
+        self.key, self.value = key, value
+
+    def __enter__(self):
+        _check(fa_set_schedule(self.key, self.value), "fa_set_schedule")
+        return self
+
+    def __exit__(self, *exc):
+        fa_set_schedule(self.key, -1)
+        return False
+
 
 def fa_debug_inject(kind: int) -> int:
     return lib().fa_debug_inject(int(kind))

@@ -148,7 +148,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
-  const float sl2 = scale * kLog2eB;
+  // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
+  // and dK, dQ take the signed scale
+  const float sl2 = fabsf(scale) * kLog2eB;
+  const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
 
   auto item = [&](int w) {
     BwdItem it;
@@ -241,7 +244,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-      constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
+      const uint32_t id_dp = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);  // dP: never negated
+      const uint32_t id_s = id_dp | neg_a;
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
       uint32_t it_s = 0, p_ph = 0;
       int n_item = 0;
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             ptx::mma_f16_ss(tmem + 0, kmajor_desc(sK, ks), kmajor_desc(sQ(st), ks), id_s, ks > 0);
-            ptx::mma_f16_ss(tmem + 128, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
+            ptx::mma_f16_ss(tmem + 128, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_dp, ks > 0);
           }
           ptx::tc_commit(ptx::smem_u32(&hdr->s_full));
           ok = ptx::mbar_wait(ptx::smem_u32(&hdr->p_full), p_ph, wc, 22);
@@ -476,7 +480,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
-  const float sl2 = scale * kLog2eB;
+  // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
+  // and dK, dQ take the signed scale
+  const float sl2 = fabsf(scale) * kLog2eB;
+  const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
   auto item = [&](int w) {
     BwdItem it;
     // causal: key tiles with the most query blocks (the first ones) go first, all heads of a
@@ -589,7 +596,8 @@ __global__ void __launch_bounds__(kThreadsO, 1)
     if (lane == 0) {
       const bool scores = warp == kWarpMmaO;
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-      constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
+      const uint32_t id_dp = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);  // dP: never negated
+      const uint32_t id_s = id_dp | neg_a;
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
       uint32_t it_s = 0, n1 = 0, n2 = 0;
       int n_item = 0;
@@ -610,7 +618,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         const int st = k % C::kStages;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
+          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_dp, ks > 0);
         commit(&hdr->dp_full);
       };
       for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
@@ -897,7 +905,10 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
-  const float sl2 = scale * kLog2eB;
+  // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
+  // and dK, dQ take the signed scale
+  const float sl2 = fabsf(scale) * kLog2eB;
+  const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
   const bool split = !CAUSAL && part_ws != nullptr;  // the host checks items * nqb < 2^31
   const uint32_t units = split ? static_cast<uint32_t>(items) * static_cast<uint32_t>(nqb) : 0u;
   auto item = [&](int w) {
@@ -1023,7 +1034,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (lane == 0) {
       const bool scores = warp == kWarpMmaF;
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-      constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
+      const uint32_t id_dp = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);  // dP: never negated
+      const uint32_t id_s = id_dp | neg_a;
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
       constexpr uint32_t id_q = ptx::idesc_f32acc(kT, D, fmt, fmt, true, true);  // A = dS read MN-major
       uint32_t it_s = 0, n1 = 0, n2 = 0, nq = 0;
@@ -1045,7 +1057,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         const int st = k % C::kStages;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_s, ks > 0);
+          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sV, ks), kmajor_desc(sdO(st), ks), id_dp, ks > 0);
         commit(&hdr->dp_full);
       };
       FusedSched<CAUSAL> sch(split, units);
@@ -1446,7 +1458,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nqb;
-  const float sl2 = scale * kLog2eB;
+  // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
+  // and dK, dQ take the signed scale
+  const float sl2 = fabsf(scale) * kLog2eB;
+  const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
   auto item = [&](int w) {
     BwdItem it;
     const int qb_rev = w / BH;  // causal: heaviest (last) query blocks first
@@ -1505,7 +1520,8 @@ __global__ void __launch_bounds__(kThreadsO, 1)
     if (lane == 0) {
       const bool scores = warp == kWarpMmaO;
       constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-      constexpr uint32_t id_s = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);
+      const uint32_t id_dp = ptx::idesc_f32acc(kT, kT, fmt, fmt, false, false);  // dP: never negated
+      const uint32_t id_s = id_dp | neg_a;
       constexpr uint32_t id_g = ptx::idesc_f32acc(kT, D, fmt, fmt, false, true);
       uint32_t it_s = 0, n1 = 0, n2 = 0;
       int n_item = 0;
@@ -1526,7 +1542,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         const int st = k % C::kStages;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sdO, ks), kmajor_desc(sV(st), ks), id_s, ks > 0);
+          ptx::mma_f16_ss(tmem + cdP, kmajor_desc(sdO, ks), kmajor_desc(sV(st), ks), id_dp, ks > 0);
         commit(&hdr->dp_full);
       };
       for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <atomic>
+#include <chrono>
 #include <mutex>
 #include <vector>
 
@@ -126,12 +127,11 @@ fa_status check_sizes(int B, int H, int M, int N, int D) {
   return FA_OK;
 }
 
-// The tensor-core paths fold scale into the exponent after taking the row
-// maximum of the raw scores, which needs scale > 0.
-fa_status check_scale(float scale, bool positive) {
+// Any finite scale: the tensor-core paths negate the score product in the tensor core when
+// scale < 0 and scale the exponent by |scale|.
+fa_status check_scale(float scale) {
   if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
     return fail(FA_ERR_INVALID, "scale must be finite (got %g)", static_cast<double>(scale));
-  if (positive && !(scale > 0.f)) return fail(FA_ERR_INVALID, "scale must be > 0 (got %g)", static_cast<double>(scale));
   return FA_OK;
 }
 
@@ -177,9 +177,15 @@ using namespace fa;
 
 namespace {
 
+// Schedule choices fixed by fa_set_schedule (-1: automatic). Process-wide.
+std::atomic<int> g_sched_fwd_split{-1};
+std::atomic<int> g_sched_bwd_split{-1};
+std::atomic<int> g_sched_host_chunks{-1};
+constexpr int kHostChunks = 8;  // most head chunks of fa_fwd_host (events kept per device)
+
 // Whether a forward call with a workspace runs the split schedule (D = 64 halves).
-// FA_FWD_SPLIT=0 / 1 forces it off / on (tests use it); by default it is used for non-causal
-// calls when whole pairs would leave the last wave of CTAs less than 90 % full.
+// fa_set_schedule(FA_SCHED_FWD_SPLIT, 0 / 1) forces it off / on; by default it is used for
+// non-causal calls when whole pairs would leave the last wave of CTAs less than 90 % full.
 bool split_capable(int D, int dtype) { return D == 64 && dtype != FA_F32; }
 
 // Units of the D=64 forward's split schedule: the key blocks of each query-tile pair's tile 0
@@ -199,10 +205,8 @@ bool use_split(int BH, int M, int N, int causal, int num_sms) {
   const long long pairs = static_cast<long long>(BH) * ((M + 255) / 256);
   const long long units = split_units(BH, M, N, causal);
   if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
-  if (const char* e = std::getenv("FA_FWD_SPLIT")) {
-    if (e[0] == '0') return false;
-    if (e[0] == '1') return true;
-  }
+  const int forced = g_sched_fwd_split.load();
+  if (forced >= 0) return forced == 1;
   if (units < 4ll * num_sms) return false;
   // causal: whole pairs dealt in a serpentine order (heaviest with lightest) measured faster
   // than the split, whose extra pieces cost more than the balance gains
@@ -213,22 +217,34 @@ bool use_split(int BH, int M, int N, int causal, int num_sms) {
 
 // Whether the fused backward (fa_bwd_ws, D = 64) runs its split schedule: non-causal calls
 // whose whole key tiles would leave the last round of CTAs less than 90 % full.
-// FA_BWD_SPLIT=0 / 1 forces it off / on (non-causal only; tests use it).
+// fa_set_schedule(FA_SCHED_BWD_SPLIT, 0 / 1) forces it off / on (non-causal only).
 bool use_bwd_split(int BH, int M, int N, int D, int causal, int num_sms) {
   if (D != 64 || causal) return false;
   const long long items = static_cast<long long>(BH) * ((N + 127) / 128);
   const long long units = items * ((M + 127) / 128);
   if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
-  if (const char* e = std::getenv("FA_BWD_SPLIT")) {
-    if (e[0] == '0') return false;
-    if (e[0] == '1') return true;
-  }
+  const int forced = g_sched_bwd_split.load();
+  if (forced >= 0) return forced == 1;
   if (units < 4ll * num_sms) return false;
   const long long rounds = (items + num_sms - 1) / num_sms;
   return items * 10 < rounds * num_sms * 9;
 }
 
-std::atomic<uint32_t> g_epoch{0};
+// Launch epochs of the split schedules' flags and counters. The sequence starts at a value
+// drawn from the clock, so a word that foreign data left in a reused workspace is unlikely to
+// equal the epoch of any launch; 0 (what a zero-filled workspace holds) is skipped.
+uint32_t next_epoch() {
+  static std::atomic<uint32_t> epoch{[] {
+    uint64_t x = static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count()) +
+                 0x9E3779B97F4A7C15ull;  // splitmix64 finaliser over the clock
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    return static_cast<uint32_t>(x ^ (x >> 31));
+  }()};
+  uint32_t e = epoch.fetch_add(1u) + 1u;
+  if (e == 0u) e = epoch.fetch_add(1u) + 1u;
+  return e;
+}
 std::atomic<int> g_inject{0};  // fa_debug_inject: consumed by the next decode launch
 
 // fa_decode / fa_decode_ex: R query rows per (batch, head), each against all N keys.
@@ -237,7 +253,7 @@ fa_status decode_impl(const void* q, const void* Kcache, const void* Vcache, voi
                       const char* name) {
   FA_TRY(check_dtype(dtype));
   FA_TRY(check_sizes(B, H, 1, N, D));
-  FA_TRY(check_scale(scale, false));
+  FA_TRY(check_scale(scale));
   if (R < 1) return fail(FA_ERR_INVALID, "%s: R=%d query rows", name, R);
   if (R > kDecMaxRows)
     return fail(FA_ERR_UNSUPPORTED, "%s: R=%d query rows above %d (fa_fwd takes any number)", name, R, kDecMaxRows);
@@ -266,7 +282,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
                    const char* name) {
   FA_TRY(check_dtype(dtype));
   FA_TRY(check_sizes(B, H, M, N, D));
-  FA_TRY(check_scale(scale, true));
+  FA_TRY(check_scale(scale));
   if (B * H == 0 || M == 0) return FA_OK;
   if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
   FA_TRY(check_ptr(Q, "Q"));
@@ -284,9 +300,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
     if (use_split(B * H, M, N, causal, ctx.num_sms)) {
       sp.ws = static_cast<float*>(ws);
       sp.flags = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + need - ctx.num_sms * 8 * sizeof(uint32_t));
-      uint32_t ep = ++g_epoch;
-      if (ep == 0u) ep = ++g_epoch;  // 0 is what a fresh workspace holds
-      sp.epoch = ep;
+      sp.epoch = next_epoch();
     }
   }
   int parts = 1;
@@ -301,10 +315,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   cudaError_t e;
   if (dtype == FA_F32) {
     uint32_t ep = 0;
-    if (parts > 1) {
-      ep = ++g_epoch;
-      if (ep == 0u) ep = ++g_epoch;  // 0 is what a fresh workspace holds
-    }
+    if (parts > 1) ep = next_epoch();
     e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, parts, static_cast<float*>(ws), ep, ctx);
   } else {
     e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
@@ -323,7 +334,7 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   FA_TRY(check_dtype(dtype));
   FA_TRY(check_sizes(B, H, M, N, D));
   if (dtype == FA_F32) return fail(FA_ERR_UNSUPPORTED, "%s supports FA_F16 and FA_BF16", name);
-  FA_TRY(check_scale(scale, true));
+  FA_TRY(check_scale(scale));
   if (B * H == 0 || M == 0) return FA_OK;
   if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
   FA_TRY(check_ptr(Q, "Q"));
@@ -350,6 +361,16 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
 
 }  // namespace
 
+namespace fa {
+fa_status decode_entry(const void* q, const void* Kcache, const void* Vcache, void* O, float* LSE, float* partial_ws,
+                       int B, int H, int R, int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream,
+                       const char* name) {
+  return decode_impl(q, Kcache, Vcache, O, LSE, partial_ws, B, H, R, N, D, scale, n_splits, dtype, stream, name);
+}
+fa_status fail_msg(fa_status s, const char* msg) { return fail(s, "%s", msg); }
+fa_status cuda_fail_msg(cudaError_t e, const char* what) { return cuda_fail(e, what); }
+}  // namespace fa
+
 extern "C" {
 
 const char* fa_status_string(fa_status s) {
@@ -370,6 +391,22 @@ fa_status fa_set_wait_budget_ns(unsigned long long ns) {
   std::lock_guard<std::mutex> lock(g_mutex);
   g_wait_budget_ns = ns;
   return FA_OK;
+}
+
+fa_status fa_set_schedule(fa_sched_key key, int value) {
+  switch (key) {
+    case FA_SCHED_FWD_SPLIT:
+    case FA_SCHED_BWD_SPLIT:
+      if (value < -1 || value > 1) return fail(FA_ERR_INVALID, "schedule key %d takes -1, 0 or 1 (got %d)", key, value);
+      (key == FA_SCHED_FWD_SPLIT ? g_sched_fwd_split : g_sched_bwd_split).store(value);
+      return FA_OK;
+    case FA_SCHED_HOST_CHUNKS:
+      if (value != -1 && (value < 1 || value > kHostChunks))
+        return fail(FA_ERR_INVALID, "host chunks take -1 or 1..%d (got %d)", kHostChunks, value);
+      g_sched_host_chunks.store(value);
+      return FA_OK;
+  }
+  return fail(FA_ERR_INVALID, "unknown schedule key %d", static_cast<int>(key));
 }
 
 fa_status fa_debug_inject(int kind) {
@@ -465,81 +502,6 @@ fa_status fa_decode_ex(const void* q, const void* Kcache, const void* Vcache, vo
                      "fa_decode_ex");
 }
 
-}  // extern "C"
-
-// ---------------------------------------------------------------------------
-// Decode with scratch that the library owns.
-//
-// Some callers cannot allocate device memory when they need to decode: code
-// that runs under a caching or arena allocator that must not grow, a runtime
-// that accounts for every buffer itself, or a C caller that has no allocator
-// of its own at that point. fa_decode_static serves them: the split partials
-// live in g_decode_scratch, a fixed array in the library's device image that
-// every GPU loading the library holds until the process exits.
-namespace fa {
-namespace {
-
-constexpr size_t kStaticScratchFloats = static_cast<size_t>(4) << 20;  // 16 MiB of float32
-
-static __device__ __align__(256) float g_decode_scratch[kStaticScratchFloats];
-
-float* g_static_ptr[kMaxDevices] = {};
-
-// Once per device, with that device current: the device address of the array.
-// In host code the array's name only stands for it; the kernels must be given
-// this address instead.
-fa_status static_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (dev < 0 || dev >= kMaxDevices) return fail(FA_ERR_CUDA, "device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_static_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(decode scratch)");
-    g_static_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_static_ptr[dev];
-  return FA_OK;
-}
-
-}  // namespace
-}  // namespace fa
-
-extern "C" {
-
-fa_status fa_decode_static(const void* q, const void* Kcache, const void* Vcache, void* O, int B, int H, int N, int D,
-                           float scale, int n_splits, fa_dtype dtype, void* stream) {
-  FA_TRY(check_dtype(dtype));
-  FA_TRY(check_sizes(B, H, 1, N, D));
-  FA_TRY(check_scale(scale, false));
-  if (B * H == 0) return FA_OK;
-  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
-  if (n_splits < 1 || n_splits > N || n_splits > 65535)
-    return fail(FA_ERR_INVALID, "n_splits=%d outside [1, min(N=%d, 65535)]", n_splits, N);
-  if (B * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_decode_static: B*H=%d above 65535", B * H);
-  const size_t need = static_cast<size_t>(B) * H * n_splits * (D + 2);
-  if (need > kStaticScratchFloats)
-    return fail(FA_ERR_INVALID,
-                "fa_decode_static: B*H*n_splits*(D+2) = %zu floats exceeds the library's fixed scratch of %zu "
-                "floats (16 MiB); use fewer splits or fa_decode with a caller workspace",
-                need, kStaticScratchFloats);
-  FA_TRY(check_ptr(q, "q"));
-  FA_TRY(check_ptr(Kcache, "Kcache"));
-  FA_TRY(check_ptr(Vcache, "Vcache"));
-  FA_TRY(check_ptr(O, "O"));
-  float* ws = nullptr;
-  FA_TRY(static_scratch(&ws));
-  LaunchCtx ctx{};
-  FA_TRY(make_ctx(&ctx, stream));
-  ctx.inject = g_inject.exchange(0);
-  cudaError_t e = launch_decode(q, Kcache, Vcache, O, nullptr, ws, B * H, 1, N, D, scale, n_splits, dtype, ctx);
-  if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "fa_decode_static: configuration not supported");
-  if (e != cudaSuccess) return cuda_fail(e, "fa_decode_static launch");
-  return FA_OK;
-}
-
 fa_status fa_last_status(void* stream) {
   DevState* st = nullptr;
   FA_TRY(device_state(&st));
@@ -565,8 +527,8 @@ fa_status fa_last_status(void* stream) {
 // ---------------------------------------------------------------------------
 // Forward on host buffers, with the copies overlapped with the kernels.
 //
-// The (batch, head) heads are cut into kHostDefaultChunks chunks (FA_HOST_CHUNKS=1..8 in the
-// environment overrides it). Three internal
+// The (batch, head) heads are cut into kHostDefaultChunks chunks (fa_set_schedule with
+// FA_SCHED_HOST_CHUNKS fixes another count, 1..8). Three internal
 // streams of the device carry the copies in, the kernels and the copies out, so
 // chunk c's inputs travel while chunk c-1 is computed and chunk c-2's output
 // travels back; events order each chunk's three steps, and the caller's stream
@@ -574,7 +536,6 @@ fa_status fa_last_status(void* stream) {
 
 namespace {
 
-constexpr int kHostChunks = 8;         // events kept per device
 constexpr int kHostDefaultChunks = 4;  // measured best at B4 H12 N2048 D64: the copies in and out share
                                        // the host link (about 220-260 GB/s together), and a chunk's
                                        // kernel has a fixed cost of about 15 us, so more chunks lose
@@ -627,11 +588,8 @@ struct HostLayout {
 HostLayout host_layout(int B, int H, int M, int N, int D, int causal, fa_dtype dtype) {
   HostLayout L;
   const long long BH = static_cast<long long>(B) * H;
-  int want = kHostDefaultChunks;
-  if (const char* e = std::getenv("FA_HOST_CHUNKS")) {  // 1..8
-    const int v = std::atoi(e);
-    if (v >= 1 && v <= kHostChunks) want = v;
-  }
+  const int forced = g_sched_host_chunks.load();
+  const int want = forced >= 1 ? forced : kHostDefaultChunks;
   L.chunks = static_cast<int>(BH < want ? BH : want);
   const int hi = static_cast<int>((BH + L.chunks - 1) / L.chunks), lo = static_cast<int>(BH / L.chunks);
   const size_t w1 = fa_fwd_workspace_bytes(1, hi, M, N, D, causal, dtype);
@@ -663,7 +621,7 @@ fa_status fa_fwd_host(const void* hQ, const void* hK, const void* hV, void* hO, 
                       void* stream) {
   FA_TRY(check_dtype(dtype));
   FA_TRY(check_sizes(B, H, M, N, D));
-  FA_TRY(check_scale(scale, true));
+  FA_TRY(check_scale(scale));
   if (B * H == 0 || M == 0) return FA_OK;
   if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
   // what the forward supports, checked before anything is queued

@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Device-side status word, one per device. A kernel that gives up a bounded
@@ -86,9 +88,18 @@ cudaError_t launch_bwd(const void* Q, const void* K, const void* V, const void* 
                        void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, int D,
                        float scale, bool causal, int dtype, const BwdSplit& sp, const LaunchCtx& ctx);
 
+// Entry-point helpers of fa_api.cu used by the other host translation units: the decode
+// entry points' checks and launch, and recording a failure's one-line reason.
+fa_status decode_entry(const void* q, const void* Kcache, const void* Vcache, void* O, float* LSE, float* partial_ws,
+                       int B, int H, int R, int N, int D, float scale, int n_splits, fa_dtype dtype, void* stream,
+                       const char* name);
+fa_status fail_msg(fa_status s, const char* msg);
+fa_status cuda_fail_msg(cudaError_t e, const char* what);
+
 // Encodes a 3-D TMA tensor map over a contiguous [outer, rows, inner] tensor
 // (inner = head dimension) with a box of [box_inner, box_rows, 1] elements and
 // 128-byte swizzle. Returns false when the driver rejects it.
+
 bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
                   uint32_t box_inner, uint32_t box_rows);
 

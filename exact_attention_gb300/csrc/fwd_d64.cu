@@ -197,7 +197,7 @@ template <bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_d64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, float* __restrict__ LSE, int BH,
-                   int M, int N, float scale_log2, float* __restrict__ ws, uint32_t* __restrict__ flags, uint32_t epoch,
+                   int M, int N, float scale_log2_signed, float* __restrict__ ws, uint32_t* __restrict__ flags, uint32_t epoch,
                    DevStatus* status, unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
   Hdr* hdr = reinterpret_cast<Hdr*>(smem_raw);
@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM);
   const int nkb = (N + kBN - 1) / kBN;
   const bool split = ws != nullptr;
+  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|
+  const bool neg_scale = scale_log2_signed < 0.f;
+  const float scale_log2 = fabsf(scale_log2_signed);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kQBuf; ++i) {
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMma || warp == kWarpMma + 1) {
     // ------------------------------------------------------------ MMA issuer of tile t (lane 0)
     constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-    constexpr uint32_t idesc_qk = ptx::idesc_f32acc(kBM, kBN, fmt, fmt, false, false);
+    const uint32_t idesc_qk = ptx::idesc_f32acc(kBM, kBN, fmt, fmt, false, false) | (neg_scale ? ptx::kNegateA : 0u);
     constexpr uint32_t idesc_pv = ptx::idesc_f32acc(kBM, kD, fmt, fmt, false, true);
     const int t = warp - kWarpMma;
     if (lane == 0) {
@@ -612,6 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = __shfl_sync(0xFFFFFFFFu, got, 0);
           if (!ok) break;
           (void)ptx::ld_acquire_u32(f);  // orders this lane's reads of the slot after the flag
+          if (lane == 0) *f = 0u;          // consumed: the workspace goes back to zeros
           const float* slot = ws + static_cast<size_t>(c2) * kSlotFloats;
           const float m_p = slot[kPairRows * kD + prow];
           const float l_p = slot[kPairRows * kD + kPairRows + prow];

@@ -104,7 +104,7 @@ template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreads32, 1)
     fwd_f32_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, float* __restrict__ O, float* __restrict__ LSE, int BH,
-                   int M, int N, float scale_log2, int parts, float* __restrict__ ws,
+                   int M, int N, float scale_log2_signed, int parts, float* __restrict__ ws,
                    unsigned long long* __restrict__ counters, uint32_t epoch, DevStatus* status,
                    unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -123,6 +123,9 @@ __global__ void __launch_bounds__(kThreads32, 1)
   const int nqt = (M + kBM32 - 1) / kBM32;
   const int nkb = (N + kBN32 - 1) / kBN32;
   const int tiles = BH * nqt;
+  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|
+  const bool neg_scale = scale_log2_signed < 0.f;
+  const float scale_log2 = fabsf(scale_log2_signed);
 
   // Unit w = (tile w / parts, part w % parts): the tile's key blocks [jb, jb + nb) of its part.
   // With parts > 1 each part leaves an unnormalised partial and counts itself in on its tile;
@@ -229,7 +232,8 @@ __global__ void __launch_bounds__(kThreads32, 1)
   } else if (warp == kWarpMma32) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t id = ptx::idesc_f32acc(kBM32, kBN32, ptx::kFmtTF32, ptx::kFmtTF32, false, false);
+      const uint32_t id =
+          ptx::idesc_f32acc(kBM32, kBN32, ptx::kFmtTF32, ptx::kFmtTF32, false, false) | (neg_scale ? ptx::kNegateA : 0u);
       constexpr uint32_t id_pv = ptx::idesc_f32acc(kBM32, kD32, ptx::kFmtTF32, ptx::kFmtTF32, false, false);
       uint32_t it = 0, p_ph = 0;
       int n = 0;

@@ -111,7 +111,7 @@ template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_half_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, void* __restrict__ Optr, float* __restrict__ LSE,
-                    int BH, int M, int N, float scale_log2, DevStatus* status, unsigned long long budget_ns) {
+                    int BH, int M, int N, float scale_log2_signed, DevStatus* status, unsigned long long budget_ns) {
   using C = FwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   FwdHdr* hdr = reinterpret_cast<FwdHdr*>(smem_raw);
@@ -127,6 +127,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM);
   const int nkb = (N + kBN - 1) / kBN;
   const int num_tiles = num_pairs * BH;
+  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|
+  const bool neg_scale = scale_log2_signed < 0.f;
+  const float scale_log2 = fabsf(scale_log2_signed);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -207,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // than one issuer per tile, whose MMAs interleave in the pipe, and than a
     // warp-wide loop).
     constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
-    constexpr uint32_t idesc_qk = ptx::idesc_f32acc(kBM, kBN, fmt, fmt, false, false);
+    const uint32_t idesc_qk = ptx::idesc_f32acc(kBM, kBN, fmt, fmt, false, false) | (neg_scale ? ptx::kNegateA : 0u);
     constexpr uint32_t idesc_pv = ptx::idesc_f32acc(kBM, C::kDO, fmt, fmt, false, true);
     if (lane == 0) {
       uint32_t kv_it = 0;

@@ -230,6 +230,9 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t m, uint32_t n, uint
          ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+// Bit 13 of the same descriptor negates A: D (+)= (-A) B. The kernels set it on the score
+// product when scale < 0, so that the softmax always multiplies by |scale|.
+constexpr uint32_t kNegateA = 1u << 13;
 
 // D[tmem] (+)= A[smem] * B[smem]^T, one elected thread.
 __device__ __forceinline__ void mma_f16_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {

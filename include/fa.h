@@ -57,7 +57,8 @@ typedef enum fa_dtype { FA_F32 = 0, FA_F16 = 1, FA_BF16 = 2 } fa_dtype;
  *   LSE [B,H,M] float32                    output, natural log of the row sum of
  *                                          exp(scale*q.k); may be NULL
  *   scale                                  multiplies Q K^T before the softmax;
- *                                          must be finite and > 0
+ *                                          any finite value (scale < 0 negates
+ *                                          the score product in the tensor core)
  *   causal                                 nonzero: key j is visible to query i
  *                                          iff j <= i (top-left aligned)
  * M, N >= 1 (N == 0 is FA_ERR_INVALID). Any M, N: ragged tails are masked.
@@ -90,7 +91,11 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  *   workspace        device pointer, 16-byte aligned, at least
  *                    fa_fwd_workspace_bytes(...) bytes, or NULL (then this is
  *                    fa_fwd). Zero-filled by the caller before its first use;
- *                    afterwards the library leaves it in a reusable state.
+ *                    afterwards the library leaves it in a reusable state
+ *                    (flags carry a per-launch epoch from a sequence that
+ *                    starts at a clock-drawn value, and consumed flags are
+ *                    reset to zero). If other data were written over it,
+ *                    zero-fill it again before the next call.
  *                    Owned by the caller; two calls must not use the same
  *                    workspace at the same time.
  *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
@@ -98,7 +103,7 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  * The split is used when the call is not causal, every SM gets at least four key
  * blocks and the last wave would be less than 90 % full (causal pairs, whose key
  * ranges differ in length, are dealt whole in a serpentine order, which measured
- * faster); FA_FWD_SPLIT=0 or 1 in the environment turns it off or on regardless.
+ * faster); fa_set_schedule(FA_SCHED_FWD_SPLIT, 0 or 1) turns it off or on regardless.
  * For f32 with few query tiles, several CTAs share each tile's keys: each writes
  * an unnormalised partial and counts itself in on the tile, and the one that
  * counts in last merges the partials the same way and writes O and LSE.
@@ -111,8 +116,8 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
  * The forward on HOST buffers: copies in, computes and copies out, overlapped.
  *
  * For callers whose Q, K, V live in host memory and who want O (and LSE) back
- * there. The (batch, head) heads are cut into 4 chunks (FA_HOST_CHUNKS=1..8 in
- * the environment overrides that); the library's
+ * there. The (batch, head) heads are cut into 4 chunks (fa_set_schedule with
+ * FA_SCHED_HOST_CHUNKS fixes another count, 1..8); the library's
  * own copy and compute streams for the device move chunk c in while chunk c-1
  * is computed (same kernels and results as fa_fwd_ws) and chunk c-2's output
  * travels back. The call is asynchronous and ordered on `stream`: work queued
@@ -130,8 +135,10 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
  *                                     16-byte aligned, zero-filled before its
  *                                     first use; it holds the device copies of
  *                                     Q, K, V, O, LSE and the forward's own
- *                                     workspace; two calls must not share it
- *                                     at the same time
+ *                                     workspace, whose place depends on the
+ *                                     problem's shape, so zero-fill it again
+ *                                     when the shape or dtype changes; two
+ *                                     calls must not share it at the same time
  *   the rest                          as for fa_fwd
  * Errors as fa_fwd, plus FA_ERR_INVALID for a NULL host buffer or a small
  * workspace; arguments are checked before anything is queued.
@@ -157,8 +164,9 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int M, int N, int D, int causal
  *   dQ [B,H,M,D], dK [B,H,N,D], dV [B,H,N,D]   outputs, dtype
  *   delta_ws         caller-owned scratch of fa_bwd_workspace_bytes(B,H,M)
  *                    bytes; holds rowsum(dO o O) (float32 [B,H,M]) on return
- * dtype must be FA_F16 or FA_BF16 (FA_ERR_UNSUPPORTED for FA_F32); scale as
- * for fa_fwd (finite, > 0).
+ * dtype must be FA_F16 or FA_BF16 (FA_ERR_UNSUPPORTED for FA_F32: the page
+ * that defines the f32 method, "Flash attention, f32", gives a forward only);
+ * scale as for fa_fwd (any finite value; dK and dQ carry its sign).
  */
 fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                  void* dQ, void* dK, void* dV, float* delta_ws, int B, int H, int M, int N, int D, float scale,
@@ -313,6 +321,24 @@ const char* fa_last_error_message(void);
  * FA_ERR_INVALID.
  */
 fa_status fa_set_wait_budget_ns(unsigned long long ns);
+
+/*
+ * Schedule controls (no counterpart on the pages). The library chooses some
+ * work schedules per call from the problem's shape; these fix a choice instead,
+ * for tuning and for tests that must reach each schedule. Process-wide (every
+ * device, every thread); results do not depend on them beyond the f32 summation
+ * order the split schedules document. value -1 restores the automatic choice,
+ * which is the default.
+ *   FA_SCHED_FWD_SPLIT    0 / 1: the D = 64 forward's split schedule (fa_fwd_ws,
+ *                         fa_fwd_host) off / on
+ *   FA_SCHED_BWD_SPLIT    0 / 1: the fused backward's split schedule (fa_bwd_ws,
+ *                         non-causal, D = 64) off / on
+ *   FA_SCHED_HOST_CHUNKS  1..8: number of head chunks fa_fwd_host pipelines
+ *                         (fa_fwd_host_workspace_bytes depends on it)
+ * Other keys or values: FA_ERR_INVALID.
+ */
+typedef enum fa_sched_key { FA_SCHED_FWD_SPLIT = 1, FA_SCHED_BWD_SPLIT = 2, FA_SCHED_HOST_CHUNKS = 3 } fa_sched_key;
+fa_status fa_set_schedule(fa_sched_key key, int value);
 
 /*
  * Test-only fault injection (no counterpart on the pages; exercises the bounded

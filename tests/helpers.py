@@ -8,8 +8,11 @@ from exact_attention_gb300 import synth
 TORCH_DT = {"f32": "float32", "f16": "float16", "bf16": "bfloat16"}
 
 # Tolerances stated for this method: max |GPU - oracle| on O, on the gradients and on LSE.
+# bf16 gradients have no stated bound: the fp16 one scaled by the ratio of the two types' unit
+# roundoffs (2^-8 / 2^-11 = 8), since the same rounding steps (P and dS rounded once to the I/O
+# type, outputs rounded once) dominate both.
 TOL_O = {"f32": 1e-4, "f16": 2e-3, "bf16": 1e-2}
-TOL_GRAD = {"f16": 1e-2, "bf16": 5e-2}
+TOL_GRAD = {"f16": 1e-2, "bf16": 8e-2}
 TOL_LSE = 1e-4
 REL_L2_F32 = 1e-5
 

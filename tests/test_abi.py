@@ -74,7 +74,8 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 8, 0, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_ERR_INVALID
     assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, -1, 1, 8, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_ERR_INVALID
     assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 8, 8, 64, 0.1, 0, 7, 0) == fa.FA_ERR_INVALID
-    assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 8, 8, 64, -1.0, 0, fa.FA_F16, 0) == fa.FA_ERR_INVALID
+    assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 8, 8, 64, float("-inf"), 0, fa.FA_F16, 0) == fa.FA_ERR_INVALID
+    assert "finite" in fa.fa_last_error_message()
     assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, 1, 1, 8, 8, 64, float("nan"), 0, fa.FA_F16, 0) == fa.FA_ERR_INVALID
     # B*H*max(M,N) overflowing a 32-bit row index
     assert fa.fa_fwd(FAKE, FAKE, FAKE, FAKE, None, 1 << 16, 1 << 10, 1 << 10, 8, 64, 0.1, 0, fa.FA_F16, 0) == \
@@ -98,8 +99,8 @@ def test_invalid_arguments_rejected_before_launch(lib):
         fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 128, 0.1, 0, fa.FA_F32, 0) == \
         fa.FA_ERR_UNSUPPORTED
-    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 64, 0.0, 0, fa.FA_F16, 0) == \
-        fa.FA_ERR_INVALID
+    assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 64, float("inf"), 0, fa.FA_F16,
+                          0) == fa.FA_ERR_INVALID
     # decode with rows: R = 0 invalid, R = 5 unsupported
     assert fa.fa_decode_ex(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 1, 0, 100, 128, 0.1, 4, fa.FA_BF16, 0) == \
         fa.FA_ERR_INVALID
@@ -113,3 +114,19 @@ def test_empty_problems_are_no_ops(lib):
     assert fa.fa_fwd(None, None, None, None, None, 2, 4, 0, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_OK
     assert fa.fa_decode(None, None, None, None, None, 0, 4, 8, 64, 0.1, 1, fa.FA_F16, 0) == fa.FA_OK
     assert fa.fa_fwd_host(None, None, None, None, None, None, 0, 0, 4, 8, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_OK
+
+
+def test_schedule_controls(lib):
+    """fa_set_schedule: valid keys and values are accepted (and reset to automatic), others refused."""
+    for key in (fa.FA_SCHED_FWD_SPLIT, fa.FA_SCHED_BWD_SPLIT):
+        for v in (0, 1, -1):
+            assert fa.fa_set_schedule(key, v) == fa.FA_OK
+        assert fa.fa_set_schedule(key, 2) == fa.FA_ERR_INVALID
+    for v in (1, 8, -1):
+        assert fa.fa_set_schedule(fa.FA_SCHED_HOST_CHUNKS, v) == fa.FA_OK
+    for v in (0, 9, -2):
+        assert fa.fa_set_schedule(fa.FA_SCHED_HOST_CHUNKS, v) == fa.FA_ERR_INVALID
+    assert fa.fa_set_schedule(0, 1) == fa.FA_ERR_INVALID
+    assert fa.fa_set_schedule(4, 1) == fa.FA_ERR_INVALID
+    with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
+        pass

@@ -55,6 +55,15 @@ def test_backward_tutorial_shape(causal, std, fused):
     check(inputs, o, grads, delta, "f16", causal, 0.5)
 
 
+@FUSED
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_tutorial_shape_bf16(causal, fused):
+    """The tutorial's shape in bf16 with N(0,1) inputs and sm_scale 0.5, the most peaked case the
+    workloads hold: |dQ|, |dK| reach about 14, where one bf16 output rounding alone is up to 2^-5."""
+    inputs, o, grads, delta = run_bwd(1, 2, 1024, 1024, 64, "bf16", causal, 0.5, seed=20, fused=fused)
+    check(inputs, o, grads, delta, "bf16", causal, 0.5)
+
+
 SHAPES = [
     (1, 1, 128, 128),
     (1, 2, 256, 384),
@@ -122,37 +131,36 @@ SPLIT_SHAPES = [
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("B,H,M,N", SPLIT_SHAPES)
-def test_backward_fused_split_schedule_matches_oracle(monkeypatch, dtype, B, H, M, N):
+def test_backward_fused_split_schedule_matches_oracle(dtype, B, H, M, N):
     """The fused pass's split schedule forced on: every SM an equal share of the (key tile,
     query block) units; a key tile cut by a share boundary gets the partial dK/dV of the SMs
     holding its later query blocks added in by the SM holding its first ones."""
-    monkeypatch.setenv("FA_BWD_SPLIT", "1")
-    inputs, o, grads, delta = run_bwd(B, H, M, N, 64, dtype, False, 0.125, seed=M + N, fused=True)
+    with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 1):
+        inputs, o, grads, delta = run_bwd(B, H, M, N, 64, dtype, False, 0.125, seed=M + N, fused=True)
     check(inputs, o, grads, delta, dtype, False, 0.125)
 
 
-def test_backward_fused_split_agrees_with_whole_tiles(monkeypatch):
+def test_backward_fused_split_agrees_with_whole_tiles():
     """Split and whole key tiles run the same products; dK and dV differ only in the f32
     order in which a cut tile's two sums meet, dQ in the order of its reduce-adds."""
     import torch
     q, k, v, do = synth.attention_inputs(2, 3, 1000, 900, 64, "f16", seed=12, with_dout=True)
     qd, kd, vd, dod = (to_device(x, "f16") for x in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, 0.125, False)
-    monkeypatch.setenv("FA_BWD_SPLIT", "0")
-    a = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False)
-    monkeypatch.setenv("FA_BWD_SPLIT", "1")
-    b = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False)
+    with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 0):
+        a = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False)
+    with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 1):
+        b = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False)
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
     for n in range(3):
         assert float((a[n].float() - b[n].float()).abs().max()) <= 4e-3, n
     assert torch.equal(a[3], b[3])  # delta
 
 
-def test_backward_fused_split_reused_workspace(monkeypatch):
+def test_backward_fused_split_reused_workspace():
     """Three calls on one workspace: the ready flags the previous call left set are cleared by
     the next call's delta kernel before its fused pass reads them."""
     import torch
-    monkeypatch.setenv("FA_BWD_SPLIT", "1")
     B, H, M, N, D = 1, 3, 512, 640, 64
     nbytes = fa.fa_bwd_ws_workspace_bytes(B, H, M, D)
     ws = torch.empty((nbytes // 4,), dtype=torch.float32, device="cuda")
@@ -161,8 +169,33 @@ def test_backward_fused_split_reused_workspace(monkeypatch):
         qd, kd, vd, dod = (to_device(x, "f16") for x in (q, k, v, do))
         o, lse = fa.forward(qd, kd, vd, 0.125, False)
         dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
-        st = fa.fa_bwd_ws(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, nbytes, B, H, M, N, D, 0.125, False, fa.FA_F16)
+        with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 1):
+            st = fa.fa_bwd_ws(qd, kd, vd, o, dod, lse, dq, dk, dv, ws, nbytes, B, H, M, N, D, 0.125, False, fa.FA_F16)
         assert st == fa.FA_OK, fa.fa_last_error_message()
         torch.cuda.synchronize()
         check((q, k, v, do), to_f64(o), (to_f64(dq), to_f64(dk), to_f64(dv)), to_f64(ws[: B * H * M].view(B, H, M)),
               "f16", False, 0.125)
+
+
+NEG_CASES = [
+    # B, H, M, N, D, dtype, causal, scale
+    (1, 2, 384, 300, 64, "f16", False, -0.5),
+    (1, 2, 300, 384, 64, "f16", True, -0.125),
+    (1, 2, 256, 256, 64, "bf16", False, -0.125),
+    (1, 2, 300, 300, 128, "f16", True, -1 / math.sqrt(128)),
+]
+
+
+@FUSED
+@pytest.mark.parametrize("B,H,M,N,D,dtype,causal,scale", NEG_CASES)
+def test_backward_negative_scale(B, H, M, N, D, dtype, causal, scale, fused):
+    """scale < 0: the score products are negated in the tensor core, the exponent uses |scale|
+    and dK, dQ take the signed scale; compared with the oracle's chain rule at that scale."""
+    inputs, o, grads, delta = run_bwd(B, H, M, N, D, dtype, causal, scale, seed=M + 2 * N, fused=fused)
+    check(inputs, o, grads, delta, dtype, causal, scale)
+
+
+def test_backward_negative_scale_split_forced():
+    with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 1):
+        inputs, o, grads, delta = run_bwd(2, 3, 1000, 900, 64, "f16", False, -0.125, seed=9, fused=True)
+    check(inputs, o, grads, delta, "f16", False, -0.125)

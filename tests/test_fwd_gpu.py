@@ -156,22 +156,30 @@ SPLIT_SHAPES = [
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("B,H,M,N", SPLIT_SHAPES)
-def test_forward_split_schedule_matches_oracle(monkeypatch, dtype, B, H, M, N, causal):
+def test_forward_split_schedule_matches_oracle(dtype, B, H, M, N, causal):
     """The split schedule (each SM an equal share of (query pair, key block) units, cut
     pairs merged with the online-softmax rescaling) forced on; causal pairs hold
     different numbers of units."""
-    monkeypatch.setenv("FA_FWD_SPLIT", "1")
     scale = 0.125
-    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, causal, scale, seed=M + N)
+    with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
+        inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, causal, scale, seed=M + N)
     check_heads(inputs, out, lse, dtype, causal, scale)
 
 
-def test_forward_split_schedule_repeated_calls(monkeypatch):
-    """Back-to-back calls reuse one workspace; each launch's flags carry a new epoch."""
-    monkeypatch.setenv("FA_FWD_SPLIT", "1")
+def test_forward_split_schedule_repeated_calls():
+    """Back-to-back calls reuse one workspace; each launch's flags carry a new epoch, and the
+    merging CTAs put the flags they consumed back to zero."""
+    import torch
+    ws = torch.zeros(fa.fa_fwd_workspace_bytes(1, 3, 512, 640, 64, 0, fa.FA_F16), dtype=torch.uint8, device="cuda")
     for seed in (1, 2, 3):
-        inputs, out, lse = run_fwd(1, 3, 512, 640, 64, "f16", False, 0.125, seed=seed)
-        check_heads(inputs, out, lse, "f16", False, 0.125)
+        q, k, v = synth.attention_inputs(1, 3, 512, 640, 64, "f16", seed=seed)
+        with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
+            out, lse = fa.forward(to_device(q, "f16"), to_device(k, "f16"), to_device(v, "f16"), 0.125, False,
+                                  workspace=ws)
+        assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+        check_heads((q, k, v), to_f64(out), to_f64(lse), "f16", False, 0.125)
+        assert int(torch.count_nonzero(ws)) == 0, "flags left set after the merge"
+
 
 
 @pytest.mark.parametrize("causal", [False, True])
@@ -242,13 +250,39 @@ def test_forward_host_buffers_without_lse_and_checks():
         fa.FA_ERR_UNSUPPORTED
 
 
-def test_forward_f32_and_half_splits_share_the_workspace(monkeypatch):
+def test_forward_f32_and_half_splits_share_the_workspace():
     """The cached forward workspace serves, in turn, the f32 key-range split (partial slots and
     epoch-tagged counters, merged by the part that finishes last) and the half-precision split
     schedule (partials and epoch flags); neither is misled by what the other left there, and a
     repeated f32 call is not misled by its own earlier counts."""
-    monkeypatch.setenv("FA_FWD_SPLIT", "1")
     for seed in (1, 2):
         for dtype in ("f32", "f16", "f32"):
-            inputs, out, lse = run_fwd(1, 2, 512, 768, 64, dtype, seed == 2, 0.125, seed=seed)
+            with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
+                inputs, out, lse = run_fwd(1, 2, 512, 768, 64, dtype, seed == 2, 0.125, seed=seed)
             check_heads(inputs, out, lse, dtype, seed == 2, 0.125, rel_l2=REL_L2_F32 if dtype == "f32" else None)
+
+
+NEG_CASES = [
+    # B, H, M, N, D, dtype, causal, scale
+    (1, 2, 300, 200, 64, "f16", False, -0.125),
+    (1, 2, 300, 700, 64, "bf16", True, -0.2),
+    (2, 3, 1000, 900, 64, "f16", False, -0.125),  # split schedule at automatic choice
+    (1, 2, 384, 256, 128, "f16", True, -1 / math.sqrt(128)),
+    (1, 1, 256, 300, 64, "f32", False, -0.125),
+    (1, 1, 5, 700, 64, "f32", True, -0.3),
+    (1, 2, 200, 200, 64, "f16", True, 0.0),        # scale 0: uniform weights over the visible keys
+]
+
+
+@pytest.mark.parametrize("B,H,M,N,D,dtype,causal,scale", NEG_CASES)
+def test_forward_negative_and_zero_scale(B, H, M, N, D, dtype, causal, scale):
+    """Any finite scale: scale < 0 negates the score product in the tensor core (the row maximum
+    is then taken over -q.k) and the exponent uses |scale|; the oracle applies scale as given."""
+    inputs, out, lse = run_fwd(B, H, M, N, D, dtype, causal, scale, seed=7 * M + N)
+    check_heads(inputs, out, lse, dtype, causal, scale, rel_l2=REL_L2_F32 if dtype == "f32" else None)
+
+
+def test_forward_negative_scale_split_forced():
+    with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
+        inputs, out, lse = run_fwd(3, 5, 700, 1500, 64, "f16", False, -0.125, seed=3)
+    check_heads(inputs, out, lse, "f16", False, -0.125)

@@ -90,8 +90,10 @@ def mp_grad(Q, K, V, dO, scale, causal, which, idx):
 
 def pin_brute_forward(impl):
     rng = np.random.default_rng(1)
+    # negative and zero scales too: the library takes any finite scale
     for (M, N, D, causal, scale) in [(3, 4, 2, False, 0.7), (4, 4, 3, True, 0.5), (2, 5, 4, False, 1.9),
-                                     (5, 3, 2, True, 0.3)]:
+                                     (5, 3, 2, True, 0.3), (3, 4, 3, False, -0.9), (4, 4, 2, True, -1.3),
+                                     (2, 3, 2, False, 0.0)]:
         Q, K, V = _rand(rng, M, D), _rand(rng, N, D), _rand(rng, N, D)
         O, L = impl.forward(Q, K, V, scale, causal)
         Om, Lm = mp_forward(Q, K, V, scale, causal)
@@ -104,7 +106,8 @@ def pin_brute_forward(impl):
 
 def pin_brute_backward(impl):
     rng = np.random.default_rng(2)
-    for (M, N, D, causal, scale) in [(3, 3, 2, False, 0.8), (3, 3, 2, True, 0.5), (2, 3, 2, False, 1.3)]:
+    for (M, N, D, causal, scale) in [(3, 3, 2, False, 0.8), (3, 3, 2, True, 0.5), (2, 3, 2, False, 1.3),
+                                     (3, 3, 2, False, -0.6), (3, 3, 2, True, -1.1)]:
         Q, K, V, dO = _rand(rng, M, D), _rand(rng, N, D), _rand(rng, N, D), _rand(rng, M, D)
         dQ, dK, dV = impl.backward(Q, K, V, dO, scale, causal)
         for which, g in (("q", dQ), ("k", dK), ("v", dV)):

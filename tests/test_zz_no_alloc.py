@@ -14,6 +14,7 @@ import math
 import numpy as np
 import pytest
 
+import oracle
 import exact_attention_gb300 as fa
 from exact_attention_gb300 import synth
 
@@ -36,15 +37,18 @@ def _decode_both(B, H, N, D, dtype, ns, seed):
     s = fa.fa_decode_static(qd, kd, vd, out, B, H, N, D, scale, ns, DT[dtype])
     assert s == fa.FA_OK, fa.fa_last_error_message()
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
-    return to_f64(out), to_f64(ref)
+    # the fp64 oracle on the same inputs, head by head
+    want = np.stack([[oracle.decode(synth.to_f64(q[b, h], dtype), synth.to_f64(k[b, h], dtype),
+                                    synth.to_f64(v[b, h], dtype), scale) for h in range(H)] for b in range(B)])
+    return to_f64(out), to_f64(ref), want
 
 
 def test_static_decode_matches_workspace_decode_twice_in_a_row():
     # two different problems back to back through the shared scratch
-    got1, ref1 = _decode_both(2, 4, 3000, 128, "bf16", 16, seed=11)
-    got2, ref2 = _decode_both(1, 3, 777, 64, "f16", 5, seed=12)
-    assert_close(got1, ref1, TOL_O["bf16"], "static decode, first call")
-    assert_close(got2, ref2, TOL_O["f16"], "static decode, second call")
+    got1, ref1, want1 = _decode_both(2, 4, 3000, 128, "bf16", 16, seed=11)
+    got2, ref2, want2 = _decode_both(1, 3, 777, 64, "f16", 5, seed=12)
+    assert_close(got1, want1.reshape(got1.shape), TOL_O["bf16"], "static decode vs oracle, first call")
+    assert_close(got2, want2.reshape(got2.shape), TOL_O["f16"], "static decode vs oracle, second call")
     # the same kernels run on the same data: the results agree exactly
     assert np.array_equal(got1, ref1) and np.array_equal(got2, ref2)
 
