@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
   // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
-  // and dK, dQ take the signed scale
-  const float sl2 = fabsf(scale) * kLog2eB;
+  // (kept above 1e-30, so that masked scores stay -inf when scale = 0) and dK, dQ take the signed scale
+  const float sl2 = fmaxf(fabsf(scale), 1e-30f) * kLog2eB;
   const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
 
   auto item = [&](int w) {
@@ -481,8 +481,8 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
   // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
-  // and dK, dQ take the signed scale
-  const float sl2 = fabsf(scale) * kLog2eB;
+  // (kept above 1e-30, so that masked scores stay -inf when scale = 0) and dK, dQ take the signed scale
+  const float sl2 = fmaxf(fabsf(scale), 1e-30f) * kLog2eB;
   const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
   auto item = [&](int w) {
     BwdItem it;
@@ -906,8 +906,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nkb;
   // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
-  // and dK, dQ take the signed scale
-  const float sl2 = fabsf(scale) * kLog2eB;
+  // (kept above 1e-30, so that masked scores stay -inf when scale = 0) and dK, dQ take the signed scale
+  const float sl2 = fmaxf(fabsf(scale), 1e-30f) * kLog2eB;
   const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
   const bool split = !CAUSAL && part_ws != nullptr;  // the host checks items * nqb < 2^31
   const uint32_t units = split ? static_cast<uint32_t>(items) * static_cast<uint32_t>(nqb) : 0u;
@@ -1459,8 +1459,8 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   const int nkb = (N + kT - 1) / kT, nqb = (M + kT - 1) / kT;
   const int items = BH * nqb;
   // scale < 0: the score product is negated in the tensor core, the exponent scales by |scale|
-  // and dK, dQ take the signed scale
-  const float sl2 = fabsf(scale) * kLog2eB;
+  // (kept above 1e-30, so that masked scores stay -inf when scale = 0) and dK, dQ take the signed scale
+  const float sl2 = fmaxf(fabsf(scale), 1e-30f) * kLog2eB;
   const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
   auto item = [&](int w) {
     BwdItem it;

@@ -123,9 +123,11 @@ __global__ void __launch_bounds__(kThreads32, 1)
   const int nqt = (M + kBM32 - 1) / kBM32;
   const int nkb = (N + kBN32 - 1) / kBN32;
   const int tiles = BH * nqt;
-  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|
+  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|.
+  // |scale| is kept above 1e-30 so that a masked score (-inf) times it stays -inf when scale = 0
+  // (every visible weight is then exp2 of about 0, i.e. 1).
   const bool neg_scale = scale_log2_signed < 0.f;
-  const float scale_log2 = fabsf(scale_log2_signed);
+  const float scale_log2 = fmaxf(fabsf(scale_log2_signed), 1e-30f);
 
   // Unit w = (tile w / parts, part w % parts): the tile's key blocks [jb, jb + nb) of its part.
   // With parts > 1 each part leaves an unnormalised partial and counts itself in on its tile;

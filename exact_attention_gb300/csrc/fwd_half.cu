@@ -127,9 +127,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM);
   const int nkb = (N + kBN - 1) / kBN;
   const int num_tiles = num_pairs * BH;
-  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|
+  // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|.
+  // |scale| is kept above 1e-30 so that a masked score (-inf) times it stays -inf when scale = 0
+  // (every visible weight is then exp2 of about 0, i.e. 1).
   const bool neg_scale = scale_log2_signed < 0.f;
-  const float scale_log2 = fabsf(scale_log2_signed);
+  const float scale_log2 = fmaxf(fabsf(scale_log2_signed), 1e-30f);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {

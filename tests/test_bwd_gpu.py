@@ -199,3 +199,10 @@ def test_backward_negative_scale_split_forced():
     with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 1):
         inputs, o, grads, delta = run_bwd(2, 3, 1000, 900, 64, "f16", False, -0.125, seed=9, fused=True)
     check(inputs, o, grads, delta, "f16", False, -0.125)
+
+
+def test_backward_zero_scale():
+    """scale = 0: every visible key gets the same weight; dK and dQ are exactly zero."""
+    inputs, o, grads, delta = run_bwd(1, 2, 256, 300, 64, "f16", True, 0.0, seed=3, fused=True)
+    check(inputs, o, grads, delta, "f16", True, 0.0)
+    assert np.all(grads[0] == 0) and np.all(grads[1] == 0)

@@ -170,7 +170,10 @@ def test_forward_split_schedule_repeated_calls():
     """Back-to-back calls reuse one workspace; each launch's flags carry a new epoch, and the
     merging CTAs put the flags they consumed back to zero."""
     import torch
-    ws = torch.zeros(fa.fa_fwd_workspace_bytes(1, 3, 512, 640, 64, 0, fa.FA_F16), dtype=torch.uint8, device="cuda")
+    nbytes = fa.fa_fwd_workspace_bytes(1, 3, 512, 640, 64, 0, fa.FA_F16)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    flags = ws[nbytes - sms * 8 * 4:]  # eight 32-bit flags per SM end the workspace
     for seed in (1, 2, 3):
         q, k, v = synth.attention_inputs(1, 3, 512, 640, 64, "f16", seed=seed)
         with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
@@ -178,7 +181,7 @@ def test_forward_split_schedule_repeated_calls():
                                   workspace=ws)
         assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
         check_heads((q, k, v), to_f64(out), to_f64(lse), "f16", False, 0.125)
-        assert int(torch.count_nonzero(ws)) == 0, "flags left set after the merge"
+        assert int(torch.count_nonzero(flags)) == 0, "flags left set after the merge"
 
 
 
@@ -286,3 +289,24 @@ def test_forward_negative_scale_split_forced():
     with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
         inputs, out, lse = run_fwd(3, 5, 700, 1500, 64, "f16", False, -0.125, seed=3)
     check_heads(inputs, out, lse, "f16", False, -0.125)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("D", [64, 128])
+def test_forward_rising_scores_rescale(dtype, causal, D):
+    """Scores that rise along the keys: each key block's scores sit above the running maximum by
+    far more than 2^8 in the exponent, and a block's second half above its first, so the halves
+    formed against the running maximum overflow and are formed again after a rescale (both the
+    first-half and the second-half paths), every block."""
+    rng = np.random.default_rng(5)
+    B, H, M, N = 1, 2, 512, 1024
+    u = np.ones(D, dtype=np.float32) / np.sqrt(D)
+    q = rng.standard_normal((B, H, M, D), dtype=np.float32) + 2.0 * u
+    k = rng.standard_normal((B, H, N, D), dtype=np.float32) + (0.2 * np.arange(N, dtype=np.float32))[:, None] * u
+    v = rng.standard_normal((B, H, N, D), dtype=np.float32)
+    q, k, v = (synth.round_f32(x.astype(np.float32), dtype) for x in (q, k, v))
+    scale = 1.0 / math.sqrt(D)
+    out, lse = fa.forward(to_device(q, dtype), to_device(k, dtype), to_device(v, dtype), scale, causal)
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    check_heads((q, k, v), to_f64(out), to_f64(lse), dtype, causal, scale)
