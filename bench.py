@@ -728,6 +728,7 @@ def run_reference(args):
 PROFILE_CASES = {
     # inputs larger than L2 (129 MB) so DRAM counters mean something, a few GB at most
     "fwd": dict(B=16, H=16, M=4096, N=4096, D=64, dtype="f16"),     # Q/K/V 0.4 GB
+    "fwd_bench": dict(B=4, H=12, M=2048, N=2048, D=64, dtype="f16"),  # the headline workload itself
     "decode": dict(B=8, H=8, N=32768, D=128, n_splits=64, dtype="bf16"),  # K/V 1.07 GB
     "bwd": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # Q/K/V/O/dO 0.34 GB (fused pass)
     "bwd3": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # the same through the three kernels
@@ -745,7 +746,7 @@ def run_profile(kind: str, launches: int = 5):
     torch.cuda.set_device(0)
     g = torch.Generator(device="cuda").manual_seed(0)
     c = PROFILE_CASES[kind]
-    if kind == "fwd":
+    if kind in ("fwd", "fwd_bench"):
         shp = (c["B"], c["H"], c["M"], c["D"])
         q = torch.randn(shp, generator=g, device="cuda").half()
         k = torch.randn(shp, generator=g, device="cuda").half()

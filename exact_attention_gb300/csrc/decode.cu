@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_split_kernel(const typenam
       int issued = 0;
       // test-only fault injection: the first CTA never fills its first stage, so its consumers'
       // bounded wait runs out and the launch reports a timeout (no fault, no trap)
-      const bool skip_first = inject == 1 && blockIdx.x == 0 && blockIdx.y == 0;
+      const bool skip_first = inject == kInjectDecodeStage && blockIdx.x == 0 && blockIdx.y == 0;
       for (int it = 0; it < nstage; ++it) {
         const int st = it % kDecStages;
         const uint32_t ph = static_cast<uint32_t>(it / kDecStages) & 1u;

@@ -245,7 +245,16 @@ uint32_t next_epoch() {
   if (e == 0u) e = epoch.fetch_add(1u) + 1u;
   return e;
 }
-std::atomic<int> g_inject{0};  // fa_debug_inject: consumed by the next decode launch
+std::atomic<int> g_inject{0};  // fa_debug_inject: consumed by the next launch of the kind it names
+
+// The pending injection if it is one of `a` or `b` (and then it is consumed), else 0.
+int take_inject(int a, int b) {
+  int k = g_inject.load();
+  while ((k == a || k == b) && k != 0) {
+    if (g_inject.compare_exchange_weak(k, 0)) return k;
+  }
+  return 0;
+}
 
 // fa_decode / fa_decode_ex: R query rows per (batch, head), each against all N keys.
 fa_status decode_impl(const void* q, const void* Kcache, const void* Vcache, void* O, float* LSE, float* partial_ws,
@@ -270,7 +279,7 @@ fa_status decode_impl(const void* q, const void* Kcache, const void* Vcache, voi
   if (LSE != nullptr) FA_TRY(check_ptr(LSE, "LSE"));
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
-  ctx.inject = g_inject.exchange(0);
+  ctx.inject = take_inject(kInjectDecodeStage, 0);
   cudaError_t e = launch_decode(q, Kcache, Vcache, O, LSE, partial_ws, B * H, R, N, D, scale, n_splits, dtype, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
@@ -292,6 +301,7 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
   if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return fail(FA_ERR_INVALID, "LSE misaligned");
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
+  if (D == 64 && dtype != FA_F32) ctx.inject = take_inject(kInjectFwdStage, kInjectFwdFlag);
   FwdSplit sp{};
   if (ws != nullptr && split_capable(D, dtype)) {
     FA_TRY(check_ptr(ws, "workspace"));
@@ -410,7 +420,7 @@ fa_status fa_set_schedule(fa_sched_key key, int value) {
 }
 
 fa_status fa_debug_inject(int kind) {
-  if (kind != 0 && kind != 1) return fail(FA_ERR_INVALID, "unknown fault-injection kind %d", kind);
+  if (kind < 0 || kind > kInjectFwdFlag) return fail(FA_ERR_INVALID, "unknown fault-injection kind %d", kind);
   g_inject.store(kind);
   return FA_OK;
 }

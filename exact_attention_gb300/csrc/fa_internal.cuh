@@ -35,6 +35,11 @@ enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
 inline size_t dtype_size(int dt) { return dt == kF32 ? 4u : 2u; }
 
+// Test-only fault injections (fa_debug_inject): which launch they reach and what it skips.
+constexpr int kInjectDecodeStage = 1;  // decode: CTA 0 never loads its first stage of keys
+constexpr int kInjectFwdStage = 2;     // D = 64 forward: CTA 0 never loads its first K/V stage
+constexpr int kInjectFwdFlag = 3;      // D = 64 forward, split schedule: CTA 1 never publishes its partial
+
 // Per-launch context every kernel receives.
 struct LaunchCtx {
   DevStatus* status;

@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_d64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, float* __restrict__ LSE, int BH,
                    int M, int N, float scale_log2_signed, float* __restrict__ ws, uint32_t* __restrict__ flags, uint32_t epoch,
-                   DevStatus* status, unsigned long long budget_ns) {
+                   DevStatus* status, unsigned long long budget_ns, int inject) {
   extern __shared__ uint8_t smem_raw[];
   Hdr* hdr = reinterpret_cast<Hdr*>(smem_raw);
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
@@ -273,6 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t kv_it = 0;
+      const bool skip_first = inject == kInjectFwdStage && blockIdx.x == 0;
       int it = 0;
       bool ok = true;
       Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
@@ -291,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          // test-only fault injection: the first CTA never fills the first stage of K/V, so the
+          // waits on it run out and the launch reports a timeout (no fault, no trap)
+          if (kv_it == 0 && skip_first) continue;
           const uint32_t f = ptx::smem_u32(&hdr->kv_full[st]);
           ptx::mbar_arrive_expect_tx(f, 2 * kTile);
           ptx::tma_load_3d(k_addr(st), &tmK, f, 0, (ti.jb + j) * kBN, ti.bh);
@@ -299,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (hdr->abort_flag) {  // let issued copies land before shared memory is released
         for (uint32_t k = kv_it > (uint32_t)kStages ? kv_it - kStages : 0u; k < kv_it; ++k) {
-          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->kv_full[k % kStages]), (k / kStages) & 1u, 100000000ull);
+          if (!(k == 0 && skip_first))
+            ptx::mbar_wait_drain(ptx::smem_u32(&hdr->kv_full[k % kStages]), (k / kStages) & 1u, 100000000ull);
         }
       }
     }
@@ -414,7 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the softmax warps' partial writes were ordered before their epi arrivals, which this
           // thread has observed: a gpu-scope release from here publishes them (cumulativity)
           __threadfence();
-          for (int w = 0; w < 8; ++w) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + w, epoch);
+          // (test-only fault injection: CTA 1 never publishes, so the CTA merging its partial
+          // gives up its bounded wait on the flags and the launch reports a timeout)
+          if (!(inject == kInjectFwdFlag && blockIdx.x == 1))
+            for (int w = 0; w < 8; ++w) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + w, epoch);
         } else {
           ptx::bulk_wait_read();  // both stores have read the buffer
         }
@@ -687,11 +695,11 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, BH, M, N, scale * kLog2e, sp.ws, sp.flags, sp.epoch,
-                              ctx.status, ctx.wait_budget_ns);
+                              ctx.status, ctx.wait_budget_ns, ctx.inject);
   }
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
   kern<<<grid, kThreads, kSmemBytes, ctx.stream>>>(mq, mk, mv, mo, LSE, BH, M, N, scale * kLog2e, nullptr, nullptr, 0u,
-                                                   ctx.status, ctx.wait_budget_ns);
+                                                   ctx.status, ctx.wait_budget_ns, ctx.inject);
   return cudaGetLastError();
 }
 

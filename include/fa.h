@@ -342,12 +342,18 @@ fa_status fa_set_schedule(fa_sched_key key, int value);
 
 /*
  * Test-only fault injection (no counterpart on the pages; exercises the bounded
- * waits described at fa_set_wait_budget_ns). kind 1: in the next fa_decode /
- * fa_decode_static launch the first CTA never loads its first stage of keys, so
- * its compute warps' bounded wait runs out, the CTA drains and exits, and
- * fa_last_status reports FA_ERR_TIMEOUT naming the decode kernel and wait site.
- * Nothing faults and the context stays usable. One-shot: the next decode launch
- * consumes it. kind 0 cancels a pending injection. Other kinds: FA_ERR_INVALID.
+ * waits described at fa_set_wait_budget_ns). One-shot: the next launch of the
+ * kind named consumes it; kind 0 cancels a pending injection; other kinds are
+ * FA_ERR_INVALID. In each case a bounded wait runs out, the CTAs drain and exit,
+ * and fa_last_status reports FA_ERR_TIMEOUT naming the kernel and the wait site;
+ * nothing faults and the context stays usable.
+ *   1  next fa_decode / fa_decode_static launch: its first CTA never loads its
+ *      first stage of keys (a wait inside one CTA)
+ *   2  next fp16/bf16 D = 64 forward: its first CTA never loads its first stage
+ *      of K/V (waits inside one CTA)
+ *   3  next fp16/bf16 D = 64 forward on the split schedule: CTA 1 never
+ *      publishes the partial of its first piece, so the CTA that merges it
+ *      gives up its wait on CTA 1's flags (a wait between CTAs)
  */
 fa_status fa_debug_inject(int kind);
 

@@ -44,3 +44,47 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
     ref = oracle.decode(f64(q, "bf16"), f64(k, "bf16"), f64(v, "bf16"), scale)
     assert_close(to_f64(out), ref, TOL_O["bf16"], "decode after the injected timeout")
+
+
+def _forward_after_timeout(B, H, M, N, kind, split):
+    """Arms injection `kind`, runs one forward with a 20 ms wait budget, returns the status and its
+    message; then runs the same forward normally and checks it against the oracle."""
+    q, k, v = synth.attention_inputs(B, H, M, N, 64, "f16", seed=kind)
+    qd, kd, vd = to_device(q, "f16"), to_device(k, "f16"), to_device(v, "f16")
+    assert fa.fa_set_wait_budget_ns(20_000_000) == fa.FA_OK
+    try:
+        assert fa.fa_debug_inject(kind) == fa.FA_OK
+        with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1 if split else 0):
+            fa.forward(qd, kd, vd, 0.125, False)
+        status = fa.fa_last_status()
+        msg = fa.fa_last_error_message()
+        assert fa.fa_last_status() == fa.FA_OK  # reading the status word cleared it
+    finally:
+        fa.fa_debug_inject(0)
+        fa.fa_set_wait_budget_ns(DEFAULT_BUDGET_NS)
+    with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1 if split else 0):
+        out, lse = fa.forward(qd, kd, vd, 0.125, False)
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        ro, _ = oracle.forward(f64(q[b, h], "f16"), f64(k[b, h], "f16"), f64(v[b, h], "f16"), 0.125, False)
+        assert_close(to_f64(out)[b, h], ro, TOL_O["f16"], f"forward after the injected timeout [{b},{h}]")
+    return status, msg
+
+
+def test_forward_stage_wait_times_out_and_context_survives():
+    """A wait inside one CTA: the first CTA's first K/V stage is never loaded, so the MMA issuers'
+    and softmax warps' bounded waits on it run out."""
+    status, msg = _forward_after_timeout(1, 2, 512, 512, 2, split=False)
+    assert status == fa.FA_ERR_TIMEOUT, (status, msg)
+    assert "kernel fwd " in msg and "block 0" in msg, msg
+
+
+def test_forward_split_flag_wait_times_out_and_context_survives():
+    """A wait between CTAs: on the split schedule CTA 1 never publishes the partial of its first
+    piece (a later part of a pair CTA 0 finishes), so CTA 0's softmax warps wait on its flags (wait
+    site 36) and CTA 0's epilogue warp waits on them (site 37); whichever budget runs out first is
+    the one reported, in block 0."""
+    status, msg = _forward_after_timeout(4, 12, 2048, 2048, 3, split=True)
+    assert status == fa.FA_ERR_TIMEOUT, (status, msg)
+    assert "kernel fwd " in msg and "block 0" in msg, msg
+    assert "wait site 36 " in msg or "wait site 37 " in msg, msg
