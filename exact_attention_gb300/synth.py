@@ -105,3 +105,9 @@ def decode_inputs(B: int, H: int, N: int, D: int, dtype: str, seed: int = 0):
     for b, h, kh, vh in iter_decode_heads(B, H, N, D, dtype, seed, workers=1 if B * H * N < (1 << 20) else 0):
         k[b, h], v[b, h] = kh, vh
     return q, k, v
+
+
+def hadamard_signs(d: int, seed: int = 0) -> np.ndarray:
+    """d random signs (+1 / -1 as int8) for the FP8 path's incoherent processing."""
+    rng = np.random.default_rng([seed, 0x5167])
+    return np.where(rng.integers(0, 2, size=d) == 1, 1, -1).astype(np.int8)

@@ -12,9 +12,14 @@ the full score matrix, a max-subtracted softmax, and the textbook chain rule
 for the gradients. See ``oracle.attention`` for the functions and the passage
 each one follows.
 
-Parity pins (``tests/test_oracle.py``): high-precision brute force on tiny
-inputs (forward values and mpmath derivatives of the backward), closed forms,
-invariants and finite differences. No function here is "parity unpinned".
+``oracle.fp8`` writes out the FP8 forward's steps (Hadamard-times-sign
+transform, E4M3 block quantisation) in float64 for the FP8 path's tests.
+
+Parity pins (``tests/test_oracle.py``, ``tests/test_oracle_fp8.py``): high-precision
+brute force on tiny inputs (forward values and mpmath derivatives of the backward),
+closed forms, invariants and finite differences; for the FP8 steps a brute-force
+E4M3 rounding, PyTorch's float8 conversion, the transform's orthogonality and the
+FP8 error against exact attention. No function here is "parity unpinned".
 """
 from .attention import (  # noqa: F401
     scores,
