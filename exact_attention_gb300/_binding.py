@@ -29,6 +29,8 @@ EXPORTS = (
     "fa_fwd_workspace_bytes",
     "fa_fwd_host",
     "fa_fwd_host_workspace_bytes",
+    "fa_fwd_fp8",
+    "fa_fwd_fp8_workspace_bytes",
     "fa_bwd",
     "fa_bwd_workspace_bytes",
     "fa_bwd_ws",
@@ -87,6 +89,10 @@ def lib() -> ctypes.CDLL:
     L.fa_bwd_ws_workspace_bytes.restype = ctypes.c_size_t
     L.fa_fwd_host.argtypes = [vp] * 6 + [ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
     L.fa_fwd_host.restype = st
+    L.fa_fwd_fp8.argtypes = [vp] * 7 + [ctypes.c_size_t, i, i, i, i, i, f, i, i, vp]
+    L.fa_fwd_fp8.restype = st
+    L.fa_fwd_fp8_workspace_bytes.argtypes = [i, i, i, i, i]
+    L.fa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
     L.fa_fwd_host_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
     L.fa_fwd_host_workspace_bytes.restype = ctypes.c_size_t
     L.fa_decode_ex.argtypes = [vp] * 6 + [i, i, i, i, i, f, i, i, vp]
@@ -160,6 +166,17 @@ def fa_fwd_host(hQ, hK, hV, hO, hLSE, dev_ws, dev_ws_bytes, B, H, M, N, D, scale
 
 def fa_fwd_host_workspace_bytes(B, H, M, N, D, causal, dtype) -> int:
     return lib().fa_fwd_host_workspace_bytes(B, H, M, N, D, int(causal), int(dtype))
+
+
+def fa_fwd_fp8(Q, K, V, O, LSE, signs, workspace, workspace_bytes, B, H, M, N, D, scale, causal, dtype,
+               stream=None) -> int:
+    return lib().fa_fwd_fp8(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), _ptr(signs), _ptr(workspace),
+                            int(workspace_bytes), B, H, M, N, D, float(scale), int(causal), int(dtype),
+                            _stream(stream))
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, M, N, D) -> int:
+    return lib().fa_fwd_fp8_workspace_bytes(B, H, M, N, D)
 
 
 
@@ -293,6 +310,24 @@ def forward(q, k, v, scale: float, causal: bool = False, out=None, lse=None, str
     _check(fa_fwd_ws(q, k, v, out, lse, ws, ws.numel() * ws.element_size(), B, H, M, N, D, scale, causal, dt, stream),
            "fa_fwd_ws")
     return out, lse
+
+
+def forward_fp8(q, k, v, scale: float, causal: bool, signs, out=None, lse=None, workspace=None, stream=None):
+    """O, LSE of the FP8 forward (D = 64); signs: a device int8 tensor of 64 entries +-1. Returns
+    (O, LSE, workspace); the workspace holds the E4M3 operands and their scales afterwards."""
+    import torch
+    B, H, M, D = _dims4(q, "q")
+    N = _dims4(k, "k")[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, M), dtype=torch.float32, device=q.device)
+    nbytes = fa_fwd_fp8_workspace_bytes(B, H, M, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=q.device)
+    _check(fa_fwd_fp8(q, k, v, out, lse, signs, workspace, workspace.numel(), B, H, M, N, D, scale, causal,
+                      fa_dtype(q), stream), "fa_fwd_fp8")
+    return out, lse, workspace
 
 
 def backward(q, k, v, o, do, lse, scale: float, causal: bool = False, stream=None, fused: bool = True):

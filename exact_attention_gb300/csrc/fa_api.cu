@@ -145,6 +145,11 @@ fa_status check_scale(float scale) {
 
 bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
                   uint32_t box_inner, uint32_t box_rows) {
+  return make_tmap_3d_ex(map, base, dtype, inner, rows, outer, box_inner, box_rows, 128);
+}
+
+bool make_tmap_3d_ex(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
+                     uint32_t box_inner, uint32_t box_rows, int swizzle_bytes) {
   if (g_encode == nullptr) {
     std::lock_guard<std::mutex> lock(g_mutex);
     if (g_encode == nullptr) {
@@ -157,17 +162,18 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner,
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
   }
-  const size_t es = dtype_size(dtype);
+  const size_t es = dtype == kU8 ? 1u : dtype_size(dtype);
   CUtensorMapDataType t = dtype == kF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                           : dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                          : dtype == kU8  ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   cuuint64_t dims[3] = {inner, rows, outer};
   cuuint64_t strides[2] = {inner * es, inner * rows * es};
   cuuint32_t box[3] = {box_inner, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = g_encode(map, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -512,6 +518,77 @@ fa_status fa_decode_ex(const void* q, const void* Kcache, const void* Vcache, vo
                      "fa_decode_ex");
 }
 
+// ---------------------------------------------------------------------------
+// FP8 forward: the workspace holds the E4M3 operands and their scales (see Fp8Ws).
+namespace {
+struct Fp8Layout {
+  size_t q8, k8, vt8, sq, sk, vmax, sv, total;
+  int npad;
+};
+Fp8Layout fp8_layout(int B, int H, int M, int N) {
+  const size_t BH = static_cast<size_t>(B) * H;
+  const size_t nqb = (static_cast<size_t>(M) + 127) / 128, nkb = (static_cast<size_t>(N) + 127) / 128;
+  auto a256 = [](size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); };
+  Fp8Layout L{};
+  L.npad = (N + 15) / 16 * 16;
+  L.q8 = 0;
+  L.k8 = L.q8 + a256(BH * M * 64);
+  L.vt8 = L.k8 + a256(BH * N * 64);
+  L.sq = L.vt8 + a256(BH * 64 * static_cast<size_t>(L.npad));
+  L.sk = L.sq + a256(BH * nqb * 4);
+  L.vmax = L.sk + a256(BH * nkb * 4);
+  L.sv = L.vmax + a256(BH * nkb * 4);
+  L.total = L.sv + a256(BH * 4);
+  return L;
+}
+}  // namespace
+
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int M, int N, int D) {
+  if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || D != 64) return 0;
+  return fp8_layout(B, H, M, N).total;
+}
+
+fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const signed char* signs,
+                     void* workspace, size_t workspace_bytes, int B, int H, int M, int N, int D, float scale,
+                     int causal, fa_dtype dtype, void* stream) {
+  FA_TRY(check_dtype(dtype));
+  FA_TRY(check_sizes(B, H, M, N, D));
+  if (dtype == FA_F32) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8: inputs must be FA_F16 or FA_BF16");
+  if (D != 64) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8: head dimension D=%d (supported: 64)", D);
+  FA_TRY(check_scale(scale));
+  if (B * H == 0 || M == 0) return FA_OK;
+  if (N == 0) return fail(FA_ERR_INVALID, "N = 0: softmax over an empty key set");
+  if (B * H > 65535) return fail(FA_ERR_UNSUPPORTED, "fa_fwd_fp8: B*H=%d above 65535", B * H);
+  FA_TRY(check_ptr(Q, "Q"));
+  FA_TRY(check_ptr(K, "K"));
+  FA_TRY(check_ptr(V, "V"));
+  FA_TRY(check_ptr(O, "O"));
+  if (signs == nullptr) return fail(FA_ERR_INVALID, "signs is NULL");
+  if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return fail(FA_ERR_INVALID, "LSE misaligned");
+  FA_TRY(check_ptr(workspace, "workspace"));
+  const Fp8Layout L = fp8_layout(B, H, M, N);
+  if (workspace_bytes < L.total)
+    return fail(FA_ERR_INVALID, "fa_fwd_fp8: workspace of %zu bytes, %zu needed", workspace_bytes, L.total);
+  LaunchCtx ctx{};
+  FA_TRY(make_ctx(&ctx, stream));
+  char* ws = static_cast<char*>(workspace);
+  Fp8Ws w{};
+  w.q8 = reinterpret_cast<uint8_t*>(ws + L.q8);
+  w.k8 = reinterpret_cast<uint8_t*>(ws + L.k8);
+  w.vt8 = reinterpret_cast<uint8_t*>(ws + L.vt8);
+  w.sq = reinterpret_cast<float*>(ws + L.sq);
+  w.sk = reinterpret_cast<float*>(ws + L.sk);
+  w.vmax = reinterpret_cast<float*>(ws + L.vmax);
+  w.sv = reinterpret_cast<float*>(ws + L.sv);
+  w.npad = L.npad;
+  cudaError_t e = launch_fp8_quant(Q, K, V, reinterpret_cast<const int8_t*>(signs), w, B * H, M, N, dtype, ctx.stream);
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8: quantisation launch");
+  e = launch_fwd_fp8(w, O, LSE, B * H, M, N, scale, causal != 0, dtype, ctx);
+  if (e == cudaErrorInvalidValue) return fail(FA_ERR_CUDA, "fa_fwd_fp8: TMA descriptor rejected by the driver");
+  if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_fp8");
+  return FA_OK;
+}
+
 fa_status fa_last_status(void* stream) {
   DevState* st = nullptr;
   FA_TRY(device_state(&st));
@@ -525,8 +602,8 @@ fa_status fa_last_status(void* stream) {
   e = cudaMemcpy(st->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the status word");
   static const char* names[] = {"?", "fwd", "fwd_f32", "bwd_delta", "bwd_dkdv", "bwd_dq", "decode_split",
-                                "decode_combine"};
-  const char* kn = h.kernel < 8 ? names[h.kernel] : "?";
+                                "decode_combine", "fwd_fp8"};
+  const char* kn = h.kernel < 9 ? names[h.kernel] : "?";
   if (h.code == kStatusTimeout)
     return fail(FA_ERR_TIMEOUT, "kernel %s gave up wait site %u in block %u", kn, h.site, h.block);
   return fail(FA_ERR_CUDA, "kernel %s reported status %u (site %u, block %u)", kn, h.code, h.site, h.block);

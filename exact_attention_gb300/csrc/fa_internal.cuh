@@ -28,10 +28,12 @@ enum KernelId : unsigned int {
   kKernBwdDq = 5,
   kKernDecodeSplit = 6,
   kKernDecodeCombine = 7,
+  kKernFwdFp8 = 8,
 };
 
-// Numeric storage types, same values as the C ABI's fa_dtype.
-enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+// Numeric storage types, same values as the C ABI's fa_dtype; kU8 (bytes: the FP8 path's E4M3
+// operands) is internal.
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2, kU8 = 3 };
 
 inline size_t dtype_size(int dt) { return dt == kF32 ? 4u : 2u; }
 
@@ -80,6 +82,20 @@ cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O,
                            int D, float scale, bool causal, int parts, float* ws, uint32_t epoch,
                            const LaunchCtx& ctx);
 
+// The FP8 forward's workspace (head dimension 64): E4M3 copies of Q [BH][M][64] and K
+// [BH][N][64] after the Hadamard-times-sign transform, V transposed [BH][64][npad] (npad = N
+// rounded up to 16), the per-block scales sq [BH][ceil(M/128)] and sk [BH][ceil(N/128)], V's
+// per-block maxima vmax [BH][ceil(N/128)] and per-head scale sv [BH].
+struct Fp8Ws {
+  uint8_t *q8, *k8, *vt8;
+  float *sq, *sk, *vmax, *sv;
+  int npad;
+};
+cudaError_t launch_fp8_quant(const void* Q, const void* K, const void* V, const int8_t* signs, const Fp8Ws& w, int BH,
+                             int M, int N, int dtype, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(const Fp8Ws& w, void* O, float* LSE, int BH, int M, int N, float scale, bool causal,
+                           int dtype, const LaunchCtx& ctx);
+
 // Split schedule of the fused backward (non-causal, D = 64): ws holds bwd_fused_split_bytes of
 // partial dK/dV slots (two per SM) then num_sms * 8 counters; ws == nullptr runs whole key tiles.
 struct BwdSplit {
@@ -107,5 +123,9 @@ fa_status cuda_fail_msg(cudaError_t e, const char* what);
 
 bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
                   uint32_t box_inner, uint32_t box_rows);
+// The same with the swizzle span chosen: 128 or 64 bytes (the box's inner extent in bytes
+// must not exceed it).
+bool make_tmap_3d_ex(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
+                     uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
 
 }  // namespace fa

@@ -1,0 +1,200 @@
+// Quantisation of the FP8 forward's operands ("Flash Attention" notes, section
+// "FlashAttention 3", the FP8 bullets): incoherent processing of Q and K with the
+// Hadamard-times-sign matrix M = diag(signs) H / 8 (d = 64), then E4M3 with one scale per
+// 128-row block; V with one scale per (batch, head), written transposed ([d][keys]) so that
+// it serves as the K-major operand of P V.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "fa_internal.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+namespace {
+
+constexpr int kD8 = 64;
+constexpr int kRowsPerBlock = 128;
+constexpr float kE4M3Max = 448.f;
+
+template <bool BF16>
+__device__ __forceinline__ float half_to_f32(uint16_t h) {
+  return BF16 ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
+}
+
+// One 64-element row of a half-precision tensor (zeros past `rows`).
+template <bool BF16>
+__device__ __forceinline__ void load_row(const uint16_t* src, int row, int rows, float* x) {
+  if (row >= rows) {
+#pragma unroll
+    for (int d = 0; d < kD8; ++d) x[d] = 0.f;
+    return;
+  }
+  const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * kD8);
+#pragma unroll
+  for (int c = 0; c < kD8 / 8; ++c) {
+    const uint4 v = p[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[8 * c + 2 * i] = half_to_f32<BF16>(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      x[8 * c + 2 * i + 1] = half_to_f32<BF16>(static_cast<uint16_t>(w[i] >> 16));
+    }
+  }
+}
+
+// Largest value of v over the CTA's 128 threads (all threads get it).
+__device__ __forceinline__ float block_max128(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  v = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  __syncthreads();
+  return v;
+}
+
+// 64 values times `inv`, rounded to E4M3, stored as 64 bytes at dst (16-byte aligned).
+__device__ __forceinline__ void store_e4m3_row(uint8_t* dst, const float* x, float inv) {
+  uint32_t w[16];
+#pragma unroll
+  for (int p = 0; p < 16; ++p)
+    w[p] = ptx::pack_e4m3x2(x[4 * p] * inv, x[4 * p + 1] * inv) |
+           (ptx::pack_e4m3x2(x[4 * p + 2] * inv, x[4 * p + 3] * inv) << 16);
+  uint4* o = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) o[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+// Q (blockIdx.z = 0) or K (1): one CTA per 128-row block of one head, one row per thread.
+// x -> x diag(signs) H / 8 by a fast Walsh-Hadamard transform in registers, then the block's
+// scale = amax / 448 and the E4M3 row.
+template <bool BF16>
+__global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __restrict__ Q,
+                                                           const uint16_t* __restrict__ K,
+                                                           const int8_t* __restrict__ signs, uint8_t* __restrict__ Q8,
+                                                           uint8_t* __restrict__ K8, float* __restrict__ sq,
+                                                           float* __restrict__ sk, int M, int N) {
+  __shared__ float red[4];
+  const bool isk = blockIdx.z == 1;
+  const int rows = isk ? N : M;
+  const int nblk = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (static_cast<int>(blockIdx.x) >= nblk) return;  // the grid covers the longer of the two
+  const size_t bh = blockIdx.y;
+  const uint16_t* src = (isk ? K : Q) + bh * static_cast<size_t>(rows) * kD8;
+  const int row = static_cast<int>(blockIdx.x) * kRowsPerBlock + static_cast<int>(threadIdx.x);
+  float x[kD8];
+  load_row<BF16>(src, row, rows, x);
+#pragma unroll
+  for (int d = 0; d < kD8; ++d)
+    if (__ldg(signs + d) < 0) x[d] = -x[d];
+#pragma unroll
+  for (int h = 1; h < kD8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < kD8; ++i) {
+      if ((i & h) == 0) {
+        const float a = x[i], b = x[i + h];
+        x[i] = a + b;
+        x[i + h] = a - b;
+      }
+    }
+  }
+  float am = 0.f;
+#pragma unroll
+  for (int d = 0; d < kD8; ++d) {
+    x[d] *= 0.125f;  // 1 / sqrt(64), exact
+    am = fmaxf(am, fabsf(x[d]));
+  }
+  am = block_max128(am, red);
+  const float scale = am > 0.f ? am / kE4M3Max : 1.f;
+  const float inv = am > 0.f ? kE4M3Max / am : 1.f;
+  if (threadIdx.x == 0) (isk ? sk : sq)[bh * nblk + blockIdx.x] = scale;
+  if (row < rows) store_e4m3_row((isk ? K8 : Q8) + (bh * rows + row) * kD8, x, inv);
+}
+
+// Largest |V| of each 128-key block of each head.
+template <bool BF16>
+__global__ void __launch_bounds__(128) fp8_v_amax_kernel(const uint16_t* __restrict__ V, float* __restrict__ vmax,
+                                                         int N) {
+  __shared__ float red[4];
+  const int nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+  const size_t bh = blockIdx.y;
+  float x[kD8];
+  load_row<BF16>(V + bh * static_cast<size_t>(N) * kD8, static_cast<int>(blockIdx.x) * kRowsPerBlock + threadIdx.x, N, x);
+  float am = 0.f;
+#pragma unroll
+  for (int d = 0; d < kD8; ++d) am = fmaxf(am, fabsf(x[d]));
+  am = block_max128(am, red);
+  if (threadIdx.x == 0) vmax[bh * nkb + blockIdx.x] = am;
+}
+
+// V of one 128-key block quantised with its head's scale and written transposed:
+// Vt8[bh][d][key], rows of Npad bytes (keys past N are zero).
+template <bool BF16>
+__global__ void __launch_bounds__(128) fp8_v_quant_kernel(const uint16_t* __restrict__ V,
+                                                          const float* __restrict__ vmax, uint8_t* __restrict__ Vt8,
+                                                          float* __restrict__ sv, int N, int Npad) {
+  __shared__ float tile[kRowsPerBlock][kD8 + 1];
+  __shared__ float red[4];
+  const int nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+  const size_t bh = blockIdx.y;
+  const int k0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
+  float am = 0.f;
+  for (int i = threadIdx.x; i < nkb; i += blockDim.x) am = fmaxf(am, vmax[bh * nkb + i]);
+  am = block_max128(am, red);
+  const float scale = am > 0.f ? am / kE4M3Max : 1.f;
+  const float inv = am > 0.f ? kE4M3Max / am : 1.f;
+  if (blockIdx.x == 0 && threadIdx.x == 0) sv[bh] = scale;
+  // the block's 128 x 64 values (contiguous in memory) into shared memory, 16 bytes per load
+  const uint16_t* src = V + (bh * static_cast<size_t>(N) + k0) * kD8;
+  for (int c = threadIdx.x; c < kRowsPerBlock * kD8 / 8; c += blockDim.x) {
+    const int key = c / (kD8 / 8), d0 = (c % (kD8 / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (k0 + key < N) v = reinterpret_cast<const uint4*>(src)[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      tile[key][d0 + 2 * i] = half_to_f32<BF16>(static_cast<uint16_t>(w[i] & 0xFFFFu));
+      tile[key][d0 + 2 * i + 1] = half_to_f32<BF16>(static_cast<uint16_t>(w[i] >> 16));
+    }
+  }
+  __syncthreads();
+  // thread t writes column d = t / 2 for keys [64 (t % 2), 64 (t % 2) + 64) of the block
+  const int d = threadIdx.x >> 1, kh = (threadIdx.x & 1) * 64;
+  float x[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) x[i] = tile[kh + i][d];
+  uint8_t* dst = Vt8 + (bh * kD8 + d) * static_cast<size_t>(Npad) + k0 + kh;
+  uint32_t w[16];
+#pragma unroll
+  for (int p = 0; p < 16; ++p)
+    w[p] = ptx::pack_e4m3x2(x[4 * p] * inv, x[4 * p + 1] * inv) |
+           (ptx::pack_e4m3x2(x[4 * p + 2] * inv, x[4 * p + 3] * inv) << 16);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (k0 + kh + 16 * c < Npad)
+      reinterpret_cast<uint4*>(dst)[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quant(const void* Q, const void* K, const void* V, const int8_t* signs, const Fp8Ws& w, int BH,
+                             int M, int N, int dtype, cudaStream_t stream) {
+  const int nqb = (M + kRowsPerBlock - 1) / kRowsPerBlock, nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+  const dim3 gqk(static_cast<unsigned>(nqb > nkb ? nqb : nkb), static_cast<unsigned>(BH), 2u);
+  const dim3 gv(static_cast<unsigned>(nkb), static_cast<unsigned>(BH));
+  const auto* q = static_cast<const uint16_t*>(Q);
+  const auto* k = static_cast<const uint16_t*>(K);
+  const auto* v = static_cast<const uint16_t*>(V);
+  if (dtype == kBF16) {
+    fp8_qk_quant_kernel<true><<<gqk, 128, 0, stream>>>(q, k, signs, w.q8, w.k8, w.sq, w.sk, M, N);
+    fp8_v_amax_kernel<true><<<gv, 128, 0, stream>>>(v, w.vmax, N);
+    fp8_v_quant_kernel<true><<<gv, 128, 0, stream>>>(v, w.vmax, w.vt8, w.sv, N, w.npad);
+  } else {
+    fp8_qk_quant_kernel<false><<<gqk, 128, 0, stream>>>(q, k, signs, w.q8, w.k8, w.sq, w.sk, M, N);
+    fp8_v_amax_kernel<false><<<gv, 128, 0, stream>>>(v, w.vmax, N);
+    fp8_v_quant_kernel<false><<<gv, 128, 0, stream>>>(v, w.vmax, w.vt8, w.sv, N, w.npad);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace fa

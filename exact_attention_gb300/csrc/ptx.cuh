@@ -220,6 +220,18 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return d;
 }
 
+// The same descriptor with 64-byte swizzle (mode 4 in [61,64)): the layout a TMA load with
+// CU_TENSOR_MAP_SWIZZLE_64B writes for 64-byte rows (8-row atoms of 512 bytes).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(4u) << 61;
+  return d;
+}
+
 // Instruction descriptor for kind::f16 / kind::tf32 with f32 accumulation:
 // D format f32 at [4,6); A format at [7,10) and B format at [10,13)
 // (0 = f16, 1 = bf16, 2 = tf32); A major at bit 15 and B major at bit 16
@@ -230,6 +242,8 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t m, uint32_t n, uint
          ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 constexpr uint32_t kFmtF16 = 0, kFmtBF16 = 1, kFmtTF32 = 2;
+// kind::f8f6f4 uses the same fields; format 0 there is E4M3.
+constexpr uint32_t kFmtE4M3 = 0;
 // Bit 13 of the same descriptor negates A: D (+)= (-A) B. The kernels set it on the score
 // product when scale < 0, so that the softmax always multiplies by |scale|.
 constexpr uint32_t kNegateA = 1u << 13;
@@ -247,6 +261,22 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// kind::f8f6f4 (E4M3 operands here), K = 32 per instruction: D (+)= A[smem] B[smem]^T.
+__device__ __forceinline__ void mma_f8_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// D (+)= A[tmem] B[smem]^T, A packed four 8-bit values per 32-bit column.
+__device__ __forceinline__ void mma_f8_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
@@ -294,6 +324,10 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
       FA_W8(0), FA_W8(8), FA_W8(16), FA_W8(24)
       : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr), FA_W8(0)
+               : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
@@ -346,6 +380,20 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two f32 values rounded to E4M3 (nearest even, saturated to +-448) in one 16-bit word: lo in
+// bits [0,8), hi in [8,16).
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// The two E4M3 values of a 16-bit word, exactly, as f16x2 (lo byte -> lo half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 t;\n\tcvt.u16.u32 t, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, t;\n\t}" : "=r"(r) : "r"(v));
   return r;
 }
 

@@ -214,6 +214,40 @@ fa_status fa_bwd_ws(const void* Q, const void* K, const void* V, const void* O, 
 size_t fa_bwd_ws_workspace_bytes(int B, int H, int M, int D);
 
 /*
+ * FP8 forward: the forward with both products on E4M3 operands.
+ *
+ * Follows "Flash Attention" (notes), section "FlashAttention 3", the FP8 bullets:
+ * incoherent processing (Q and K multiplied on the right by M = diag(signs) H / 8,
+ * H the 64 x 64 Hadamard matrix, so that (Q M)(K M)^T = Q K^T while outliers
+ * spread over all 64 columns) and block quantisation (one scale per 128-row
+ * block of Q M and of K M, scale = block max / 448). V has one scale per
+ * (batch, head), because its key blocks are summed in one accumulator; the
+ * softmax weights are rounded to E4M3 for P V; O is divided by the sum of the
+ * rounded weights, LSE (natural log, f32) uses the exact sum. Two launches of
+ * quantisation kernels into the workspace, then the attention kernel.
+ *
+ *   Q, K, V, O, LSE, B, H, M, N, scale, causal   as for fa_fwd
+ *   D                  64 (other values: FA_ERR_UNSUPPORTED)
+ *   dtype              FA_F16 or FA_BF16 (storage of Q, K, V, O)
+ *   signs              device pointer to D signed bytes, each +1 or -1 (a
+ *                      negative byte counts as -1), drawn by the caller
+ *   workspace          device pointer, 16-byte aligned, at least
+ *                      fa_fwd_fp8_workspace_bytes(B,H,M,N,D) bytes: the E4M3
+ *                      copies of Q M [B*H][M][64] and K M [B*H][N][64], V
+ *                      transposed [B*H][64][N rounded up to 16], then the f32
+ *                      scales; caller-owned, written before it is read (no
+ *                      zero-fill needed), one call at a time
+ * The results are approximations: RMSE of O about 2e-3 to 8e-3 against exact
+ * attention on unit-variance inputs at scale 1/8.
+ */
+fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float* LSE, const signed char* signs,
+                     void* workspace, size_t workspace_bytes, int B, int H, int M, int N, int D, float scale,
+                     int causal, fa_dtype dtype, void* stream);
+
+/* Bytes of workspace fa_fwd_fp8 needs (0 on bad sizes or D != 64). */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int M, int N, int D);
+
+/*
  * Decode (flash decoding): one query row per (batch, head) against a KV cache
  * (fa_decode_ex below takes up to four rows and returns the LSE too).
  *

@@ -24,7 +24,7 @@ def lib():
 def declared_functions():
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(fa_[a-z_0-9]+)\s*\(", src)))
 
 
 def test_header_declares_the_binding_exports():
@@ -33,7 +33,7 @@ def test_header_declares_the_binding_exports():
 
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (fa_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (fa_[a-z_0-9]+)\b", out))
     missing = [f for f in declared_functions() if f not in exported]
     assert not missing, f"declared but not exported: {missing}"
     for f in declared_functions():

@@ -20,7 +20,7 @@ import oracle
 from exact_attention_gb300 import synth
 from oracle import fp8
 
-from helpers import TOL_FP8
+from helpers import TOL_FP8, fp8_rmse
 
 
 def _all_e4m3():
@@ -123,14 +123,15 @@ def test_forward_fp8_closed_forms():
 @pytest.mark.parametrize("N,causal", [(512, False), (512, True), (1024, False)])
 def test_forward_fp8_error_within_tolerance(N, causal):
     """The FP8 method itself against exact attention on the workload's inputs (fp16 N(0,1),
-    scale 1/8): RMSE within the pages' FP8 figure, max |error| within the fp16 bound times the
-    E4M3/fp16 unit-roundoff ratio."""
+    scale 1/8): RMSE (rows seeing 256 keys or more) within the pages' FP8 figure, max |error|
+    within the fp16 bound times the E4M3/fp16 unit-roundoff ratio."""
     q, k, v = synth.attention_inputs(1, 2, N, N, 64, "f16", seed=N)
     q, k, v = (synth.to_f64(x, "f16") for x in (q, k, v))
     signs = np.where(np.random.default_rng(6).standard_normal(64) > 0, 1.0, -1.0)
     Oe, Le = oracle.forward(q, k, v, 0.125, causal)
     Of, Lf = fp8.forward_fp8(q, k, v, 0.125, causal, signs)
-    assert np.sqrt(np.mean((Of - Oe) ** 2)) <= TOL_FP8["rmse"]
+    for h in range(2):
+        assert fp8_rmse(Of[0, h] - Oe[0, h], N, causal) <= TOL_FP8["rmse"]
     assert np.max(np.abs(Of - Oe)) <= TOL_FP8["max_abs"]
     assert np.max(np.abs(Lf - Le)) <= TOL_FP8["lse"]
 
