@@ -615,6 +615,23 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
                   "bf16 forward B4 H12 M=N=2048 D64 scale 0.125 non-causal", "fwd_d64_kernel<bf16,non-causal>")
     forward_entry("fwd_f16_N2048_causal", 4, 12, 2048, 2048, 64, "f16", True, 0.125,
                   "fp16 forward B4 H12 M=N=2048 D64 scale 0.125 causal (FLOP halved)", "fwd_d64_kernel<f16,causal>")
+    # FP8 forward (E4M3 operands, fp16 I/O) at the fp16 workload's largest shape: the whole call
+    # (three quantisation launches, then the attention kernel), against the fp8 tensor peak
+    for causal in (False, True):
+        q, k, v = attn(4, 12, 2048, 2048, 64, "f16", seed=2048)
+        o = torch.empty_like(q)
+        lse = torch.empty((4, 12, 2048), dtype=torch.float32, device="cuda")
+        signs = torch.from_numpy(synth.hadamard_signs(64, 0)).cuda()
+        nb = fa.fa_fwd_fp8_workspace_bytes(4, 12, 2048, 2048, 64)
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        t = timed(lambda: check(fa.fa_fwd_fp8(q, k, v, o, lse, signs, ws, nb, 4, 12, 2048, 2048, 64, 0.125, causal,
+                                              fa.FA_F16, stream), "fa_fwd_fp8"))
+        tag = "causal" if causal else "noncausal"
+        out[f"fwd_fp8_N2048_{tag}"] = tensor_entry(
+            f"FP8 forward (E4M3 operands after the Hadamard-times-sign transform, per-block scales; fp16 I/O) "
+            f"B4 H12 M=N=2048 D64 scale 0.125 {tag}: quantisation + attention per call",
+            4.0 * 4 * 12 * 2048 * 2048 * 64 / (2 if causal else 1), t, f"fwd_fp8_kernel<f16,{tag}> (+ fp8 quantisation)",
+            peak_tf * 2.0, f"{peaks_src} bf16 burst x nominal fp8/bf16 (4.5/2.25)")
     # f32, one head, 256^2 and 4096^2 (3xTF32)
     forward_entry("fwd_f32_N256", 1, 1, 256, 256, 64, "f32", False, 0.125,
                   "f32 forward 1 head Nq=Nk=256 D64 scale 0.125 (3xTF32)", "fwd_f32_kernel<non-causal>")
@@ -729,6 +746,7 @@ PROFILE_CASES = {
     # inputs larger than L2 (129 MB) so DRAM counters mean something, a few GB at most
     "fwd": dict(B=16, H=16, M=4096, N=4096, D=64, dtype="f16"),     # Q/K/V 0.4 GB
     "fwd_bench": dict(B=4, H=12, M=2048, N=2048, D=64, dtype="f16"),  # the headline workload itself
+    "fwd_fp8": dict(B=4, H=12, M=2048, N=2048, D=64, dtype="f16"),  # FP8 forward at the same shape
     "decode": dict(B=8, H=8, N=32768, D=128, n_splits=64, dtype="bf16"),  # K/V 1.07 GB
     "bwd": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # Q/K/V/O/dO 0.34 GB (fused pass)
     "bwd3": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # the same through the three kernels
@@ -755,6 +773,13 @@ def run_profile(kind: str, launches: int = 5):
         lse = torch.empty(shp[:3], device="cuda")
         for _ in range(launches):
             fa.forward(q, k, v, 0.125, False, out=o, lse=lse)
+    elif kind == "fwd_fp8":
+        shp = (c["B"], c["H"], c["M"], c["D"])
+        q, k, v = (torch.randn(shp, generator=g, device="cuda").half() for _ in range(3))
+        signs = torch.where(torch.rand(c["D"], generator=g, device="cuda") < 0.5, -1, 1).to(torch.int8)
+        ws = None
+        for _ in range(launches):
+            _, _, ws = fa.forward_fp8(q, k, v, 0.125, False, signs, workspace=ws)
     elif kind in ("bwd", "bwd3"):
         shp = (c["B"], c["H"], c["M"], c["D"])
         q, k, v, do = (torch.randn(shp, generator=g, device="cuda").half() for _ in range(4))

@@ -21,27 +21,6 @@ __device__ __forceinline__ float half_to_f32(uint16_t h) {
   return BF16 ? __uint_as_float(static_cast<uint32_t>(h) << 16) : __half2float(__ushort_as_half(h));
 }
 
-// One 64-element row of a half-precision tensor (zeros past `rows`).
-template <bool BF16>
-__device__ __forceinline__ void load_row(const uint16_t* src, int row, int rows, float* x) {
-  if (row >= rows) {
-#pragma unroll
-    for (int d = 0; d < kD8; ++d) x[d] = 0.f;
-    return;
-  }
-  const uint4* p = reinterpret_cast<const uint4*>(src + static_cast<size_t>(row) * kD8);
-#pragma unroll
-  for (int c = 0; c < kD8 / 8; ++c) {
-    const uint4 v = p[c];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[8 * c + 2 * i] = half_to_f32<BF16>(static_cast<uint16_t>(w[i] & 0xFFFFu));
-      x[8 * c + 2 * i + 1] = half_to_f32<BF16>(static_cast<uint16_t>(w[i] >> 16));
-    }
-  }
-}
-
 // Largest value of v over the CTA's 128 threads (all threads get it).
 __device__ __forceinline__ float block_max128(float v, float* red) {
 #pragma unroll
@@ -53,37 +32,43 @@ __device__ __forceinline__ float block_max128(float v, float* red) {
   return v;
 }
 
-// 64 values times `inv`, rounded to E4M3, stored as 64 bytes at dst (16-byte aligned).
-__device__ __forceinline__ void store_e4m3_row(uint8_t* dst, const float* x, float inv) {
-  uint32_t w[16];
-#pragma unroll
-  for (int p = 0; p < 16; ++p)
-    w[p] = ptx::pack_e4m3x2(x[4 * p] * inv, x[4 * p + 1] * inv) |
-           (ptx::pack_e4m3x2(x[4 * p + 2] * inv, x[4 * p + 3] * inv) << 16);
-  uint4* o = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) o[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-}
-
 // Q (blockIdx.z = 0) or K (1): one CTA per 128-row block of one head, one row per thread.
 // x -> x diag(signs) H / 8 by a fast Walsh-Hadamard transform in registers, then the block's
-// scale = amax / 448 and the E4M3 row.
+// scale = amax / 448 and the E4M3 row. The block moves through shared memory in 16-byte
+// pieces, so that its global loads and stores are contiguous across each warp.
 template <bool BF16>
 __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __restrict__ Q,
                                                            const uint16_t* __restrict__ K,
                                                            const int8_t* __restrict__ signs, uint8_t* __restrict__ Q8,
                                                            uint8_t* __restrict__ K8, float* __restrict__ sq,
                                                            float* __restrict__ sk, int M, int N) {
+  __shared__ uint32_t tile[kRowsPerBlock][kD8 / 2 + 1];  // 32 words of halves a row (+1: no bank conflicts)
   __shared__ float red[4];
   const bool isk = blockIdx.z == 1;
   const int rows = isk ? N : M;
   const int nblk = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   if (static_cast<int>(blockIdx.x) >= nblk) return;  // the grid covers the longer of the two
   const size_t bh = blockIdx.y;
-  const uint16_t* src = (isk ? K : Q) + bh * static_cast<size_t>(rows) * kD8;
-  const int row = static_cast<int>(blockIdx.x) * kRowsPerBlock + static_cast<int>(threadIdx.x);
+  const int r0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
+  const int nrows = min(kRowsPerBlock, rows - r0);
+  const uint4* src = reinterpret_cast<const uint4*>((isk ? K : Q) + (bh * rows + r0) * kD8);
+  for (int c = threadIdx.x; c < kRowsPerBlock * kD8 / 8; c += blockDim.x) {
+    const int r = c >> 3, q = c & 7;
+    const uint4 v = r < nrows ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+    tile[r][4 * q] = v.x;
+    tile[r][4 * q + 1] = v.y;
+    tile[r][4 * q + 2] = v.z;
+    tile[r][4 * q + 3] = v.w;
+  }
+  __syncthreads();
+  const int r = threadIdx.x;
   float x[kD8];
-  load_row<BF16>(src, row, rows, x);
+#pragma unroll
+  for (int w = 0; w < kD8 / 2; ++w) {
+    const uint32_t v = tile[r][w];
+    x[2 * w] = half_to_f32<BF16>(static_cast<uint16_t>(v & 0xFFFFu));
+    x[2 * w + 1] = half_to_f32<BF16>(static_cast<uint16_t>(v >> 16));
+  }
 #pragma unroll
   for (int d = 0; d < kD8; ++d)
     if (__ldg(signs + d) < 0) x[d] = -x[d];
@@ -104,25 +89,42 @@ __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __res
     x[d] *= 0.125f;  // 1 / sqrt(64), exact
     am = fmaxf(am, fabsf(x[d]));
   }
-  am = block_max128(am, red);
+  am = block_max128(am, red);  // (its barriers also order the tile's reads before the writes below)
   const float scale = am > 0.f ? am / kE4M3Max : 1.f;
   const float inv = am > 0.f ? kE4M3Max / am : 1.f;
   if (threadIdx.x == 0) (isk ? sk : sq)[bh * nblk + blockIdx.x] = scale;
-  if (row < rows) store_e4m3_row((isk ? K8 : Q8) + (bh * rows + row) * kD8, x, inv);
+  // the E4M3 row (16 words) back into the tile, then out 16 bytes at a time
+#pragma unroll
+  for (int p = 0; p < 16; ++p)
+    tile[r][p] = ptx::pack_e4m3x2(x[4 * p] * inv, x[4 * p + 1] * inv) |
+                 (ptx::pack_e4m3x2(x[4 * p + 2] * inv, x[4 * p + 3] * inv) << 16);
+  __syncthreads();
+  uint4* dst = reinterpret_cast<uint4*>((isk ? K8 : Q8) + (bh * rows + r0) * kD8);
+  for (int c = threadIdx.x; c < nrows * kD8 / 16; c += blockDim.x) {
+    const int rr = c >> 2, q = c & 3;
+    dst[c] = make_uint4(tile[rr][4 * q], tile[rr][4 * q + 1], tile[rr][4 * q + 2], tile[rr][4 * q + 3]);
+  }
 }
 
-// Largest |V| of each 128-key block of each head.
+// Largest |V| of each 128-key block of each head (16-byte loads contiguous across each warp).
 template <bool BF16>
 __global__ void __launch_bounds__(128) fp8_v_amax_kernel(const uint16_t* __restrict__ V, float* __restrict__ vmax,
                                                          int N) {
   __shared__ float red[4];
   const int nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
   const size_t bh = blockIdx.y;
-  float x[kD8];
-  load_row<BF16>(V + bh * static_cast<size_t>(N) * kD8, static_cast<int>(blockIdx.x) * kRowsPerBlock + threadIdx.x, N, x);
+  const int k0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
+  const int nrows = min(kRowsPerBlock, N - k0);
+  const uint4* src = reinterpret_cast<const uint4*>(V + (bh * N + k0) * kD8);
   float am = 0.f;
+  for (int c = threadIdx.x; c < nrows * kD8 / 8; c += blockDim.x) {
+    const uint4 v = src[c];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int d = 0; d < kD8; ++d) am = fmaxf(am, fabsf(x[d]));
+    for (int i = 0; i < 4; ++i)
+      am = fmaxf(am, fmaxf(fabsf(half_to_f32<BF16>(static_cast<uint16_t>(w[i] & 0xFFFFu))),
+                           fabsf(half_to_f32<BF16>(static_cast<uint16_t>(w[i] >> 16)))));
+  }
   am = block_max128(am, red);
   if (threadIdx.x == 0) vmax[bh * nkb + blockIdx.x] = am;
 }

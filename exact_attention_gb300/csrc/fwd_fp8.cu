@@ -7,11 +7,13 @@
 // The schedule and the roles are those of the fp16/bf16 D = 64 forward (whole pairs of
 // 128-row query tiles per CTA, one CTA per SM):
 //
-//   S0 [0,128)  S1 [128,256)  P0 [256,288)  P1 [288,320)  O0 [320,384)  O1 [384,448)
+//   S0 [0,128)  S1 [128,256)  P0 [256,288)  P1 [288,320)  O0 [320,400)  O1 [400,480)
 //
 // with the softmax's exponent constant per key block j: scale * log2(e) * sq * sk[j], and the
-// weights rounded to E4M3 (four per tensor-memory column) for P V. O is divided by the sum of
-// the rounded weights and multiplied by sv; LSE uses the exact f32 sum.
+// weights rounded to E4M3 (four per tensor-memory column) for P V. Each stage's V tile carries
+// 16 constant rows after its 64 (row 64 all ones, the rest zero), so P V has N = 80 and its
+// column 64 accumulates the sum of the rounded weights in the tensor core, rescaled with O;
+// O is divided by that sum and multiplied by sv. LSE uses the exact f32 sum.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -35,7 +37,10 @@ using fwdc::TileInfo;
 constexpr int kD = 64;
 constexpr int kQSlot = 16384;  // Q8 tile (8 KB) or, after its last S, the tile's fp16 O (16 KB)
 constexpr int kKTile = kBN * kD;  // 8 KB: 128 keys x 64 bytes
-constexpr int kVTile = kD * kBN;  // 8 KB: 64 rows of 128 keys
+constexpr int kVTile = kD * kBN;  // 8 KB: 64 rows of 128 keys (what TMA loads)
+constexpr int kVRows = kD + 16;   // plus a row of ones and 15 of zeros
+constexpr int kVSlot = kVRows * kBN;  // 10 KB per stage
+constexpr int kDO = kVRows;       // columns of an O accumulator: 64 of O, the weight sum, 15 zeros
 constexpr int kStages = 4;
 constexpr int kQBuf = 2;
 constexpr int kThreads = 384;
@@ -45,11 +50,12 @@ constexpr int kWarpEpi = 11;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
-constexpr int kSmemData = kQBuf * 2 * kQSlot + kStages * (kKTile + kVTile);
+constexpr int kSmemData = kQBuf * 2 * kQSlot + kStages * (kKTile + kVSlot);
 constexpr int kSmemBytes = 1024 + 1024 + kSmemData;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 320;
+static_assert(kColO + 2 * kDO <= 512, "tensor-memory plan");
 
 struct Hdr {
   unsigned long long q_full[kQBuf], q_empty[kQBuf];
@@ -78,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
   const uint32_t data_u32 = (raw_u32 + 1024u + 1023u) & ~1023u;
   auto q_addr = [&](int qb, int t) { return data_u32 + (qb * 2 + t) * kQSlot; };
-  auto k_addr = [&](int st) { return data_u32 + kQBuf * 2 * kQSlot + st * (kKTile + kVTile); };
+  auto k_addr = [&](int st) { return data_u32 + kQBuf * 2 * kQSlot + st * (kKTile + kVSlot); };
   auto v_addr = [&](int st) { return k_addr(st) + kKTile; };
 
   const int warp = threadIdx.x >> 5;
@@ -119,6 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(&hdr->tmem_base), 512);
     ptx::tmem_relinquish();
   }
+  // the constant rows of every stage's V tile: row 64 all E4M3 ones (0x38), rows 65..79 zero
+  // (each row's 16-byte chunks are equal, so the 128-byte swizzle leaves them in place)
+  for (int i = threadIdx.x; i < kStages * (kVSlot - kVTile) / 16; i += kThreads) {
+    const int st = i / ((kVSlot - kVTile) / 16), c = i % ((kVSlot - kVTile) / 16);
+    const uint32_t w = c < kBN / 16 ? 0x38383838u : 0u;
+    *reinterpret_cast<uint4*>(smem_raw + (v_addr(st) - raw_u32) + kVTile + 16 * c) = make_uint4(w, w, w, w);
+  }
+  ptx::fence_proxy_async_smem();  // generic-proxy writes -> the tensor core's reads
   if (warp == kWarpProd && lane == 0) {
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
@@ -167,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer of tile t (lane 0)
     const uint32_t idesc_qk =
         ptx::idesc_f32acc(kBM, kBN, ptx::kFmtE4M3, ptx::kFmtE4M3, false, false) | (neg_scale ? ptx::kNegateA : 0u);
-    constexpr uint32_t idesc_pv = ptx::idesc_f32acc(kBM, kD, ptx::kFmtE4M3, ptx::kFmtE4M3, false, false);
+    constexpr uint32_t idesc_pv = ptx::idesc_f32acc(kBM, kDO, ptx::kFmtE4M3, ptx::kFmtE4M3, false, false);
     const int t = warp - kWarpMma;
     if (lane == 0) {
       uint32_t kv_base = 0;
@@ -178,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto commit = [&](unsigned long long* bar) { ptx::tc_commit(ptx::smem_u32(bar)); };
       const uint32_t dS = tmem + kColS + t * kBN;
-      const uint32_t dO = tmem + kColO + t * kD;
+      const uint32_t dO = tmem + kColO + t * kDO;
       const uint32_t aP = tmem + kColP + t * (kBN / 4);
       for (int it = 0; ok; ++it) {
         const int tile = classic_tile<CAUSAL>(it);
@@ -272,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_sel = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + lane_sel + kColS + t * kBN;
     const uint32_t tP = tmem + lane_sel + kColP + t * (kBN / 4);
-    const uint32_t tO = tmem + lane_sel + kColO + t * kD;
+    const uint32_t tO = tmem + lane_sel + kColO + t * kDO;
     const uint32_t s_full = ptx::smem_u32(&hdr->s_full[t]);
     const uint32_t sm_a = ptx::smem_u32(&hdr->sm_a[t]);
     const uint32_t sm_b = ptx::smem_u32(&hdr->sm_b[t]);
@@ -294,7 +308,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float csq = scale_log2 * (qtile < nqb ? sq[static_cast<size_t>(ti.bh) * nqb + qtile] : 1.f);
       const float* skh = sk + static_cast<size_t>(ti.bh) * nkb;
       float m2 = -INFINITY;
-      float l = 0.f;
       float le = 0.f;
       for (int j = 0; j < nbt; ++j, ++nblk) {
         const float cj = csq * __ldg(skh + j);
@@ -329,14 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rescale) {
           const float m_new = fmaxf(m2, mxs);
           corr = m_new == -INFINITY ? 1.f : ptx::ex2(m2 - m_new);
-          l *= corr;
           le *= corr;
           m2 = m_new;
         }
         const float neg_m = m2 == -INFINITY ? 0.f : -m2;
         const float2 c2 = make_float2(cj, cj), nm2 = make_float2(neg_m, neg_m);
         float2 se = make_float2(0.f, 0.f);
-        float sr0 = 0.f, sr1 = 0.f;
         // P over keys [c, c + 32): E4M3, four per column, stored to columns [c/4, c/4 + 8)
         auto p_piece = [&](int c) {
           uint32_t pk[8];
@@ -350,7 +361,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float a = ptx::ex2(x.x), b = ptx::ex2(x.y);
               se = fadd2(se, make_float2(a, b));
               hw[u] = ptx::pack_e4m3x2(a, b);
-              ptx::add_f16x2_to_f32(ptx::e4m3x2_to_f16x2(hw[u]), sr0, sr1);
             }
             pk[i] = hw[0] | (hw[1] << 16);
           }
@@ -378,6 +388,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
             ptx::tmem_st32(tO + c, o);
           }
+          {  // the weight sum (column 64) with it
+            uint32_t o[16];
+            ptx::tmem_ld16(tO + kD, o);
+            ptx::tmem_wait_ld16(o);
+            o[0] = __float_as_uint(__uint_as_float(o[0]) * corr);
+            ptx::tmem_st16(tO + kD, o);
+          }
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -391,7 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         p_piece(64);
         p_piece(96);
         le += se.x + se.y;
-        l += sr0 + sr1;
         ptx::tmem_wait_st();
       }
       if (!ok) break;
@@ -403,6 +419,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       o_ph ^= 1u;
       ptx::tc_fence_after();
       // O = acc * sv / l, into the tile's Q slot in the 128-byte swizzled layout of the O map
+      float l;
+      {
+        uint32_t o[16];
+        ptx::tmem_ld16(tO + kD, o);
+        ptx::tmem_wait_ld16(o);
+        l = __uint_as_float(o[0]);  // the sum of the rounded weights, from the tensor core
+      }
       const float f = sv[ti.bh] / l;
       const int r_in = wq * 32 + lane;
       uint8_t* buf = smem_raw + (q_addr(qb, t) - raw_u32);
