@@ -171,6 +171,10 @@ __global__ void __launch_bounds__(kThreads32, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernFwdF32};
+  // launched as a programmatic dependent: the set-up above overlapped the previous kernel's tail;
+  // no global memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
 
   if (warp == kWarpProd32) {
     // ------------------------------------------------------------ TMA producer
@@ -500,10 +504,18 @@ cudaError_t launch32(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   // the tiles' counters follow the partial slots
   unsigned long long* counters =
       parts > 1 ? reinterpret_cast<unsigned long long*>(ws + static_cast<size_t>(units) * kF32Slot) : nullptr;
-  kern<<<grid, kThreads32, kSmem32, ctx.stream>>>(mq, mk, mv, static_cast<float*>(O), LSE, BH, M, N,
-                                                  scale * kLog2e32, parts, ws, counters, epoch, ctx.status,
-                                                  ctx.wait_budget_ns);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads32);
+  cfg.dynamicSmemBytes = kSmem32;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];  // a programmatic dependent of the kernel before it on the stream
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, static_cast<float*>(O), LSE, BH, M, N, scale * kLog2e32, parts, ws,
+                            counters, epoch, ctx.status, ctx.wait_budget_ns);
 }
 
 }  // namespace

@@ -164,6 +164,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernFwd};
+  // launched as a programmatic dependent: the set-up above overlapped the previous kernel's tail;
+  // no global memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
 
   if (warp == kWarpProd) {
     // ------------------------------------------------------------ TMA producer
@@ -443,9 +447,17 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   if (e != cudaSuccess) return e;
   const long long tiles = static_cast<long long>((M + 2 * kBM - 1) / (2 * kBM)) * BH;
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
-  kern<<<grid, kThreads, C::kSmemBytes, ctx.stream>>>(mq, mk, mv, O, LSE, BH, M, N, scale * kLog2e, ctx.status,
-                                                      ctx.wait_budget_ns);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = ctx.stream;
+  cudaLaunchAttribute attr[1];  // a programmatic dependent of the kernel before it on the stream
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, O, LSE, BH, M, N, scale * kLog2e, ctx.status, ctx.wait_budget_ns);
 }
 
 }  // namespace

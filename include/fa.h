@@ -85,8 +85,14 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  * gives every SM an equal contiguous share of (query pair, key block) work; a
  * pair whose key blocks are shared by two or more SMs is merged at the end by the
  * SM holding its first blocks, with the same (m, l) rescaling the online softmax
- * uses between key blocks. The merge waits on flags written by other SMs, so the
- * kernel is launched cooperatively (all CTAs resident at once).
+ * uses between key blocks. That SM waits (bounded, fa_set_wait_budget_ns) for the
+ * flags of the SMs holding the rest, which process those pieces first; the
+ * launch has one CTA per SM and relies on all of them becoming resident within
+ * the wait budget, which holds unless kernels on other streams or processes
+ * keep SMs busy for longer than that (then FA_ERR_TIMEOUT;
+ * fa_set_schedule(FA_SCHED_FWD_SPLIT, 0) runs whole pairs, with no waits).
+ * Every forward launch is a programmatic dependent of the kernel before it on
+ * the stream: its set-up overlaps that kernel's tail.
  *
  *   workspace        device pointer, 16-byte aligned, at least
  *                    fa_fwd_workspace_bytes(...) bytes, or NULL (then this is
