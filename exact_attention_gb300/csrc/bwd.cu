@@ -49,6 +49,10 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const uint16_t* __restri
                                                         float* __restrict__ delta, float* __restrict__ acc_zero,
                                                         uint32_t* __restrict__ counters_zero, int n_counters,
                                                         long long rows) {
+  // launched as a programmatic dependent of the kernel before it on the stream (a previous
+  // backward's dQ conversion reads the accumulator this kernel zeroes): wait for it first
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
   // the fused pass's counters (split schedule) start at zero
   if (blockIdx.x == 0)
     for (int k = threadIdx.x; k < n_counters; k += blockDim.x) counters_zero[k] = 0u;
@@ -1729,10 +1733,18 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     // the fused D = 64 pass accumulates dQ into dQacc, which this kernel zeroes on the way, and
     // its split schedule's counters start at zero
     float* zero = D == 64 ? dQacc : nullptr;
-    bwd_delta_kernel<D, BF16><<<static_cast<int>(blocks), 256, 0, ctx.stream>>>(
-        static_cast<const uint16_t*>(O), static_cast<const uint16_t*>(dO), delta, zero, counters,
-        split ? ctx.num_sms * kCwF : 0, rows);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t dcfg{};
+    dcfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    dcfg.blockDim = dim3(256);
+    dcfg.stream = ctx.stream;
+    cudaLaunchAttribute dattr[1];
+    dattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    dattr[0].val.programmaticStreamSerializationAllowed = 1;
+    dcfg.attrs = dattr;
+    dcfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&dcfg, bwd_delta_kernel<D, BF16>, static_cast<const uint16_t*>(O),
+                                       static_cast<const uint16_t*>(dO), delta, zero, counters,
+                                       split ? ctx.num_sms * kCwF : 0, rows);
     if (e != cudaSuccess) return e;
   }
   CUtensorMap mq, mk, mv, mdo;

@@ -52,9 +52,18 @@ __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __res
   const int r0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
   const int nrows = min(kRowsPerBlock, rows - r0);
   const uint4* src = reinterpret_cast<const uint4*>((isk ? K : Q) + (bh * rows + r0) * kD8);
-  for (int c = threadIdx.x; c < kRowsPerBlock * kD8 / 8; c += blockDim.x) {
+  // eight independent 16-byte loads a thread, all in flight at once
+  uint4 ld[kRowsPerBlock * kD8 / 8 / 128];
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
+    ld[i] = (c >> 3) < nrows ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
     const int r = c >> 3, q = c & 7;
-    const uint4 v = r < nrows ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 v = ld[i];
     tile[r][4 * q] = v.x;
     tile[r][4 * q + 1] = v.y;
     tile[r][4 * q + 2] = v.z;
@@ -100,9 +109,11 @@ __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __res
                  (ptx::pack_e4m3x2(x[4 * p + 2] * inv, x[4 * p + 3] * inv) << 16);
   __syncthreads();
   uint4* dst = reinterpret_cast<uint4*>((isk ? K8 : Q8) + (bh * rows + r0) * kD8);
-  for (int c = threadIdx.x; c < nrows * kD8 / 16; c += blockDim.x) {
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 16 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
     const int rr = c >> 2, q = c & 3;
-    dst[c] = make_uint4(tile[rr][4 * q], tile[rr][4 * q + 1], tile[rr][4 * q + 2], tile[rr][4 * q + 3]);
+    if (rr < nrows) dst[c] = make_uint4(tile[rr][4 * q], tile[rr][4 * q + 1], tile[rr][4 * q + 2], tile[rr][4 * q + 3]);
   }
 }
 
@@ -117,8 +128,15 @@ __global__ void __launch_bounds__(128) fp8_v_amax_kernel(const uint16_t* __restr
   const int nrows = min(kRowsPerBlock, N - k0);
   const uint4* src = reinterpret_cast<const uint4*>(V + (bh * N + k0) * kD8);
   float am = 0.f;
-  for (int c = threadIdx.x; c < nrows * kD8 / 8; c += blockDim.x) {
-    const uint4 v = src[c];
+  uint4 ld[kRowsPerBlock * kD8 / 8 / 128];
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
+    ld[i] = c < nrows * kD8 / 8 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const uint4 v = ld[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -148,10 +166,17 @@ __global__ void __launch_bounds__(128) fp8_v_quant_kernel(const uint16_t* __rest
   if (blockIdx.x == 0 && threadIdx.x == 0) sv[bh] = scale;
   // the block's 128 x 64 values (contiguous in memory) into shared memory, 16 bytes per load
   const uint16_t* src = V + (bh * static_cast<size_t>(N) + k0) * kD8;
-  for (int c = threadIdx.x; c < kRowsPerBlock * kD8 / 8; c += blockDim.x) {
+  uint4 ld[kRowsPerBlock * kD8 / 8 / 128];
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
+    ld[i] = k0 + c / (kD8 / 8) < N ? reinterpret_cast<const uint4*>(src)[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
     const int key = c / (kD8 / 8), d0 = (c % (kD8 / 8)) * 8;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (k0 + key < N) v = reinterpret_cast<const uint4*>(src)[c];
+    const uint4 v = ld[i];
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
