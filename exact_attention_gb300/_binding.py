@@ -18,7 +18,7 @@ from typing import Optional
 
 FA_OK, FA_ERR_INVALID, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = range(5)
 FA_F32, FA_F16, FA_BF16 = 0, 1, 2
-FA_SCHED_FWD_SPLIT, FA_SCHED_BWD_SPLIT, FA_SCHED_HOST_CHUNKS = 1, 2, 3
+FA_SCHED_FWD_SPLIT, FA_SCHED_BWD_SPLIT, FA_SCHED_HOST_CHUNKS, FA_SCHED_BWD_PAIR = 1, 2, 3, 4
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfa.so")
 

@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "bwd_common.cuh"
 #include "fa_internal.cuh"
 #include "ptx.cuh"
 
@@ -34,13 +35,10 @@ __device__ __forceinline__ int item_of_round(int r, int items) {
   return w < items ? static_cast<int>(w) : items;
 }
 
-constexpr int kT = 128;          // tile rows (keys or queries) and streamed block rows
-constexpr int kChunkB = 16384;   // 128 rows x 128 bytes, one swizzled chunk
 constexpr int kStagesB = 2;
 constexpr int kThreadsB = 192;   // 4 compute warps, producer (4), MMA (5)
 constexpr int kWarpProdB = 4;
 constexpr int kWarpMmaB = 5;
-constexpr float kLog2eB = 1.4426950408889634f;
 constexpr int kMinSmem = 120 * 1024;  // keeps one CTA per SM (each allocates all of tensor memory)
 
 // ------------------------------------------------------------------------- delta
@@ -110,27 +108,6 @@ struct BwdCfg {
   static constexpr int kSmemNeed = 1024 + static_cast<int>(kHdrBytes) + kData;
   static constexpr int kSmem = kSmemNeed > kMinSmem ? kSmemNeed : kMinSmem;
 };
-
-// Which part of the work a persistent CTA does next.
-struct BwdItem {
-  int bh, r0;  // head, first row of this CTA's tile
-  int lo, hi;  // streamed blocks [lo, hi)
-};
-
-// Scores, in the packed-halves layout an MMA A operand uses in tensor memory.
-template <bool BF16>
-__device__ __forceinline__ uint32_t pack2(float a, float b) {
-  return BF16 ? ptx::pack_bf16x2(a, b) : ptx::pack_f16x2(a, b);
-}
-
-// K-major 128-row operand at `addr` (D/64 chunks): descriptor for k-step ks.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t addr, int ks) {
-  return ptx::sdesc_sw128(addr + (ks >> 2) * kChunkB + (ks & 3) * 32, 16, 1024);
-}
-// MN-major operand (rows = reduction dim, D contiguous): descriptor for k-step ks of 16 rows.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t addr, int ks) {
-  return ptx::sdesc_sw128(addr + ks * 2048, kChunkB, 1024);
-}
 
 // ---------------------------------------------------------------------- dK / dV
 // TMEM: S^T [0,128) -> P^T packed [0,64); dP^T [128,256) -> dS^T packed [128,192);
@@ -1797,7 +1774,10 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     const long long items = static_cast<long long>(BH) * nkb;
     const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
     cudaError_t e;
-    if constexpr (D == 64) {  // tensor memory holds the overlapped layout
+    if (D == 64 && sp.pair) {
+      e = launch_bwd_dkdv64_pair(Q, K, V, dO, LSE, delta, dK, dV, BH, M, N, scale, CAUSAL, dtype, ctx);
+      if (e != cudaSuccess) return e;
+    } else if constexpr (D == 64) {  // tensor memory holds the overlapped layout
       auto kern = bwd_dkdv64_kernel<BF16, CAUSAL>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, OvCfg<64>::kSmem);
       if (e != cudaSuccess) return e;

@@ -177,6 +177,23 @@ bool make_tmap_3d_ex(CUtensorMap* map, const void* base, int dtype, uint64_t inn
   return r == CUDA_SUCCESS;
 }
 
+bool make_tmap_3d_view(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t pitch, uint64_t rows,
+                       uint64_t outer, uint32_t box_inner, uint32_t box_rows) {
+  if (!make_tmap_3d(map, base, dtype, pitch, rows, outer, box_inner, box_rows)) return false;  // loads the encoder
+  const size_t es = dtype_size(dtype);
+  const CUtensorMapDataType t = dtype == kF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                : dtype == kF16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[3] = {inner, rows, outer};
+  cuuint64_t strides[2] = {pitch * es, pitch * rows * es};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, t, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -187,6 +204,7 @@ namespace {
 std::atomic<int> g_sched_fwd_split{-1};
 std::atomic<int> g_sched_bwd_split{-1};
 std::atomic<int> g_sched_host_chunks{-1};
+std::atomic<int> g_sched_bwd_pair{-1};
 constexpr int kHostChunks = 8;  // most head chunks of fa_fwd_host (events kept per device)
 
 // Whether a forward call with a workspace runs the split schedule (D = 64 halves).
@@ -365,8 +383,13 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   FA_TRY(check_ptr(delta_ws, "delta_ws"));
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
-  BwdSplit sp{nullptr};
+  BwdSplit sp{};
   if (dQacc != nullptr && split_ws != nullptr && use_bwd_split(B * H, M, N, D, causal, ctx.num_sms)) sp.ws = split_ws;
+  // fa_bwd's dK/dV kernel at D = 64 on CTA pairs: by default for non-causal calls (where it
+  // measured as fast or faster); causal calls keep single CTAs (a pair's item of 256 keys starts at
+  // the query block of its first key, so the second CTA's first block is wholly masked)
+  const int pair_forced = g_sched_bwd_pair.load();
+  sp.pair = dQacc == nullptr && D == 64 && (pair_forced == 1 || (pair_forced == -1 && causal == 0));
   cudaError_t e =
       launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, dQacc, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);
@@ -415,6 +438,10 @@ fa_status fa_set_schedule(fa_sched_key key, int value) {
     case FA_SCHED_BWD_SPLIT:
       if (value < -1 || value > 1) return fail(FA_ERR_INVALID, "schedule key %d takes -1, 0 or 1 (got %d)", key, value);
       (key == FA_SCHED_FWD_SPLIT ? g_sched_fwd_split : g_sched_bwd_split).store(value);
+      return FA_OK;
+    case FA_SCHED_BWD_PAIR:
+      if (value < -1 || value > 1) return fail(FA_ERR_INVALID, "schedule key %d takes -1, 0 or 1 (got %d)", key, value);
+      g_sched_bwd_pair.store(value);
       return FA_OK;
     case FA_SCHED_HOST_CHUNKS:
       if (value != -1 && (value < 1 || value > kHostChunks))

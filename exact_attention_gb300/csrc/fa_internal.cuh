@@ -99,9 +99,16 @@ cudaError_t launch_fwd_fp8(const Fp8Ws& w, void* O, float* LSE, int BH, int M, i
 // Split schedule of the fused backward (non-causal, D = 64): ws holds bwd_fused_split_bytes of
 // partial dK/dV slots (two per SM) then num_sms * 8 counters; ws == nullptr runs whole key tiles.
 struct BwdSplit {
-  float* ws;
+  float* ws = nullptr;
+  bool pair = false;  // three-kernel path, D = 64: the dK/dV kernel on CTA pairs
 };
 size_t bwd_fused_split_bytes(int num_sms);
+
+// dK / dV with D = 64 on CTA pairs (cta_group::2), launched as a programmatic dependent of the
+// delta kernel; the three-kernel backward's alternative to its single-CTA dK/dV kernel.
+cudaError_t launch_bwd_dkdv64_pair(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                                   const float* delta, void* dK, void* dV, int BH, int M, int N, float scale,
+                                   bool causal, int dtype, const LaunchCtx& ctx);
 
 // dQacc == nullptr: delta, dK/dV and dQ kernels; else (D = 64) delta, one fused dK/dV/dQ kernel
 // that accumulates dQ in dQacc (B*H*M*D f32), and a conversion of dQacc into dQ.
@@ -127,5 +134,9 @@ bool make_tmap_3d(CUtensorMap* map, const void* base, int dtype, uint64_t inner,
 // must not exceed it).
 bool make_tmap_3d_ex(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t rows, uint64_t outer,
                      uint32_t box_inner, uint32_t box_rows, int swizzle_bytes);
+// A view of the first `inner` elements of rows `pitch` elements apart (128-byte swizzle); a box
+// wider than the view reads the columns past it as zeros. False when the driver refuses it.
+bool make_tmap_3d_view(CUtensorMap* map, const void* base, int dtype, uint64_t inner, uint64_t pitch, uint64_t rows,
+                       uint64_t outer, uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace fa

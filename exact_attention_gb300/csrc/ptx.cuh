@@ -113,6 +113,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow(bar, parity, w, site);
 }
 
+// ------------------------------------------------------- CTA pairs (clusters of two)
+// The kernels that run as CTA pairs (tcgen05 cta_group::2) use these. A pair is a cluster of two
+// CTAs; rank 0 issues the MMAs for both.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Every thread of both CTAs: all memory operations before it are visible to both CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// The shared::cluster address of `bar` (a shared::cta address of this CTA's layout) in CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t bar, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(bar), "r"(rank));
+  return r;
+}
+// Arrive on a barrier given by its shared::cluster address (this CTA's or the peer's). Default
+// (CTA-scope) semantics: what an arrival hands over across the pair is tensor memory the arriving
+// thread has finished storing (tcgen05.wait::st, then tcgen05.fence::before_thread_sync) or shared
+// memory a TMA load has completed into (its barrier waited first), both read afterwards by the
+// tensor core. A cluster-scope release measured about 0.8 us per block slower in the pair
+// backward (a fence on every arrival), and cluster-scope acquires on the waits a further 0.4 us.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cl_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cl_bar) : "memory");
+}
+
 // Bounded wait used only while draining after an abort: ignores the abort
 // flag and records nothing.
 static __device__ __noinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity, uint64_t budget_ns) {
@@ -206,6 +234,27 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                : "memory");
 }
 
+// The same for a CTA pair (cta_group::2): one warp of each CTA of the pair executes the
+// allocation (both get the same columns in their own tensor memory) and the deallocation.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Arrive once on `bar` (same shared-memory offset) in both CTAs of the pair when every pair MMA this
+// thread issued so far completes.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (PTX ISA, tcgen05
 // "Shared memory descriptor"): start>>4 in [0,14), leading-dimension byte
 // offset>>4 in [16,30), stride-dimension byte offset>>4 in [32,46), the fixed
@@ -261,6 +310,24 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// CTA-pair forms (cta_group::2, issued by rank 0 of the pair): M = 256 rows, rows 0-127 in rank 0's
+// tensor memory and A operand, 128-255 in rank 1's; B's N columns are split in halves, the first
+// from rank 0's shared memory and the second from rank 1's, at the same descriptor address.
+__device__ __forceinline__ void mma_f16_ss_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f16_ts_pair(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
       "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }

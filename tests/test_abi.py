@@ -118,7 +118,7 @@ def test_empty_problems_are_no_ops(lib):
 
 def test_schedule_controls(lib):
     """fa_set_schedule: valid keys and values are accepted (and reset to automatic), others refused."""
-    for key in (fa.FA_SCHED_FWD_SPLIT, fa.FA_SCHED_BWD_SPLIT):
+    for key in (fa.FA_SCHED_FWD_SPLIT, fa.FA_SCHED_BWD_SPLIT, fa.FA_SCHED_BWD_PAIR):
         for v in (0, 1, -1):
             assert fa.fa_set_schedule(key, v) == fa.FA_OK
         assert fa.fa_set_schedule(key, 2) == fa.FA_ERR_INVALID
@@ -127,6 +127,6 @@ def test_schedule_controls(lib):
     for v in (0, 9, -2):
         assert fa.fa_set_schedule(fa.FA_SCHED_HOST_CHUNKS, v) == fa.FA_ERR_INVALID
     assert fa.fa_set_schedule(0, 1) == fa.FA_ERR_INVALID
-    assert fa.fa_set_schedule(4, 1) == fa.FA_ERR_INVALID
+    assert fa.fa_set_schedule(5, 1) == fa.FA_ERR_INVALID
     with fa.schedule(fa.FA_SCHED_FWD_SPLIT, 1):
         pass

@@ -19,7 +19,11 @@ def run_bwd(B, H, M, N, D, dtype, causal, scale, seed=0, std=1.0, fused=False):
     q, k, v, do = synth.attention_inputs(B, H, M, N, D, dtype, seed=seed, std=std, with_dout=True)
     qd, kd, vd, dod = (to_device(x, dtype) for x in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, scale, causal)
-    dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal, fused=fused)
+    if fused in (False, "pair"):  # fa_bwd, its D = 64 dK/dV kernel on single CTAs or on CTA pairs
+        with fa.schedule(fa.FA_SCHED_BWD_PAIR, 1 if fused == "pair" else 0):
+            dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
+    else:
+        dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal, fused=fused)
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
     return (q, k, v, do), to_f64(o), (to_f64(dq), to_f64(dk), to_f64(dv)), to_f64(delta)
 
@@ -42,8 +46,10 @@ def check(inputs, o_gpu, grads, delta, dtype, causal, scale, heads=None):
     return worst
 
 
-# fused: fa_bwd_ws (dQ formed in the dK/dV pass and accumulated in f32 for D = 64) instead of fa_bwd
-FUSED = pytest.mark.parametrize("fused", [False, True], ids=["3kernels", "fused"])
+# fused: fa_bwd_ws (dQ formed in the dK/dV pass and accumulated in f32 for D = 64) instead of fa_bwd;
+# "3kernels" / "pair": fa_bwd with its D = 64 dK/dV kernel on single CTAs / on CTA pairs (forced
+# either way; the same kernels at D = 128)
+FUSED = pytest.mark.parametrize("fused", [False, "pair", True], ids=["3kernels", "pair", "fused"])
 
 
 @FUSED
@@ -117,6 +123,43 @@ def test_backward_fused_matches_three_kernels():
         assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]), causal
         assert torch.equal(a[3], b[3])  # delta
         assert float((a[0].float() - b[0].float()).abs().max()) <= 4e-3, causal
+
+
+PAIR_SHAPES = [
+    # B, H, M, N: one key tile per pair with an empty second half, ragged tails, more pair items
+    # than pairs (the persistent loop), heads whose key range ends inside a pair
+    (1, 1, 128, 128),
+    (1, 1, 5, 700),
+    (2, 3, 700, 900),
+    (1, 2, 1024, 1024),
+    (4, 12, 512, 512),
+    (1, 3, 2048, 384),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("B,H,M,N", PAIR_SHAPES)
+def test_backward_pair_matches_single_cta(dtype, causal, B, H, M, N):
+    """fa_bwd's dK/dV on CTA pairs against the single-CTA kernel on the same inputs (the same
+    products, the same rounding points), then against the oracle."""
+    import torch
+    scale = 0.125
+    q, k, v, do = synth.attention_inputs(B, H, M, N, 64, dtype, seed=M + 3 * N + H, with_dout=True)
+    qd, kd, vd, dod = (to_device(x, dtype) for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, scale, causal)
+    with fa.schedule(fa.FA_SCHED_BWD_PAIR, 0):
+        a = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
+    with fa.schedule(fa.FA_SCHED_BWD_PAIR, 1):
+        b = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    # dK and dV: the same products with the same rounding points, bit for bit; delta: the same
+    # kernel; dQ: the same kernel, whose f32 sums can differ between runs in the last bit
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
+    assert float((a[0].float() - b[0].float()).abs().max()) <= 1e-3 * max(1.0, float(a[0].float().abs().max()))
+    heads = [(0, 0), (B - 1, H - 1)]
+    check((q, k, v, do), to_f64(o), (to_f64(b[0]), to_f64(b[1]), to_f64(b[2])), to_f64(b[3]), dtype, causal,
+          scale, heads=heads)
 
 
 SPLIT_SHAPES = [
