@@ -1795,6 +1795,7 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (D == 64 && sp.pair) return launch_bwd_dq64_pair(Q, K, V, dO, LSE, delta, dQ, BH, M, N, scale, CAUSAL, dtype, ctx);
   {
     auto kern = bwd_dq_kernel<D, BF16, CAUSAL>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, OvCfg<D>::kSmem);

@@ -468,6 +468,394 @@ __global__ void __launch_bounds__(kPThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------------------- dQ on pairs
+// The dQ kernel of the three-kernel backward ("06: Fused attention", attn_bwd_dq: a CTA owns query
+// rows and walks the key blocks; S = Q K^T, dP = dO V^T, dS = P o (dP - delta), dQ = scale dS K) on
+// CTA pairs: the pair owns 256 queries of one head, 128 in each CTA, and walks the key blocks of 128
+// once for both.
+//   S   = Q K^T    A: each CTA's Q tile;  B: K's 128 rows split, keys 0-63 in rank 0, 64-127 in rank 1
+//   dP  = dO V^T   the same with dO and V
+//   dQ += dS K     A: dS in each CTA's tensor memory;  B: K's 64 columns split, 0-31 in rank 0, 32-63
+//                  in rank 1 (MN-major, each half in the first 64 bytes of 128-byte rows)
+// A key block is streamed once per 256 queries (its row halves by one CTA each, its column halves
+// by one CTA each), where the single-CTA kernel streams it once per 128.
+constexpr int kQStages = 4;
+constexpr int kQStage = 2 * kPRowHalf + kChunkB;  // K and V row halves, K column half
+constexpr uint32_t kQStageTx = static_cast<uint32_t>(kQStage);
+
+struct PairDqHdr {
+  unsigned long long fixed_full, fixed_empty, peer_fixed;
+  unsigned long long full[kQStages], empty[kQStages], peer_full[kQStages];
+  unsigned long long s_full, dp_full, free2, acc_full;  // MMA -> compute, committed to both CTAs
+  unsigned long long sig1, sig2;                        // rank 0: compute warps of both CTAs -> MMA
+  unsigned long long mma_done[2];
+  uint32_t tmem_base;
+  int abort_flag;
+};
+constexpr uint32_t kQHdrBytes = (sizeof(PairDqHdr) + 127u) & ~127u;
+constexpr int kQSmem = 1024 + static_cast<int>(kQHdrBytes) + 2 * kChunkB + kQStages * kQStage;
+static_assert(kQSmem <= 232448, "shared memory budget");
+
+// TMEM: S [0,128), dP [128,256), dS packed [256,320), dQ [320,384), in both CTAs.
+template <bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kPThreads, 1)
+    bwd_dq64_pair_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmdO,
+                         const __grid_constant__ CUtensorMap tmKr, const __grid_constant__ CUtensorMap tmVr,
+                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmKv,
+                         int have_views, const float* __restrict__ LSE, const float* __restrict__ delta,
+                         uint16_t* __restrict__ dQ, int BH, int M, int N, float scale, DevStatus* status,
+                         unsigned long long budget_ns) {
+  constexpr int D = 64;
+  constexpr uint32_t cS = 0, cdP = 128, cdS = 256, cdQ = 320;
+  extern __shared__ uint8_t smem_raw[];
+  PairDqHdr* hdr = reinterpret_cast<PairDqHdr*>(smem_raw);
+  const uint32_t data = (ptx::smem_u32(smem_raw) + kQHdrBytes + 1023u) & ~1023u;
+  const uint32_t sQ = data, sdO = data + kChunkB;
+  auto stage = [&](int st) { return data + 2 * kChunkB + st * kQStage; };
+  auto sKr = [&](int st) { return stage(st); };
+  auto sVr = [&](int st) { return stage(st) + kPRowHalf; };
+  auto sKc = [&](int st) { return stage(st) + 2 * kPRowHalf; };
+  const uint32_t rank = ptx::cluster_rank();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nkb = (N + kT - 1) / kT, nqb2 = (M + 2 * kT - 1) / (2 * kT);
+  const int items = BH * nqb2;
+  const float sl2 = fmaxf(fabsf(scale), 1e-30f) * kLog2eB;
+  const uint32_t neg_a = scale < 0.f ? ptx::kNegateA : 0u;
+  auto item = [&](int w) {
+    BwdItem it;
+    const int qb2_rev = w / BH;  // causal: the heaviest (last) pairs of query tiles first
+    it.bh = w - qb2_rev * BH;
+    const int qb2 = CAUSAL ? nqb2 - 1 - qb2_rev : qb2_rev;
+    it.r0 = qb2 * 2 * kT + static_cast<int>(rank) * kT;  // this CTA's 128 queries
+    it.lo = 0;
+    it.hi = CAUSAL ? min(nkb, (qb2 * 2 * kT + 2 * kT - 1) / kT + 1) : nkb;  // up to the pair's last query
+    return it;
+  };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&hdr->fixed_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->fixed_empty), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->peer_fixed), 1);
+    for (int st = 0; st < kQStages; ++st) {
+      ptx::mbar_init(ptx::smem_u32(&hdr->full[st]), 1);
+      ptx::mbar_init(ptx::smem_u32(&hdr->empty[st]), 1);
+      ptx::mbar_init(ptx::smem_u32(&hdr->peer_full[st]), 1);
+    }
+    ptx::mbar_init(ptx::smem_u32(&hdr->s_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->dp_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->free2), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->acc_full), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->sig1), 16);
+    ptx::mbar_init(ptx::smem_u32(&hdr->sig2), 16);
+    ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[1]), 1);
+    hdr->abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kPWarpMma) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&hdr->tmem_base), 512);
+    ptx::tmem_relinquish_pair();
+  }
+  if (warp == kPWarpProd && lane == 0) {
+    ptx::prefetch_tmap(&tmQ);
+    ptx::prefetch_tmap(&tmdO);
+    ptx::prefetch_tmap(&tmKr);
+    ptx::prefetch_tmap(&tmVr);
+    ptx::prefetch_tmap(rank == 0 && have_views ? &tmKv : &tmK);
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers initialised, the pair's tensor memory allocated
+  ptx::tc_fence_after();
+  const uint32_t tmem = hdr->tmem_base;
+  ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDq};
+  // launched as a programmatic dependent of the dK/dV kernel: global memory only after it completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
+
+  if (warp == kPWarpProd) {
+    // ------------------------------------------------------------ TMA producer (lane 0)
+    if (lane == 0) {
+      const CUtensorMap* mKc = rank == 0 ? (have_views ? &tmKv : &tmK) : &tmK;
+      const int xc = rank == 0 ? 0 : 32;
+      uint32_t it_s = 0;
+      int n_item = 0;
+      bool ok = true;
+      for (int r = 0, w = pair_item_of_round<CAUSAL>(0, items); w < items && ok;
+           w = pair_item_of_round<CAUSAL>(++r, items), ++n_item) {
+        const BwdItem itm = item(w);
+        if (!ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_empty), (n_item & 1) ^ 1, wc, 10)) break;
+        const uint32_t ff = ptx::smem_u32(&hdr->fixed_full);
+        ptx::mbar_arrive_expect_tx(ff, 2 * kChunkB);
+        ptx::tma_load_3d(sQ, &tmQ, ff, 0, itm.r0, itm.bh);
+        ptx::tma_load_3d(sdO, &tmdO, ff, 0, itm.r0, itm.bh);
+        for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
+          const int st = it_s % kQStages;
+          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / kQStages) & 1u) ^ 1u, wc, 11);
+          if (!ok) break;
+          const uint32_t fb = ptx::smem_u32(&hdr->full[st]);
+          ptx::mbar_arrive_expect_tx(fb, kQStageTx);
+          const int yr = j * kT + static_cast<int>(rank) * (kT / 2);
+          ptx::tma_load_3d(sKr(st), &tmKr, fb, 0, yr, itm.bh);
+          ptx::tma_load_3d(sVr(st), &tmVr, fb, 0, yr, itm.bh);
+          ptx::tma_load_3d(sKc(st), mKc, fb, xc, j * kT, itm.bh);
+        }
+      }
+      if (hdr->abort_flag) {  // let issued copies land before shared memory is released
+        for (uint32_t k = it_s > (uint32_t)kQStages ? it_s - kQStages : 0u; k < it_s; ++k)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % kQStages]), (k / kQStages) & 1u, 100000000ull);
+      }
+    }
+  } else if ((warp == kPWarpMma || warp == kPWarpGrad) && rank == 0) {
+    // ------------------------------------------------------------ MMA issuers of the pair (lane 0)
+    if (lane == 0) {
+      const bool scores = warp == kPWarpMma;
+      constexpr uint32_t fmt = BF16 ? ptx::kFmtBF16 : ptx::kFmtF16;
+      const uint32_t id_dp = ptx::idesc_f32acc(2 * kT, kT, fmt, fmt, false, false);  // dP: never negated
+      const uint32_t id_s = id_dp | neg_a;
+      constexpr uint32_t id_g = ptx::idesc_f32acc(2 * kT, D, fmt, fmt, false, true);
+      uint32_t it_s = 0, n1 = 0, n2 = 0;
+      int n_item = 0;
+      bool ok = true;
+      auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+        return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
+      };
+      auto commit = [&](unsigned long long* bar) { ptx::tc_commit_pair(ptx::smem_u32(bar)); };
+      auto stage_ready = [&](uint32_t k) {
+        const uint32_t ph = (k / kQStages) & 1u;
+        return wait(&hdr->full[k % kQStages], ph, 21) && wait(&hdr->peer_full[k % kQStages], ph, 24);
+      };
+      auto qk = [&](uint32_t k) {  // S = Q K^T over the pair's 256 queries
+        const int st = k % kQStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss_pair(tmem + cS, kmajor_desc(sQ, ks), kmajor_desc(sKr(st), ks), id_s, ks > 0);
+        commit(&hdr->s_full);
+      };
+      auto dov = [&](uint32_t k) {  // dP = dO V^T
+        const int st = k % kQStages;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          ptx::mma_f16_ss_pair(tmem + cdP, kmajor_desc(sdO, ks), kmajor_desc(sVr(st), ks), id_dp, ks > 0);
+        commit(&hdr->dp_full);
+      };
+      for (int r = 0, w = pair_item_of_round<CAUSAL>(0, items); w < items && ok;
+           w = pair_item_of_round<CAUSAL>(++r, items), ++n_item) {
+        const BwdItem itm = item(w);
+        if (scores) {
+          if (!wait(&hdr->fixed_full, n_item & 1, 20) || !wait(&hdr->peer_fixed, n_item & 1, 25)) break;
+          if (itm.lo < itm.hi) {
+            ok = stage_ready(it_s);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            qk(it_s);
+            dov(it_s);
+            if (itm.lo + 1 < itm.hi && !stage_ready(it_s + 1)) break;
+          }
+        }
+        for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
+          const int st = it_s % kQStages;
+          const bool more = j + 1 < itm.hi;
+          if (scores) {
+            // S(j) read in both CTAs
+            ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            if (more) qk(it_s + 1);
+          }
+          // dP(j) read and dS(j) stored in both CTAs
+          ok = wait(&hdr->sig2, (n2++) & 1u, 23);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          if (scores) {
+            if (more) dov(it_s + 1);
+            if (j + 2 < itm.hi && !stage_ready(it_s + 2)) {
+              ok = false;
+              break;
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < kT / 16; ++ks)  // dQ += dS K
+              ptx::mma_f16_ts_pair(tmem + cdQ, tmem + cdS + ks * 8, mnmajor_desc(sKc(st), ks), id_g,
+                                   (j > itm.lo || ks > 0));
+            commit(&hdr->free2);
+            commit(&hdr->empty[st]);
+          }
+        }
+        if (!ok) break;
+        commit(scores ? &hdr->fixed_empty : &hdr->acc_full);
+      }
+      const int me = scores ? 0 : 1;
+      commit(&hdr->mma_done[me]);
+      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[me]), 0u, 1000000000ull);
+    }
+  } else if (warp == kPWarpGrad && rank == 1) {
+    // ------------------------------------------------------------ relay (lane 0): rank 1's loads landed
+    if (lane == 0) {
+      const uint32_t peer_fixed = ptx::peer_addr(ptx::smem_u32(&hdr->peer_fixed), 0);
+      uint32_t it_s = 0;
+      int n_item = 0;
+      bool ok = true;
+      for (int r = 0, w = pair_item_of_round<CAUSAL>(0, items); w < items && ok;
+           w = pair_item_of_round<CAUSAL>(++r, items), ++n_item) {
+        const BwdItem itm = item(w);
+        ok = ptx::mbar_wait(ptx::smem_u32(&hdr->fixed_full), n_item & 1, wc, 26);
+        if (!ok) break;
+        ptx::mbar_arrive_remote(peer_fixed);
+        for (int j = itm.lo; j < itm.hi && ok; ++j, ++it_s) {
+          const int st = it_s % kQStages;
+          ok = ptx::mbar_wait(ptx::smem_u32(&hdr->full[st]), (it_s / kQStages) & 1u, wc, 27);
+          if (ok) ptx::mbar_arrive_remote(ptx::peer_addr(ptx::smem_u32(&hdr->peer_full[st]), 0));
+        }
+      }
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------ compute warps: one query row per thread
+    const int quarter = warp & 3, half = warp >> 2;
+    const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's key columns [c0, c0 + 64)
+    const uint32_t sig1 = ptx::peer_addr(ptx::smem_u32(&hdr->sig1), 0);
+    const uint32_t sig2 = ptx::peer_addr(ptx::smem_u32(&hdr->sig2), 0);
+    uint32_t nb = 0;
+    int n_item = 0;
+    bool ok = true;
+    auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
+      const bool r = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site));
+      ptx::tc_fence_after();
+      return r;
+    };
+    auto signal = [&](uint32_t cl_bar) {
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_remote(cl_bar);
+    };
+    for (int r = 0, w = pair_item_of_round<CAUSAL>(0, items); w < items && ok;
+         w = pair_item_of_round<CAUSAL>(++r, items), ++n_item) {
+      const BwdItem itm = item(w);
+      const int row = itm.r0 + quarter * 32 + lane;
+      const bool valid = row < M;
+      const size_t g = static_cast<size_t>(itm.bh) * M + (valid ? row : 0);
+      const float nlse2 = valid ? -LSE[g] * kLog2eB : -INFINITY;  // past M: P = 0
+      const float ndlt = valid ? -delta[g] : 0.f;
+      for (int j = itm.lo; j < itm.hi; ++j, ++nb) {
+        ok = wait_all(&hdr->s_full, nb & 1u, 30);
+        if (!ok) break;
+        const int kb = j * kT + static_cast<int>(c0);  // first key of this warp's columns
+        const bool edge = kb + 64 > N || (CAUSAL && kb + 63 > row);
+        float p[64];
+        {
+          uint32_t s[64];
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0, s);
+          ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
+          ptx::tmem_wait_ld32(s);
+          ptx::tmem_wait_ld32(s + 32);
+          const float2 c2 = make_float2(sl2, sl2), nl2 = make_float2(nlse2, nlse2);
+#pragma unroll
+          for (int k = 0; k < 64; k += 2) {
+            const float2 x = ptx::ffma2(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), c2, nl2);
+            p[k] = ptx::ex2(x.x);
+            p[k + 1] = ptx::ex2(x.y);
+            if (edge) {
+              if (kb + k >= N || (CAUSAL && kb + k > row)) p[k] = 0.f;
+              if (kb + k + 1 >= N || (CAUSAL && kb + k + 1 > row)) p[k + 1] = 0.f;
+            }
+          }
+        }
+        signal(sig1);  // S(j) read: the next S may be computed
+        ok = wait_all(&hdr->dp_full, nb & 1u, 31);
+        if (ok && nb > 0) ok = wait_all(&hdr->free2, (nb - 1u) & 1u, 32);  // dS(j-1) read by dQ's MMA
+        if (!ok) break;
+        const float2 nd2 = make_float2(ndlt, ndlt);
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t dp[32];
+          ptx::tmem_ld32(tmem + lane_sel + cdP + c0 + c, dp);
+          ptx::tmem_wait_ld32(dp);
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float2 t = ptx::fadd2(make_float2(__uint_as_float(dp[2 * k]), __uint_as_float(dp[2 * k + 1])), nd2);
+            const float2 ds = ptx::fmul2(make_float2(p[c + 2 * k], p[c + 2 * k + 1]), t);
+            pk[k] = pack2<BF16>(ds.x, ds.y);
+          }
+          ptx::tmem_st16(tmem + lane_sel + cdS + (c0 + c) / 2, pk);
+        }
+        ptx::tmem_wait_st();
+        signal(sig2);
+      }
+      if (!ok) break;
+      ok = wait_all(&hdr->acc_full, n_item & 1, 33);
+      if (!ok) break;
+      const bool none = itm.lo >= itm.hi;
+      uint32_t a[32];
+      ptx::tmem_ld32(tmem + lane_sel + cdQ + 32 * half, a);
+      ptx::tmem_wait_ld32(a);
+      uint32_t h[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k)
+        h[k] = none ? 0u : pack2<BF16>(__uint_as_float(a[2 * k]) * scale, __uint_as_float(a[2 * k + 1]) * scale);
+      if (valid) {
+        uint4* d4 = reinterpret_cast<uint4*>(dQ + g * D + 32 * half);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+      }
+      ptx::tc_fence_before();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // neither CTA frees the pair's tensor memory while the other may still use it
+  if (warp == kPWarpMma) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+template <bool BF16, bool CAUSAL>
+cudaError_t launch_dq_pair_t(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                             const float* delta, void* dQ, int BH, int M, int N, float scale, int dtype,
+                             const LaunchCtx& ctx) {
+  constexpr int D = 64;
+  CUtensorMap mq, mdo, mkr, mvr, mk, mkv;
+  if (!make_tmap_3d(&mq, Q, dtype, D, M, BH, 64, kT) || !make_tmap_3d(&mdo, dO, dtype, D, M, BH, 64, kT) ||
+      !make_tmap_3d(&mkr, K, dtype, D, N, BH, 64, kT / 2) || !make_tmap_3d(&mvr, V, dtype, D, N, BH, 64, kT / 2) ||
+      !make_tmap_3d(&mk, K, dtype, D, N, BH, 64, kT))
+    return cudaErrorInvalidValue;
+  const int have_views = make_tmap_3d_view(&mkv, K, dtype, 32, D, N, BH, 64, kT);
+  if (!have_views) mkv = mk;
+  auto kern = bwd_dq64_pair_kernel<BF16, CAUSAL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kQSmem;
+  cfg.stream = ctx.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cfg.gridDim = dim3(2 * static_cast<unsigned>(ctx.num_sms / 2));
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs = n > 0 ? n : 1;
+  }
+  const long long items = static_cast<long long>(BH) * ((M + 2 * kT - 1) / (2 * kT));
+  const int pairs = static_cast<int>(items < max_pairs ? items : max_pairs);
+  cfg.gridDim = dim3(2 * static_cast<unsigned>(pairs));
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, mq, mdo, mkr, mvr, mk, mkv, have_views, LSE, delta,
+                            static_cast<uint16_t*>(dQ), BH, M, N, scale, ctx.status, ctx.wait_budget_ns);
+}
+
 template <bool BF16, bool CAUSAL>
 cudaError_t launch_pair_t(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                           const float* delta, void* dK, void* dV, int BH, int M, int N, float scale, int dtype,
@@ -530,6 +918,16 @@ cudaError_t launch_bwd_dkdv64_pair(const void* Q, const void* K, const void* V, 
   if (!bf && causal) return launch_pair_t<false, true>(Q, K, V, dO, LSE, delta, dK, dV, BH, M, N, scale, dtype, ctx);
   if (bf && !causal) return launch_pair_t<true, false>(Q, K, V, dO, LSE, delta, dK, dV, BH, M, N, scale, dtype, ctx);
   return launch_pair_t<true, true>(Q, K, V, dO, LSE, delta, dK, dV, BH, M, N, scale, dtype, ctx);
+}
+
+cudaError_t launch_bwd_dq64_pair(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                                 const float* delta, void* dQ, int BH, int M, int N, float scale, bool causal,
+                                 int dtype, const LaunchCtx& ctx) {
+  const bool bf = dtype == kBF16;
+  if (!bf && !causal) return launch_dq_pair_t<false, false>(Q, K, V, dO, LSE, delta, dQ, BH, M, N, scale, dtype, ctx);
+  if (!bf && causal) return launch_dq_pair_t<false, true>(Q, K, V, dO, LSE, delta, dQ, BH, M, N, scale, dtype, ctx);
+  if (bf && !causal) return launch_dq_pair_t<true, false>(Q, K, V, dO, LSE, delta, dQ, BH, M, N, scale, dtype, ctx);
+  return launch_dq_pair_t<true, true>(Q, K, V, dO, LSE, delta, dQ, BH, M, N, scale, dtype, ctx);
 }
 
 }  // namespace fa

@@ -385,9 +385,10 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   FA_TRY(make_ctx(&ctx, stream));
   BwdSplit sp{};
   if (dQacc != nullptr && split_ws != nullptr && use_bwd_split(B * H, M, N, D, causal, ctx.num_sms)) sp.ws = split_ws;
-  // fa_bwd's dK/dV kernel at D = 64 on CTA pairs: by default for non-causal calls (where it
-  // measured as fast or faster); causal calls keep single CTAs (a pair's item of 256 keys starts at
-  // the query block of its first key, so the second CTA's first block is wholly masked)
+  // fa_bwd's dK/dV and dQ kernels at D = 64 on CTA pairs: by default for non-causal calls (where
+  // they measured as fast or faster); causal calls keep single CTAs (a pair's 256 rows walk the
+  // blocks of its later half, so the earlier CTA gets one wholly masked block per item, and the
+  // items are coarser to balance)
   const int pair_forced = g_sched_bwd_pair.load();
   sp.pair = dQacc == nullptr && D == 64 && (pair_forced == 1 || (pair_forced == -1 && causal == 0));
   cudaError_t e =

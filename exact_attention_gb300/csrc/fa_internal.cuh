@@ -100,7 +100,7 @@ cudaError_t launch_fwd_fp8(const Fp8Ws& w, void* O, float* LSE, int BH, int M, i
 // partial dK/dV slots (two per SM) then num_sms * 8 counters; ws == nullptr runs whole key tiles.
 struct BwdSplit {
   float* ws = nullptr;
-  bool pair = false;  // three-kernel path, D = 64: the dK/dV kernel on CTA pairs
+  bool pair = false;  // three-kernel path, D = 64: the dK/dV and dQ kernels on CTA pairs
 };
 size_t bwd_fused_split_bytes(int num_sms);
 
@@ -109,6 +109,10 @@ size_t bwd_fused_split_bytes(int num_sms);
 cudaError_t launch_bwd_dkdv64_pair(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
                                    const float* delta, void* dK, void* dV, int BH, int M, int N, float scale,
                                    bool causal, int dtype, const LaunchCtx& ctx);
+// dQ with D = 64 on CTA pairs, launched as a programmatic dependent of the dK/dV kernel.
+cudaError_t launch_bwd_dq64_pair(const void* Q, const void* K, const void* V, const void* dO, const float* LSE,
+                                 const float* delta, void* dQ, int BH, int M, int N, float scale, bool causal,
+                                 int dtype, const LaunchCtx& ctx);
 
 // dQacc == nullptr: delta, dK/dV and dQ kernels; else (D = 64) delta, one fused dK/dV/dQ kernel
 // that accumulates dQ in dQacc (B*H*M*D f32), and a conversion of dQacc into dQ.

@@ -19,7 +19,7 @@ def run_bwd(B, H, M, N, D, dtype, causal, scale, seed=0, std=1.0, fused=False):
     q, k, v, do = synth.attention_inputs(B, H, M, N, D, dtype, seed=seed, std=std, with_dout=True)
     qd, kd, vd, dod = (to_device(x, dtype) for x in (q, k, v, do))
     o, lse = fa.forward(qd, kd, vd, scale, causal)
-    if fused in (False, "pair"):  # fa_bwd, its D = 64 dK/dV kernel on single CTAs or on CTA pairs
+    if fused in (False, "pair"):  # fa_bwd, its D = 64 gradient kernels on single CTAs or on CTA pairs
         with fa.schedule(fa.FA_SCHED_BWD_PAIR, 1 if fused == "pair" else 0):
             dq, dk, dv, delta = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
     else:
@@ -47,8 +47,8 @@ def check(inputs, o_gpu, grads, delta, dtype, causal, scale, heads=None):
 
 
 # fused: fa_bwd_ws (dQ formed in the dK/dV pass and accumulated in f32 for D = 64) instead of fa_bwd;
-# "3kernels" / "pair": fa_bwd with its D = 64 dK/dV kernel on single CTAs / on CTA pairs (forced
-# either way; the same kernels at D = 128)
+# "3kernels" / "pair": fa_bwd with its D = 64 dK/dV and dQ kernels on single CTAs / on CTA pairs
+# (forced either way; the same kernels at D = 128)
 FUSED = pytest.mark.parametrize("fused", [False, "pair", True], ids=["3kernels", "pair", "fused"])
 
 
@@ -141,8 +141,8 @@ PAIR_SHAPES = [
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("B,H,M,N", PAIR_SHAPES)
 def test_backward_pair_matches_single_cta(dtype, causal, B, H, M, N):
-    """fa_bwd's dK/dV on CTA pairs against the single-CTA kernel on the same inputs (the same
-    products, the same rounding points), then against the oracle."""
+    """fa_bwd's dK/dV and dQ kernels on CTA pairs against the single-CTA kernels on the same inputs
+    (the same products, the same rounding points), then against the oracle."""
     import torch
     scale = 0.125
     q, k, v, do = synth.attention_inputs(B, H, M, N, 64, dtype, seed=M + 3 * N + H, with_dout=True)
@@ -154,7 +154,7 @@ def test_backward_pair_matches_single_cta(dtype, causal, B, H, M, N):
         b = fa.backward(qd, kd, vd, o, dod, lse, scale, causal)
     assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
     # dK and dV: the same products with the same rounding points, bit for bit; delta: the same
-    # kernel; dQ: the same kernel, whose f32 sums can differ between runs in the last bit
+    # kernel; dQ: the same products, whose f32 sums can differ between runs in the last bit
     assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2]) and torch.equal(a[3], b[3])
     assert float((a[0].float() - b[0].float()).abs().max()) <= 1e-3 * max(1.0, float(a[0].float().abs().max()))
     heads = [(0, 0), (B - 1, H - 1)]
