@@ -370,9 +370,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 // quarter w % 4 (one tile row per thread) and the half w / 4 of the streamed
 // block's 128 columns. Per block the compute warps signal twice: once the scores
 // are read and P is formed (dK/dV: P^T stored), once dP is read and dS stored.
-// Two MMA-issuing threads share the work (a thread that has issued tcgen05 work
-// is slow to reach its next barrier operation, so one issuer left the tensor
-// pipe idle): warp 9 issues the next block's scores at the first signal and its
+// Two MMA-issuing threads share the work (an MMA instruction holds its issuing
+// thread until the tensor pipe accepts it, about the time the pipe's earlier
+// work takes, so one issuer left the tensor pipe idle): warp 9 issues the next block's scores at the first signal and its
 // dP at the second; warp 10 issues the gradient products of this block at each
 // signal and releases the streamed stage (warp 9's products on it completed
 // before the compute warps read them). Each barrier's next phase depends on work

@@ -373,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 0; j < nb && ok; ++j) {
           // K_{j+2} is normally long loaded: its barrier is checked while the softmax forms
-          // P_t(j), since a barrier operation right after tcgen05 work is slow for this thread
+          // P_t(j), not between the softmax's signal and the MMAs it releases
           if (j + 2 < nb) {
             ok = kv_ready(j + 2);
             if (!ok) break;
