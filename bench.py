@@ -660,11 +660,19 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
                 desc + " through fa_bwd_ws (delta, fused dK/dV/dQ, dQ conversion; FLOP = 2.5 x forward)", flops, t,
                 f"bwd_fused64_kernel<f16,{tag}>")
             dws = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
-            t = timed(lambda: check(fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, dws, B, H, M, M, 64, 0.5, causal,
-                                              fa.FA_F16, stream), "fa_bwd"))
+            run3 = lambda: check(fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, dws, B, H, M, M, 64, 0.5, causal,
+                                           fa.FA_F16, stream), "fa_bwd")
+            t = timed(run3)  # automatic schedule: dK/dV and dQ on CTA pairs when not causal
+            kern3 = "bwd_dkdv64_kernel + bwd_dq_kernel" if causal else "bwd_dkdv64_pair_kernel + bwd_dq64_pair_kernel"
             out[f"{name0}_bwd_3kernels_{tag}"] = tensor_entry(
                 desc + " through fa_bwd (delta, dK/dV, dQ kernels; FLOP = 2.5 x forward)", flops, t,
-                f"bwd_dkdv64_kernel + bwd_dq_kernel<f16,{tag}>")
+                f"{kern3}<f16,{tag}>")
+            if not causal:
+                with fa.schedule(fa.FA_SCHED_BWD_PAIR, 0):
+                    t = timed(run3)
+                out[f"{name0}_bwd_3kernels_single_cta_{tag}"] = tensor_entry(
+                    desc + " through fa_bwd with single-CTA dK/dV and dQ kernels (FLOP = 2.5 x forward)", flops, t,
+                    f"bwd_dkdv64_kernel + bwd_dq_kernel<f16,{tag}>")
     # bf16 decode B8 H32 N32768 D128 at n_splits 16 and 256 (64 is the main line's)
     d = DEC
     qdec = dev(synth.decode_query(d["B"], d["H"], d["D"], d["dtype"], 0), "bf16")
