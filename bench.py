@@ -391,7 +391,7 @@ def run_ours(args):
 
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     peak_bw = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    # ---- f32 forward on its own (one head, M=N=4096, D=64, 3xTF32), L2 flushed before each call
+    # ---- f32 forward on its own (one head, M=N=4096, D=64), L2 flushed before each call
     f32 = None
     if world == 1:
         q32, k32, v32 = synth.attention_inputs(1, 1, 4096, 4096, 64, "f32", seed=0)
@@ -420,12 +420,13 @@ def run_ours(args):
         check(fa.fa_last_status(stream), "f32 forward")
         t32 = sum(a.elapsed_time(b) for a, b in recs32) / len(recs32) / 1e3
         tf32 = 4.0 * 4096 * 4096 * 64 / t32 / 1e12
-        peak32 = peak_tf * 1.1 / 2.25 / 3.0
-        f32 = {"config": "f32 forward, 1 head, M=N=4096, D=64, scale 0.125 (3xTF32; key blocks of each query tile shared by 4 SMs, merged by the part that finishes last)", "value": round(tf32, 2),
+        peak32 = peak_tf / 6.0
+        f32 = {"config": "f32 forward, 1 head, M=N=4096, D=64, scale 0.125 through fa_fwd_ws (operands split into three bf16 parts, six products; key blocks of each query tile shared by 4 SMs, merged by the part that finishes last; the split prologue is inside the timed call)", "value": round(tf32, 2),
                "unit": "TFLOP/s", "us_per_call": round(t32 * 1e6, 1),
-               "roofline": {"kernel": "fwd_f32_kernel<non-causal>", "bound": "tensor", "achieved": round(tf32, 2),
-                            "peak": round(peak32, 1), "unit": "TFLOP/s", "frac": round(tf32 / peak32, 4),
-                            "peak_source": f"{peaks_src} bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products",
+               "roofline": {"kernel": "f32_presplit_kernel + fwd_f32ws_kernel<non-causal>", "bound": "tensor",
+                            "achieved": round(tf32, 2), "peak": round(peak32, 1), "unit": "TFLOP/s",
+                            "frac": round(tf32 / peak32, 4),
+                            "peak_source": f"{peaks_src} bf16 burst / 6 products (each f32 product is six bf16 ones)",
                             "traffic": None}}
 
     # ---- grouped-query decode on its own: four query rows per K/V head of the same cache,
@@ -602,8 +603,8 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
         flops = 4.0 * B * H * M * N * D / (2 if causal else 1)
         peak, note = peak_tf, None
         if dtype == "f32":
-            peak = peak_tf * 1.1 / 2.25 / 3.0
-            note = f"{peaks_src} bf16 burst x nominal tf32/bf16 (1.1/2.25) / 3 products"
+            peak = peak_tf / 6.0
+            note = f"{peaks_src} bf16 burst / 6 products (each f32 product is six bf16 ones)"
         out[name] = tensor_entry(desc, flops, t, kernel, peak, note)
 
     # fp16 forward, B4 H12 D64, M = N over {512, 1024, 2048}; bf16 and causal at 2048
@@ -634,7 +635,8 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
             peak_tf * 2.0, f"{peaks_src} bf16 burst x nominal fp8/bf16 (4.5/2.25)")
     # f32, one head, 256^2 and 4096^2 (3xTF32)
     forward_entry("fwd_f32_N256", 1, 1, 256, 256, 64, "f32", False, 0.125,
-                  "f32 forward 1 head Nq=Nk=256 D64 scale 0.125 (3xTF32)", "fwd_f32_kernel<non-causal>")
+                  "f32 forward 1 head Nq=Nk=256 D64 scale 0.125 (fa_fwd_ws: three bf16 parts, six products)",
+                  "f32_presplit_kernel + fwd_f32ws_kernel<non-causal>")
     # fp16 forward + backward, Z1 H2 N1024 D64, sm_scale 0.5, causal and not
     for causal in (False, True):
         tag = "causal" if causal else "noncausal"
@@ -759,6 +761,8 @@ PROFILE_CASES = {
     "bwd": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # Q/K/V/O/dO 0.34 GB (fused pass)
     "bwd3": dict(B=8, H=16, M=2048, N=2048, D=64, dtype="f16"),  # the same through the three kernels
     "decode_rows": dict(B=8, H=8, N=32768, D=128, n_splits=64, rows=4, dtype="bf16"),  # K/V 1.07 GB
+    "f32": dict(B=1, H=1, M=4096, N=4096, D=64, dtype="f32"),  # the f32 workload (L2-resident, 3 MB)
+    "f32_big": dict(B=4, H=12, M=2048, N=2048, D=64, dtype="f32"),  # Q/K/V 100 MB, split planes 200 MB
 }
 
 
@@ -777,6 +781,13 @@ def run_profile(kind: str, launches: int = 5):
         q = torch.randn(shp, generator=g, device="cuda").half()
         k = torch.randn(shp, generator=g, device="cuda").half()
         v = torch.randn(shp, generator=g, device="cuda").half()
+        o = torch.empty_like(q)
+        lse = torch.empty(shp[:3], device="cuda")
+        for _ in range(launches):
+            fa.forward(q, k, v, 0.125, False, out=o, lse=lse)
+    elif kind in ("f32", "f32_big"):
+        shp = (c["B"], c["H"], c["M"], c["D"])
+        q, k, v = (torch.randn(shp, generator=g, device="cuda") for _ in range(3))
         o = torch.empty_like(q)
         lse = torch.empty(shp[:3], device="cuda")
         for _ in range(launches):

@@ -200,6 +200,8 @@ using namespace fa;
 
 namespace {
 
+size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
+
 // Schedule choices fixed by fa_set_schedule (-1: automatic). Process-wide.
 std::atomic<int> g_sched_fwd_split{-1};
 std::atomic<int> g_sched_bwd_split{-1};
@@ -338,19 +340,23 @@ fa_status fwd_impl(const void* Q, const void* K, const void* V, void* O, float* 
     }
   }
   int parts = 1;
+  size_t split_bytes = 0;
   if (dtype == FA_F32 && ws != nullptr && D == 64) {
     parts = fwd_f32_parts(B * H, M, N, ctx.num_sms);
-    const size_t need = fwd_f32_split_bytes(B * H, M, parts);
-    if (parts > 1) {
-      FA_TRY(check_ptr(ws, "workspace"));
-      if (ws_bytes < need) return fail(FA_ERR_INVALID, "%s: workspace of %zu bytes, %zu needed", name, ws_bytes, need);
-    }
+    split_bytes = align256(fwd_f32_split_bytes(B * H, M, parts));
+    const size_t need = split_bytes + fwd_f32_presplit_bytes(B * H, N);
+    FA_TRY(check_ptr(ws, "workspace"));
+    if (ws_bytes < need) return fail(FA_ERR_INVALID, "%s: workspace of %zu bytes, %zu needed", name, ws_bytes, need);
   }
   cudaError_t e;
   if (dtype == FA_F32) {
     uint32_t ep = 0;
     if (parts > 1) ep = next_epoch();
-    e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, parts, static_cast<float*>(ws), ep, ctx);
+    if (ws != nullptr && D == 64)  // operands split once by a prologue, pipelined main kernel
+      e = launch_fwd_f32_presplit(Q, K, V, O, LSE, B * H, M, N, scale, causal != 0, parts, static_cast<float*>(ws),
+                                  ep, static_cast<char*>(ws) + split_bytes, ctx);
+    else
+      e = launch_fwd_f32(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, 1, nullptr, 0, ctx);
   } else {
     e = launch_fwd_half(Q, K, V, O, LSE, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
   }
@@ -478,7 +484,9 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0) return 0;
   DevState* st = nullptr;
   if (device_state(&st) != FA_OK) return 0;
-  if (dtype == FA_F32 && D == 64) return fwd_f32_split_bytes(B * H, M, fwd_f32_parts(B * H, M, N, st->num_sms));
+  if (dtype == FA_F32 && D == 64)  // the split's partials, then K and V split into tf32 parts
+    return align256(fwd_f32_split_bytes(B * H, M, fwd_f32_parts(B * H, M, N, st->num_sms))) +
+           fwd_f32_presplit_bytes(B * H, N);
   if (!split_capable(D, dtype)) return 0;
   return fwd_d64_split_bytes(st->num_sms);
 }
@@ -690,8 +698,6 @@ fa_status host_pipe(HostPipe** out) {
   *out = &hp;
   return FA_OK;
 }
-
-size_t align256(size_t x) { return (x + 255u) & ~static_cast<size_t>(255u); }
 
 // Device workspace of fa_fwd_host: the forward's own workspace for the largest chunk, then
 // Q, K, V, O and LSE of the whole problem, each 256-byte aligned.

@@ -78,6 +78,14 @@ cudaError_t launch_fwd_half(const void* Q, const void* K, const void* V, void* O
 // launch, so counts an earlier launch left behind read as zero).
 int fwd_f32_parts(int BH, int M, int N, int num_sms);
 size_t fwd_f32_split_bytes(int BH, int M, int parts);
+constexpr int kF32SlotFloats = 64 * 128 + 2 * 128;  // one part's partial: O [64][128 rows], m, l
+// The f32 forward with a workspace (D = 64): a prologue kernel writes K's tf32 hi and lo parts and
+// V's transposed hi and lo parts into `presplit` (fwd_f32_presplit_bytes), then the main kernel
+// streams them (split_ws, parts, epoch as for launch_fwd_f32).
+size_t fwd_f32_presplit_bytes(int BH, int N);
+cudaError_t launch_fwd_f32_presplit(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M,
+                                    int N, float scale, bool causal, int parts, float* split_ws, uint32_t epoch,
+                                    void* presplit, const LaunchCtx& ctx);
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
                            int D, float scale, bool causal, int parts, float* ws, uint32_t epoch,
                            const LaunchCtx& ctx);

@@ -45,7 +45,7 @@ constexpr int kThreads32 = 320;     // softmax 0-3, split 4-7, producer 8, MMA 9
 constexpr int kWarpProd32 = 8, kWarpMma32 = 9;
 constexpr float kLog2e32 = 1.4426950408889634f;
 constexpr float kLn2_32 = 0.6931471805599453f;
-constexpr int kF32Slot = kD32 * 128 + 2 * 128;  // one part's partial: O [64][128 rows], m, l
+constexpr int kF32Slot = kF32SlotFloats;
 
 struct F32Hdr {
   unsigned long long q_full, q_split, q_empty;
@@ -532,7 +532,8 @@ int fwd_f32_parts(int BH, int M, int N, int num_sms) {
 size_t fwd_f32_split_bytes(int BH, int M, int parts) {
   if (parts <= 1) return 0;
   const size_t tiles = static_cast<size_t>((M + kBM32 - 1) / kBM32) * BH;
-  return tiles * parts * kF32Slot * sizeof(float) + tiles * 4 * sizeof(unsigned long long);  // slots, counters
+  // slots, then per tile one counter per softmax warp (4 here, 8 in the pipelined kernel)
+  return tiles * parts * kF32Slot * sizeof(float) + tiles * 8 * sizeof(unsigned long long);
 }
 
 cudaError_t launch_fwd_f32(const void* Q, const void* K, const void* V, void* O, float* LSE, int BH, int M, int N,
