@@ -469,6 +469,8 @@ def run_ours(args):
 
     launches_per_step = 1 + (3 if have_bwd else 0) + 2
     traffic = load_traffic()
+    if f32 is not None:
+        f32["roofline"]["traffic"] = traffic.get("f32")
     line = {
         "metric": METRIC,
         "value": round(fwd_tflops, 2),
