@@ -12,8 +12,10 @@
 //  * the softmax warps write the tile's query rows, split, into tensor memory, the A operand of
 //    S = Q K^T; eight softmax warps, two per row (32 keys of each block each);
 //  * S / P and the block partial of P V are double-buffered in tensor memory, so S(j+1) is computed
-//    while the softmax works on block j, and P(j) V(j) while it works on block j+1; the MMA thread
-//    issues QK(j+2) right behind PV(j).
+//    while the softmax works on block j, and P(j) V(j) while it works on block j+1; one thread
+//    issues the score products and another the P V products (one issuing thread reaches only half
+//    the tensor core's rate with N = 64 MMAs), the first writing S of a buffer again once P V of
+//    the block two back has read P there.
 // As in fwd_f32.cu every block's P V starts from zero in tensor memory and the softmax threads add
 // the block partials in registers with round-to-nearest adds (the tensor core's f32 accumulation
 // truncates). Tensor memory: Q parts at 0, 32, 64 (32 columns each, two bf16 per column); buffer b
@@ -31,8 +33,8 @@ constexpr int kDw = 64;
 constexpr int kPlaneW = kBNw * 128;       // 8 KB: 64 rows of 64 bf16 (128-byte swizzled rows)
 constexpr int kStagesW = 4;
 constexpr int kStageW = 6 * kPlaneW;      // K parts 0-2, V parts 0-2
-constexpr int kThreadsW = 320;            // softmax 0-7, producer 8, MMA 9
-constexpr int kWarpProdW = 8, kWarpMmaW = 9;
+constexpr int kThreadsW = 352;            // softmax 0-7, producer 8, MMA issuers 9 (S) and 10 (P V)
+constexpr int kWarpProdW = 8, kWarpMmaW = 9, kWarpPvW = 10;
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr float kLn2W = 0.6931471805599453f;
 constexpr uint32_t cQ = 0, cS = 128, cO = 384;  // Q part p at 32 p; buffer b: S at cS + 128 b, O at cO + 64 b
@@ -43,7 +45,7 @@ struct F32wHdr {
   unsigned long long s_full[2];   // S of buffer b computed
   unsigned long long p_full[2];   // P of buffer b stored, the previous block's partial read (8 warps)
   unsigned long long pv_done[2];  // P V of buffer b computed into its O partial
-  unsigned long long mma_done;
+  unsigned long long mma_done[2];
   unsigned long long xchg[4];     // per lane quarter: both softmax warps published their value
   uint32_t tmem_base;
   int abort_flag;
@@ -134,7 +136,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
       ptx::mbar_init(ptx::smem_u32(&hdr->p_full[b]), 8);
       ptx::mbar_init(ptx::smem_u32(&hdr->pv_done[b]), 1);
     }
-    ptx::mbar_init(ptx::smem_u32(&hdr->mma_done), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[1]), 1);
     hdr->abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -189,48 +192,24 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->kv_full[k % kStagesW]), (k / kStagesW) & 1u, 100000000ull);
       }
     }
-  } else if (warp == kWarpMmaW) {
-    // ------------------------------------------------------------ MMA issuer (lane 0)
+  } else if (warp == kWarpMmaW || warp == kWarpPvW) {
+    // ------------------------------------------------------------ MMA issuers (lane 0)
+    // One thread issues the score products, another the P V products: a thread holds an MMA
+    // instruction about 66 cycles whatever its N, so one issuer leaves the N = 64 products at half
+    // the tensor core's rate (measured). The score issuer writes S of buffer b again only after
+    // P V of the block two back, which read P there, has completed.
     if (lane == 0) {
+      const bool scores = warp == kWarpMmaW;
       const uint32_t id_qk =
           ptx::idesc_f32acc(kBMw, kBNw, ptx::kFmtBF16, ptx::kFmtBF16, false, false) | (neg_scale ? ptx::kNegateA : 0u);
       constexpr uint32_t id_pv = ptx::idesc_f32acc(kBMw, kDw, ptx::kFmtBF16, ptx::kFmtBF16, false, true);
       auto wait = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
-        return ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
-      };
-      // the six products A_x B_y, smallest first, so each k-step adds its largest term last
-      constexpr int kPa[6] = {2, 1, 0, 1, 0, 0}, kPb[6] = {0, 1, 2, 0, 1, 0};
-      // S_b = sum of Q_x K_y^T for block gg (b = gg & 1); A from tensor memory, K K-major
-      auto qk = [&](uint32_t gg) {
-        const int st = gg % kStagesW;
-        const uint32_t d = tmem + cS + 128u * (gg & 1u);
-#pragma unroll
-        for (int ks = 0; ks < kDw / 16; ++ks)
-#pragma unroll
-          for (int t = 0; t < 6; ++t)
-            ptx::mma_f16_ts(d, tmem + cQ + 32 * kPa[t] + ks * 8, ptx::sdesc_sw128(sK(st, kPb[t]) + ks * 32, 16, 1024),
-                            id_qk, (ks > 0 || t > 0) ? 1u : 0u);
-        ptx::tc_commit(ptx::smem_u32(&hdr->s_full[gg & 1u]));
-      };
-      // O_b = sum of P_x V_y for block gg, from zero (V MN-major); releases the block's stage
-      auto pv = [&](uint32_t gg) {
-        const int st = gg % kStagesW;
-        const uint32_t b = gg & 1u, o = tmem + cO + 64u * b, pb = tmem + cS + 128u * b;
-#pragma unroll
-        for (int ks = 0; ks < kBNw / 16; ++ks)
-#pragma unroll
-          for (int t = 0; t < 6; ++t)
-            ptx::mma_f16_ts(o, pb + 32 * kPa[t] + ks * 8,
-                            ptx::sdesc_sw128(sV(st, kPb[t]) + ks * 2048, kPlaneW, 1024), id_pv,
-                            (ks > 0 || t > 0) ? 1u : 0u);
-        ptx::tc_commit(ptx::smem_u32(&hdr->pv_done[b]));
-        ptx::tc_commit(ptx::smem_u32(&hdr->kv_empty[st]));
-      };
-      auto kv_ready = [&](uint32_t gg) {
-        const bool r = wait(&hdr->kv_full[gg % kStagesW], (gg / kStagesW) & 1u, 21);
+        const bool r = ptx::mbar_wait(ptx::smem_u32(bar), parity, wc, site);
         ptx::tc_fence_after();
         return r;
       };
+      // the six products A_x B_y, smallest first, so each k-step adds its largest term last
+      constexpr int kPa[6] = {2, 1, 0, 1, 0, 0}, kPb[6] = {0, 1, 2, 0, 1, 0};
       uint32_t g = 0;
       int n = 0;
       bool ok = true;
@@ -238,35 +217,54 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         int bh, q0, jb, nb;
         tile_of(w, bh, q0, jb, nb);
         if (nb == 0) continue;
-        // the unit's Q is in tensor memory (written after the previous unit's last S was read)
-        if (!wait(&hdr->q_full, n & 1, 20)) break;
-        ++n;
-        ptx::tc_fence_after();
-        ok = kv_ready(g);
-        if (!ok) break;
-        qk(g);
-        if (nb > 1) {
-          ok = kv_ready(g + 1);
-          if (!ok) break;
-          qk(g + 1);
-        }
-        for (int j = 0; j < nb && ok; ++j) {
-          const uint32_t gg = g + j;
-          // P(gg) stored (and the partial two blocks back, which O_b held, read)
-          ok = wait(&hdr->p_full[gg & 1u], (gg >> 1) & 1u, 22);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          pv(gg);
-          // S_b is free again once P V has read P(gg): issued behind it
-          if (j + 2 < nb) {
-            ok = kv_ready(gg + 2);
-            if (ok) qk(gg + 2);
+        if (scores) {
+          // the unit's Q is in tensor memory (written after the previous unit's last S was read)
+          if (!wait(&hdr->q_full, n & 1, 20)) break;
+          ++n;
+          for (int j = 0; j < nb && ok; ++j) {
+            const uint32_t gg = g + j, b = gg & 1u;
+            const int st = gg % kStagesW;
+            // S_b free: P V of block gg - 2 has read P there; K of block gg landed
+            if (gg >= 2) ok = wait(&hdr->pv_done[b], ((gg - 2u) >> 1) & 1u, 23);
+            if (ok) ok = wait(&hdr->kv_full[st], (gg / kStagesW) & 1u, 21);
+            if (!ok) break;
+            // S_b = sum of Q_x K_y^T (A from tensor memory, K K-major)
+            const uint32_t d = tmem + cS + 128u * b;
+#pragma unroll
+            for (int ks = 0; ks < kDw / 16; ++ks)
+#pragma unroll
+              for (int t = 0; t < 6; ++t)
+                ptx::mma_f16_ts(d, tmem + cQ + 32 * kPa[t] + ks * 8,
+                                ptx::sdesc_sw128(sK(st, kPb[t]) + ks * 32, 16, 1024), id_qk,
+                                (ks > 0 || t > 0) ? 1u : 0u);
+            ptx::tc_commit(ptx::smem_u32(&hdr->s_full[b]));
+          }
+        } else {
+          for (int j = 0; j < nb && ok; ++j) {
+            const uint32_t gg = g + j, b = gg & 1u;
+            const int st = gg % kStagesW;
+            // P(gg) stored (and the partial two blocks back, which O_b held, read); its S was
+            // computed from this stage, so V of block gg has landed too
+            ok = wait(&hdr->p_full[b], (gg >> 1) & 1u, 22);
+            if (!ok) break;
+            // O_b = sum of P_x V_y for block gg, from zero (V MN-major); then the stage is free
+            const uint32_t o = tmem + cO + 64u * b, pb = tmem + cS + 128u * b;
+#pragma unroll
+            for (int ks = 0; ks < kBNw / 16; ++ks)
+#pragma unroll
+              for (int t = 0; t < 6; ++t)
+                ptx::mma_f16_ts(o, pb + 32 * kPa[t] + ks * 8,
+                                ptx::sdesc_sw128(sV(st, kPb[t]) + ks * 2048, kPlaneW, 1024), id_pv,
+                                (ks > 0 || t > 0) ? 1u : 0u);
+            ptx::tc_commit(ptx::smem_u32(&hdr->pv_done[b]));
+            ptx::tc_commit(ptx::smem_u32(&hdr->kv_empty[st]));
           }
         }
         g += nb;
       }
-      ptx::tc_commit(ptx::smem_u32(&hdr->mma_done));
-      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
+      const int me = scores ? 0 : 1;
+      ptx::tc_commit(ptx::smem_u32(&hdr->mma_done[me]));
+      ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done[me]), 0u, 1000000000ull);
     }
   } else if (warp < 8) {
     // ------------------------------------------------------------ softmax / epilogue
