@@ -18,9 +18,10 @@
 //    the block two back has read P there.
 // As in fwd_f32.cu every block's P V starts from zero in tensor memory and the softmax threads add
 // the block partials in registers with round-to-nearest adds (the tensor core's f32 accumulation
-// truncates). Tensor memory: Q parts at 0, 32, 64 (32 columns each, two bf16 per column); buffer b
-// at 128 + 128 b: S (64 f32 columns), then P's parts 0 and 1 written over it and part 2 in the next
-// 32 columns; the block partial of O of buffer b at 384 + 64 b.
+// truncates). Tensor memory: Q parts at 0, 32, 64 (32 columns each, two bf16 per column); three S
+// buffers at 128 + 64 b (64 f32 columns each; P's parts 0 and 1 written over S, part 2 in 32 columns
+// of its own), so the score products can run up to three blocks ahead of P V; two block partials of
+// O at 384 + 64 o.
 #include "fa_internal.cuh"
 #include "ptx.cuh"
 
@@ -37,14 +38,18 @@ constexpr int kThreadsW = 352;            // softmax 0-7, producer 8, MMA issuer
 constexpr int kWarpProdW = 8, kWarpMmaW = 9, kWarpPvW = 10;
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr float kLn2W = 0.6931471805599453f;
-constexpr uint32_t cQ = 0, cS = 128, cO = 384;  // Q part p at 32 p; buffer b: S at cS + 128 b, O at cO + 64 b
+// Tensor memory: Q part p at 32 p; S buffer b (0..2) at 128 + 64 b, P's parts 0 and 1 written over it,
+// part 2 at p2_col(b) (96, 320, 352); O partial buffer o (0..1) at 384 + 64 o
+constexpr uint32_t cQ = 0, cS = 128, cO = 384;
+__device__ __forceinline__ uint32_t p2_col(uint32_t b) { return b == 0u ? 96u : 256u + 32u * (b + 1u); }
 
 struct F32wHdr {
   unsigned long long kv_full[kStagesW], kv_empty[kStagesW];
   unsigned long long q_full;      // the unit's Q rows are in tensor memory (8 softmax warps)
-  unsigned long long s_full[2];   // S of buffer b computed
-  unsigned long long p_full[2];   // P of buffer b stored, the previous block's partial read (8 warps)
-  unsigned long long pv_done[2];  // P V of buffer b computed into its O partial
+  unsigned long long s_full[3];   // S of buffer b computed
+  unsigned long long p_full[3];   // P of buffer b stored, the previous block's partial read (8 warps)
+  unsigned long long s_free[3];   // P V has read P of buffer b: S may be computed there again
+  unsigned long long pv_done[2];  // P V into O partial buffer o computed
   unsigned long long mma_done[2];
   unsigned long long xchg[4];     // per lane quarter: both softmax warps published their value
   uint32_t tmem_base;
@@ -131,11 +136,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
     ptx::mbar_init(ptx::smem_u32(&hdr->q_full), 8);
     for (int q = 0; q < 4; ++q) ptx::mbar_init(ptx::smem_u32(&hdr->xchg[q]), 2);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 3; ++b) {
       ptx::mbar_init(ptx::smem_u32(&hdr->s_full[b]), 1);
       ptx::mbar_init(ptx::smem_u32(&hdr->p_full[b]), 8);
-      ptx::mbar_init(ptx::smem_u32(&hdr->pv_done[b]), 1);
+      ptx::mbar_init(ptx::smem_u32(&hdr->s_free[b]), 1);
     }
+    ptx::mbar_init(ptx::smem_u32(&hdr->pv_done[0]), 1);
+    ptx::mbar_init(ptx::smem_u32(&hdr->pv_done[1]), 1);
     ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[1]), 1);
     hdr->abort_flag = 0;
@@ -222,14 +229,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           if (!wait(&hdr->q_full, n & 1, 20)) break;
           ++n;
           for (int j = 0; j < nb && ok; ++j) {
-            const uint32_t gg = g + j, b = gg & 1u;
+            const uint32_t gg = g + j, b = gg % 3u;
             const int st = gg % kStagesW;
-            // S_b free: P V of block gg - 2 has read P there; K of block gg landed
-            if (gg >= 2) ok = wait(&hdr->pv_done[b], ((gg - 2u) >> 1) & 1u, 23);
+            // S_b free: P V of block gg - 3 has read P there; K of block gg landed
+            if (gg >= 3) ok = wait(&hdr->s_free[b], ((gg - 3u) / 3u) & 1u, 23);
             if (ok) ok = wait(&hdr->kv_full[st], (gg / kStagesW) & 1u, 21);
             if (!ok) break;
             // S_b = sum of Q_x K_y^T (A from tensor memory, K K-major)
-            const uint32_t d = tmem + cS + 128u * b;
+            const uint32_t d = tmem + cS + 64u * b;
 #pragma unroll
             for (int ks = 0; ks < kDw / 16; ++ks)
 #pragma unroll
@@ -241,22 +248,25 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           }
         } else {
           for (int j = 0; j < nb && ok; ++j) {
-            const uint32_t gg = g + j, b = gg & 1u;
+            const uint32_t gg = g + j, b = gg % 3u, ob = gg & 1u;
             const int st = gg % kStagesW;
-            // P(gg) stored (and the partial two blocks back, which O_b held, read); its S was
+            // P(gg) stored (and the partial two blocks back, which O_ob held, read); its S was
             // computed from this stage, so V of block gg has landed too
-            ok = wait(&hdr->p_full[b], (gg >> 1) & 1u, 22);
+            ok = wait(&hdr->p_full[b], (gg / 3u) & 1u, 22);
             if (!ok) break;
-            // O_b = sum of P_x V_y for block gg, from zero (V MN-major); then the stage is free
-            const uint32_t o = tmem + cO + 64u * b, pb = tmem + cS + 128u * b;
+            // O_ob = sum of P_x V_y for block gg, from zero (V MN-major); then P's buffer and the
+            // stage are free
+            const uint32_t o = tmem + cO + 64u * ob;
+            const uint32_t pcol[3] = {tmem + cS + 64u * b, tmem + cS + 64u * b + 32u, tmem + p2_col(b)};
 #pragma unroll
             for (int ks = 0; ks < kBNw / 16; ++ks)
 #pragma unroll
               for (int t = 0; t < 6; ++t)
-                ptx::mma_f16_ts(o, pb + 32 * kPa[t] + ks * 8,
+                ptx::mma_f16_ts(o, pcol[kPa[t]] + ks * 8,
                                 ptx::sdesc_sw128(sV(st, kPb[t]) + ks * 2048, kPlaneW, 1024), id_pv,
                                 (ks > 0 || t > 0) ? 1u : 0u);
-            ptx::tc_commit(ptx::smem_u32(&hdr->pv_done[b]));
+            ptx::tc_commit(ptx::smem_u32(&hdr->pv_done[ob]));
+            ptx::tc_commit(ptx::smem_u32(&hdr->s_free[b]));
             ptx::tc_commit(ptx::smem_u32(&hdr->kv_empty[st]));
           }
         }
@@ -328,10 +338,10 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         ptx::tmem_wait_ld32(t);
       };
       for (int j = 0; j < nb; ++j) {
-        const uint32_t gg = g + j, b = gg & 1u;
-        ok = wait_all(&hdr->s_full[b], (gg >> 1) & 1u, 30);
+        const uint32_t gg = g + j, b = gg % 3u, ob = gg & 1u;
+        ok = wait_all(&hdr->s_full[b], (gg / 3u) & 1u, 30);
         if (!ok) break;
-        const uint32_t tB = tmem + lane_sel + cS + 128u * b;  // this lane quarter's rows of buffer b
+        const uint32_t tB = tmem + lane_sel + cS + 64u * b;  // this lane quarter's rows of buffer b
         const int k0 = (jb + j) * kBNw + static_cast<int>(c0);  // first key of this warp's columns
         const bool edge = k0 + 32 > N || (CAUSAL && k0 + 31 > q0);
         uint32_t r[32];
@@ -376,14 +386,14 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         }
         ptx::tmem_st16(tB + c0 / 2, w0);
         ptx::tmem_st16(tB + 32 + c0 / 2, w1);
-        ptx::tmem_st16(tB + 64 + c0 / 2, w2);
+        ptx::tmem_st16(tmem + lane_sel + p2_col(b) + c0 / 2, w2);
         const float2 sum2 = ptx::fadd2(sum_a, sum_b);
         // the previous block's partial joins the accumulator; both go to the new maximum
         if (j > 0) {
-          ok = wait_all(&hdr->pv_done[b ^ 1u], ((gg - 1u) >> 1) & 1u, 32);
+          ok = wait_all(&hdr->pv_done[ob ^ 1u], ((gg - 1u) >> 1) & 1u, 32);
           if (!ok) break;
           uint32_t t[32];
-          load_partial(b ^ 1u, t);
+          load_partial(ob ^ 1u, t);
           const float2 cc = make_float2(corr, corr);
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
