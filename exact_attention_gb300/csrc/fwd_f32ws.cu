@@ -475,21 +475,29 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         if (count == 0u) break;
         if (static_cast<int>(count) < holders) continue;  // a later part finishes these columns
         __threadfence();  // the other parts' partials, counted in before this one, are visible
+        // (loops unrolled so that several parts' loads are in flight at once: each pass costs a
+        // memory round trip per unroll group, not per part)
         float mm = m2;
+#pragma unroll 4
         for (int p = 0; p < parts; ++p)
           if (p != part && nonempty(p)) mm = fmaxf(mm, __ldcg(slot_of(p) + kDw * kBMw + rr));
         const float a = m2 == -INFINITY ? 0.f : ptx::ex2(m2 - mm);
         l *= a;
 #pragma unroll
         for (int c = 0; c < 32; ++c) oacc[c] *= a;
+#pragma unroll 2
         for (int p = 0; p < parts; ++p) {
           if (p == part || !nonempty(p)) continue;
           const float* sp = slot_of(p);
           const float mp = __ldcg(sp + kDw * kBMw + rr);
-          const float bw = mp == -INFINITY ? 0.f : ptx::ex2(mp - mm);
-          l = fmaf(bw, __ldcg(sp + kDw * kBMw + kBMw + rr), l);
+          const float lp = __ldcg(sp + kDw * kBMw + kBMw + rr);
+          float col[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) oacc[c] = fmaf(bw, __ldcg(sp + (c0 + c) * kBMw + rr), oacc[c]);
+          for (int c = 0; c < 32; ++c) col[c] = __ldcg(sp + (c0 + c) * kBMw + rr);
+          const float bw = mp == -INFINITY ? 0.f : ptx::ex2(mp - mm);
+          l = fmaf(bw, lp, l);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) oacc[c] = fmaf(bw, col[c], oacc[c]);
         }
         m2 = mm;
       }
