@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
 
   if (warp == kWarpProdB) {
     // ------------------------------------------------------------ producer (whole warp)
-    uint32_t it_s = 0;
+    uint32_t it_s = 0, n_fixed = 0;  // n_fixed: K/V loads issued (lane 0)
     int n_item = 0;
     bool ok = true;
     for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
             ptx::tma_load_3d(sK + c * kChunkB, &tmK, ff, c * 64, itm.r0, itm.bh);
             ptx::tma_load_3d(sV + c * kChunkB, &tmV, ff, c * 64, itm.r0, itm.bh);
           }
+          ++n_fixed;
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -220,6 +221,11 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(fb);
       }
+    }
+    if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
+      for (uint32_t k = it_s > (uint32_t)kStagesB ? it_s - kStagesB : 0u; k < it_s; ++k)
+        ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % kStagesB]), (k / kStagesB) & 1u, 100000000ull);
+      if (n_fixed > 0u) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->fixed_full), (n_fixed - 1u) & 1u, 100000000ull);
     }
   } else if (warp == kWarpMmaB) {
     // ------------------------------------------------------------ MMA issuer
@@ -262,7 +268,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         }
         if (!ok) break;
         ptx::tc_commit(ptx::smem_u32(&hdr->fixed_empty));
-        ptx::tc_commit(ptx::smem_u32(&hdr->acc_full));
+        // only items with a query block have accumulators to hand over; an empty item's commit
+        // would complete the barrier's next phase too early (two phases ahead of its waiters)
+        if (itm.lo < itm.hi) ptx::tc_commit(ptx::smem_u32(&hdr->acc_full));
       }
       ptx::tc_commit(ptx::smem_u32(&hdr->mma_done));
       ptx::mbar_wait_drain(ptx::smem_u32(&hdr->mma_done), 0u, 1000000000ull);
@@ -272,7 +280,7 @@ __global__ void __launch_bounds__(kThreadsB, 1)
     const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t tS = tmem + lane_sel, tdP = tmem + 128 + lane_sel;
     const uint32_t tdV = tmem + 256 + lane_sel, tdK = tmem + 256 + D + lane_sel;
-    uint32_t it_s = 0, s_ph = 0;
+    uint32_t it_s = 0, s_ph = 0, n_acc = 0;  // n_acc: items with a query block (acc_full phases)
     int n_item = 0;
     bool ok = true;
     for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
@@ -323,12 +331,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       if (!ok) break;
       // epilogue: dV and scale * dK for this thread's key
-      ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(&hdr->acc_full), n_item & 1, wc, 32));
-      if (!ok) break;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+      if (!none) {
+        ok = __all_sync(0xFFFFFFFFu, ptx::mbar_wait(ptx::smem_u32(&hdr->acc_full), (n_acc++) & 1u, wc, 32));
+        if (!ok) break;
+      }
       ptx::tc_fence_after();
       const bool valid = key < N;
       const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D;
-      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         const uint32_t src = part == 0 ? tdV : tdK;
@@ -511,7 +521,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
         nd_v[k] = in ? -delta[g] : 0.f;
       }
     };
-    uint32_t it_s = 0;
+    uint32_t it_s = 0, n_fixed = 0;  // n_fixed: K/V loads issued (lane 0)
     int n_item = 0;
     bool ok = true;
     int r = 0;
@@ -531,6 +541,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::mbar_arrive_expect_tx(ff, 2 * C::kTileBytes);
           ptx::tma_load_3d(sK, &tmK, ff, 0, itm.r0, itm.bh);
           ptx::tma_load_3d(sV, &tmV, ff, 0, itm.r0, itm.bh);
+          ++n_fixed;
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -571,6 +582,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
     if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
       for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
         ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
+      if (n_fixed > 0u) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->fixed_full), (n_fixed - 1u) & 1u, 100000000ull);
     }
   } else if (warp == kWarpMmaO || warp == kWarpGradO) {
     // ------------------------------------------------------------ MMA issuers (lane 0)
@@ -652,7 +664,12 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           }
         }
         if (!ok) break;
-        commit(scores ? &hdr->fixed_empty : &hdr->acc_full);
+        // (an item without a query block hands over no accumulators: its commit would complete
+        // acc_full's next phase before the compute warps wait for this one)
+        if (scores)
+          commit(&hdr->fixed_empty);
+        else if (itm.lo < itm.hi)
+          commit(&hdr->acc_full);
       }
       const int me = scores ? 0 : 1;
       commit(&hdr->mma_done[me]);
@@ -664,6 +681,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
     const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's query columns [c0, c0 + 64)
     uint32_t it_s = 0, nb = 0;  // blocks processed (all items): s_full/dp_full/free phases
+    uint32_t n_acc = 0;         // items with a query block (acc_full phases)
     int n_item = 0;
     bool ok = true;
     auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
@@ -747,11 +765,13 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       }
       if (!ok) break;
       // epilogue: this warp writes columns [32 * half, 32 * half + 32) of dV and scale * dK
-      ok = wait_all(&hdr->acc_full, n_item & 1, 35);
-      if (!ok) break;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+      if (!none) {
+        ok = wait_all(&hdr->acc_full, (n_acc++) & 1u, 35);
+        if (!ok) break;
+      }
       const bool valid = key < N;
       const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
-      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t a[32];
@@ -951,7 +971,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         nd_v[k] = in ? -delta[g] : 0.f;
       }
     };
-    uint32_t it_s = 0;
+    uint32_t it_s = 0, n_fixed = 0;  // n_fixed: K/V loads issued (lane 0)
     int n_item = 0;
     bool ok = true;
     FusedSched<CAUSAL> sch(split, units);
@@ -968,6 +988,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           ptx::mbar_arrive_expect_tx(ff, 2 * C::kTileBytes);
           ptx::tma_load_3d(sK, &tmK, ff, 0, itm.r0, itm.bh);
           ptx::tma_load_3d(sV, &tmV, ff, 0, itm.r0, itm.bh);
+          ++n_fixed;
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -1009,6 +1030,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
       for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
         ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
+      if (n_fixed > 0u) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->fixed_full), (n_fixed - 1u) & 1u, 100000000ull);
     }
   } else if (warp == kWarpMmaF || warp == kWarpGradF) {
     // ------------------------------------------------------------ MMA issuers (lane 0)
@@ -1045,8 +1067,12 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       FusedPiece pc;
       for (; ok && sch.next(pc, items, nqb, item); ++n_item) {
         const BwdItem itm = pc.it;
+        // Both issuers wait for the item's K and V, although only the scores issuer's products
+        // need them first: each arrives once per item on fixed_empty, and an issuer that arrived
+        // for items without a query block without waiting would run ahead, complete the
+        // barrier's phases early and let the producer refill K and V with copies in flight.
+        if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
         if (scores) {
-          if (!wait(&hdr->fixed_full, n_item & 1, 20)) break;
           if (itm.lo < itm.hi) {
             ok = stage_ready(it_s);
             if (!ok) break;
@@ -1105,7 +1131,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           }
         }
         if (!ok) break;
-        if (!scores) commit(&hdr->acc_full);
+        // (a piece without a query block hands over no accumulators: its commit would complete
+        // acc_full's next phase before the compute warps wait for this one)
+        if (!scores && itm.lo < itm.hi) commit(&hdr->acc_full);
         commit(&hdr->fixed_empty);  // K and V read by this thread's products of the item
       }
       const int me = scores ? 0 : 1;
@@ -1164,6 +1192,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
     };
     uint32_t it_s = 0, nb = 0;  // blocks processed (all items): s_full/dp_full/free phases
+    uint32_t n_acc = 0;         // pieces with a query block (acc_full phases)
     int n_item = 0;
     bool ok = true;
     auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
@@ -1317,16 +1346,24 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       if (ok && itm.lo < itm.hi) ok = dq_readout();  // the piece's last block
       if (!ok) break;
       // epilogue: this warp's columns [d0, d0 + kDcF) of dV and dK, for key row rr
-      ok = wait_all(&hdr->acc_full, n_item & 1, 35);
-      if (!ok) break;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
       const int rr = quarter * 32 + lane;
       float g2[2][kDcF];
+      if (!none) {
+        ok = wait_all(&hdr->acc_full, (n_acc++) & 1u, 35);
+        if (!ok) break;
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        uint32_t a[kDcF];
-        ld_grad((part == 0 ? cdV : cdK) + d0, a);
+        for (int part = 0; part < 2; ++part) {
+          uint32_t a[kDcF];
+          ld_grad((part == 0 ? cdV : cdK) + d0, a);
 #pragma unroll
-        for (int k = 0; k < kDcF; ++k) g2[part][k] = __uint_as_float(a[k]);
+          for (int k = 0; k < kDcF; ++k) g2[part][k] = __uint_as_float(a[k]);
+        }
+      } else {
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int k = 0; k < kDcF; ++k) g2[part][k] = 0.f;
       }
       ptx::tc_fence_before();
       if (pc.kind != 0) {
@@ -1390,7 +1427,6 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
       // dV and scale * dK in the I/O type, as the two 128 x 64 output tiles (128-byte swizzled
       // rows, the tensor maps' layout; rows past N are clipped by the maps), stored by TMA
-      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
       uint32_t hv[kDcF / 2], hk[kDcF / 2];
 #pragma unroll
       for (int k = 0; k < kDcF / 2; ++k) {
@@ -1467,7 +1503,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
 
   if (warp == kWarpProdO) {
     if (lane == 0) {
-      uint32_t it_s = 0;
+      uint32_t it_s = 0, n_fixed = 0;  // n_fixed: Q/dO loads issued
       int n_item = 0;
       bool ok = true;
       for (int r = 0, w = item_of_round<CAUSAL>(0, items); w < items && ok; w = item_of_round<CAUSAL>(++r, items), ++n_item) {
@@ -1479,6 +1515,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::tma_load_3d(sQ + c * kChunkB, &tmQ, ff, c * 64, itm.r0, itm.bh);
           ptx::tma_load_3d(sdO + c * kChunkB, &tmdO, ff, c * 64, itm.r0, itm.bh);
         }
+        ++n_fixed;
         for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
           const int st = it_s % C::kStages;
           ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / C::kStages) & 1u) ^ 1u, wc, 11);
@@ -1494,6 +1531,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
       if (hdr->abort_flag) {  // let issued copies land before shared memory is released
         for (uint32_t k = it_s > (uint32_t)C::kStages ? it_s - C::kStages : 0u; k < it_s; ++k)
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
+        if (n_fixed > 0u) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->fixed_full), (n_fixed - 1u) & 1u, 100000000ull);
       }
     }
   } else if (warp == kWarpMmaO || warp == kWarpGradO) {

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const CUtensorMap* mQc = rank == 0 ? (have_views ? &tmQv : &tmQ) : &tmQ;
     const CUtensorMap* mdOc = rank == 0 ? (have_views ? &tmdOv : &tmdO) : &tmdO;
     const int xc = rank == 0 ? 0 : 32;
-    uint32_t it_s = 0;
+    uint32_t it_s = 0, n_fixed = 0;  // n_fixed: K/V loads issued (lane 0)
     int n_item = 0;
     bool ok = true;
     int r = 0;
@@ -192,6 +192,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           ptx::mbar_arrive_expect_tx(ff, 2 * kChunkB);
           ptx::tma_load_3d(sK, &tmK, ff, 0, itm.r0, itm.bh);
           ptx::tma_load_3d(sV, &tmV, ff, 0, itm.r0, itm.bh);
+          ++n_fixed;
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0 && hdr->abort_flag) {  // let issued copies land before shared memory is released
       for (uint32_t k = it_s > (uint32_t)kPStages ? it_s - kPStages : 0u; k < it_s; ++k)
         ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % kPStages]), (k / kPStages) & 1u, 100000000ull);
+      if (n_fixed > 0u) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->fixed_full), (n_fixed - 1u) & 1u, 100000000ull);
     }
   } else if ((warp == kPWarpMma || warp == kPWarpGrad) && rank == 0) {
     // ------------------------------------------------------------ MMA issuers of the pair (lane 0)
@@ -318,7 +320,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
           }
         }
         if (!ok) break;
-        commit(scores ? &hdr->fixed_empty : &hdr->acc_full);
+        // (an item without a query block hands over no accumulators: its commit would complete
+        // acc_full's next phase before the compute warps wait for this one)
+        if (scores)
+          commit(&hdr->fixed_empty);
+        else if (itm.lo < itm.hi)
+          commit(&hdr->acc_full);
       }
       const int me = scores ? 0 : 1;
       commit(&hdr->mma_done[me]);
@@ -351,7 +358,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's query columns [c0, c0 + 64)
     const uint32_t sig1 = ptx::peer_addr(ptx::smem_u32(&hdr->sig1), 0);
     const uint32_t sig2 = ptx::peer_addr(ptx::smem_u32(&hdr->sig2), 0);
-    uint32_t it_s = 0, nb = 0;
+    uint32_t it_s = 0, nb = 0, n_acc = 0;  // n_acc: items with a query block (acc_full phases)
     int n_item = 0;
     bool ok = true;
     auto wait_all = [&](unsigned long long* bar, uint32_t parity, uint32_t site) {
@@ -434,11 +441,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
       }
       if (!ok) break;
       // epilogue: this warp writes columns [32 * half, 32 * half + 32) of dV and scale * dK
-      ok = wait_all(&hdr->acc_full, n_item & 1, 35);
-      if (!ok) break;
+      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
+      if (!none) {
+        ok = wait_all(&hdr->acc_full, (n_acc++) & 1u, 35);
+        if (!ok) break;
+      }
       const bool valid = key < N;
       const size_t g = (static_cast<size_t>(itm.bh) * N + (valid ? key : 0)) * D + 32 * half;
-      const bool none = itm.lo >= itm.hi;  // no query block: the gradients are zero
 #pragma unroll
       for (int part = 0; part < 2; ++part) {
         uint32_t a[32];
@@ -578,7 +587,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     if (lane == 0) {
       const CUtensorMap* mKc = rank == 0 ? (have_views ? &tmKv : &tmK) : &tmK;
       const int xc = rank == 0 ? 0 : 32;
-      uint32_t it_s = 0;
+      uint32_t it_s = 0, n_fixed = 0;  // n_fixed: Q/dO loads issued
       int n_item = 0;
       bool ok = true;
       for (int r = 0, w = pair_item_of_round<CAUSAL>(0, items); w < items && ok;
@@ -589,6 +598,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         ptx::mbar_arrive_expect_tx(ff, 2 * kChunkB);
         ptx::tma_load_3d(sQ, &tmQ, ff, 0, itm.r0, itm.bh);
         ptx::tma_load_3d(sdO, &tmdO, ff, 0, itm.r0, itm.bh);
+        ++n_fixed;
         for (int j = itm.lo; j < itm.hi; ++j, ++it_s) {
           const int st = it_s % kQStages;
           ok = ptx::mbar_wait(ptx::smem_u32(&hdr->empty[st]), ((it_s / kQStages) & 1u) ^ 1u, wc, 11);
@@ -604,6 +614,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
       if (hdr->abort_flag) {  // let issued copies land before shared memory is released
         for (uint32_t k = it_s > (uint32_t)kQStages ? it_s - kQStages : 0u; k < it_s; ++k)
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->full[k % kQStages]), (k / kQStages) & 1u, 100000000ull);
+        if (n_fixed > 0u) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->fixed_full), (n_fixed - 1u) & 1u, 100000000ull);
       }
     }
   } else if ((warp == kPWarpMma || warp == kPWarpGrad) && rank == 0) {

@@ -310,6 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(k == 0 && skip_first))
             ptx::mbar_wait_drain(ptx::smem_u32(&hdr->kv_full[k % kStages]), (k / kStages) & 1u, 100000000ull);
         }
+        // Q loads issued: one per piece taken (it)
+        for (int k = it > kQBuf ? it - kQBuf : 0; k < it; ++k)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->q_full[k % kQBuf]), static_cast<uint32_t>(k / kQBuf) & 1u, 100000000ull);
       }
     }
   } else if (warp == kWarpMma || warp == kWarpMma + 1) {

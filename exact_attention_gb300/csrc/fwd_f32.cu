@@ -205,6 +205,11 @@ __global__ void __launch_bounds__(kThreads32, 1)
           }
         }
       }
+      if (hdr->abort_flag) {  // let issued copies land before shared memory is released
+        for (uint32_t k = it > (uint32_t)kStages32 ? it - kStages32 : 0u; k < it; ++k)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->kv_full[k % kStages32]), (k / kStages32) & 1u, 100000000ull);
+        if (n > 0) ptx::mbar_wait_drain(ptx::smem_u32(&hdr->q_full), static_cast<uint32_t>(n - 1) & 1u, 100000000ull);
+      }
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ split warps: x -> (tf32 hi, lo)

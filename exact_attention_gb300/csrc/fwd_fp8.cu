@@ -154,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t kv_it = 0;
       bool ok = true;
-      for (int it = 0; ok; ++it) {
+      int it = 0;  // pieces taken; one Q load each
+      for (; ok; ++it) {
         const int tile = classic_tile<CAUSAL>(it);
         if (tile >= num_tiles) break;
         const TileInfo ti = tile_info<CAUSAL>(tile, BH, num_pairs, nkb);
@@ -179,6 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (hdr->abort_flag) {  // let issued copies land before shared memory is released
         for (uint32_t k = kv_it > (uint32_t)kStages ? kv_it - kStages : 0u; k < kv_it; ++k)
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->kv_full[k % kStages]), (k / kStages) & 1u, 100000000ull);
+        for (int k = it > kQBuf ? it - kQBuf : 0; k < it; ++k)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->q_full[k % kQBuf]), static_cast<uint32_t>(k / kQBuf) & 1u, 100000000ull);
       }
     }
   } else if (warp == kWarpMma || warp == kWarpMma + 1) {

@@ -206,6 +206,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->k_full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
           ptx::mbar_wait_drain(ptx::smem_u32(&hdr->v_full[k % C::kStages]), (k / C::kStages) & 1u, 100000000ull);
         }
+        // Q loads issued: one per piece taken (it)
+        for (int k = it > C::kQBuf ? it - C::kQBuf : 0; k < it; ++k)
+          ptx::mbar_wait_drain(ptx::smem_u32(&hdr->q_full[k % C::kQBuf]), static_cast<uint32_t>(k / C::kQBuf) & 1u,
+                               100000000ull);
       }
     }
   } else if (warp == kWarpMma) {

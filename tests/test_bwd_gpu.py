@@ -92,6 +92,22 @@ def test_backward_matches_oracle(dtype, D, causal, B, H, M, N, fused):
     check(inputs, o, grads, delta, dtype, causal, scale)
 
 
+@FUSED
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_causal_keys_past_every_query(D, fused):
+    """Causal with N > M and more key tiles than SMs: a CTA takes a key tile that some query sees
+    and then one past every query (no query block: zero gradients, no accumulators to hand
+    over). The accumulators-final barrier must advance only for the first, or the compute warps'
+    parity wait would see it two phases ahead; and every thread arriving on the barrier that frees
+    K and V must first wait for them, or its arrivals for such tiles run ahead of the loads."""
+    B, H, M, N = 4, 50, 128, 1024
+    scale = 1.0 / math.sqrt(D)
+    inputs, o, grads, delta = run_bwd(B, H, M, N, D, "f16", True, scale, seed=17, fused=fused)
+    check(inputs, o, grads, delta, "f16", True, scale, heads=[(0, 0), (1, 31), (3, 49)])
+    # keys past the last query get nothing
+    assert np.all(grads[1][:, :, M:] == 0) and np.all(grads[2][:, :, M:] == 0)
+
+
 def test_backward_gradient_identities():
     """sum_j dK_j = 0 (rows of dS sum to zero) and sum_j dV_j = sum_i dO_i."""
     inputs, o, (dq, dk, dv), _ = run_bwd(1, 2, 512, 512, 64, "f16", True, 0.125, seed=3)
