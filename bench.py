@@ -12,8 +12,9 @@ Step i runs the forward and the backward on input set i % 4 of four seeded sets
 calls of each part run back to back on one stream between one pair of CUDA
 events. `value` is the forward's TFLOP/s (4*B*H*M*N*D per call); the decode
 GB/s (K+V bytes read per call) is reported in the `decode` object. `configs`
-times every configuration of the workload list on its own (one call between
-two events, L2 flushed before it). `e2e` repeats the forward through the C ABI
+times every configuration of the workload list on its own, the same way (calls
+back to back over copies of its inputs larger than twice L2; one isolated call
+with L2 flushed is reported beside it). `e2e` repeats the forward through the C ABI
 on pinned host buffers (fa_fwd_host: the inputs copied in and O/LSE copied back
 inside the timed region, overlapped with the kernels chunk by chunk).
 
@@ -44,6 +45,40 @@ DEC = dict(B=8, H=32, N=32768, D=128, n_splits=64, dtype="bf16")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
 ROTATE = 4  # input sets of the forward/backward workload used in turn: 4 x 63 MB > 129 MB of L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+ROT_BYTES = 300 << 20  # rotated input copies of a configuration: more than twice L2 (129 MB)
+
+
+def rotation(set_bytes: int, cap: int = 1024) -> int:
+    """How many copies of a configuration's inputs (and outputs, workspace) to use in turn, so that
+    together they exceed ROT_BYTES and no call finds the previous call's data in L2."""
+    return max(2, min(cap, -(-ROT_BYTES // max(1, set_bytes))))
+
+
+def time_calls(torch, stream, flush, run, n_sets: int, calls: int = 20, isolated: int = 10):
+    """`run(i)` issues one call on copy i of the inputs. Returns (seconds per call back to back,
+    seconds per call isolated). Back to back: max(calls, 2 n_sets) calls rotating over the copies
+    between one pair of CUDA events (the headline's protocol). Isolated: one call between two
+    events with L2 flushed (a 512 MB write) before it, which adds the event pair's own time
+    (about 2 us) and a cold L2 to every call."""
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    for i in range(3):
+        run(i % n_sets)
+    n = max(calls, 2 * n_sets)
+    a, b = ev(), ev()
+    a.record(stream)
+    for i in range(n):
+        run(i % n_sets)
+    b.record(stream)
+    recs = []
+    for i in range(isolated):
+        flush.zero_()
+        x, y = ev(), ev()
+        x.record(stream)
+        run(i % n_sets)
+        y.record(stream)
+        recs.append((x, y))
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n / 1e3, sum(x.elapsed_time(y) for x, y in recs) / len(recs) / 1e3
 
 
 def fwd_flops(c=FWD) -> float:
@@ -396,33 +431,25 @@ def run_ours(args):
     if world == 1:
         q32, k32, v32 = synth.attention_inputs(1, 1, 4096, 4096, 64, "f32", seed=0)
         q32, k32, v32 = (torch.from_numpy(x).to("cuda") for x in (q32, k32, v32))
-        o32 = torch.empty_like(q32)
-        l32 = torch.empty((1, 1, 4096), dtype=torch.float32, device="cuda")
-
         ws32_bytes = fa.fa_fwd_workspace_bytes(1, 1, 4096, 4096, 64, 0, fa.FA_F32)
-        ws32 = torch.zeros(max(ws32_bytes, 16), dtype=torch.uint8, device="cuda")
+        n32 = rotation(4 * q32.numel() * 4 + ws32_bytes)
+        sets32 = [dict(q=q32.clone(), k=k32.clone(), v=v32.clone(), o=torch.empty_like(q32),
+                       l=torch.empty((1, 1, 4096), dtype=torch.float32, device="cuda"),
+                       ws=torch.zeros(max(ws32_bytes, 16), dtype=torch.uint8, device="cuda")) for _ in range(n32)]
 
-        def run_f32():
-            check(fa.fa_fwd_ws(q32, k32, v32, o32, l32, ws32 if ws32_bytes else None, ws32_bytes, 1, 1, 4096, 4096, 64,
-                               0.125, 0, fa.FA_F32, stream), "fa_fwd_ws f32")
+        def run_f32(i):
+            t = sets32[i]
+            check(fa.fa_fwd_ws(t["q"], t["k"], t["v"], t["o"], t["l"], t["ws"] if ws32_bytes else None, ws32_bytes,
+                               1, 1, 4096, 4096, 64, 0.125, 0, fa.FA_F32, stream), "fa_fwd_ws f32")
 
-        for _ in range(3):
-            run_f32()
-        recs32 = []
-        for _ in range(30):
-            flush.zero_()
-            a, b = ev(), ev()
-            a.record(stream)
-            run_f32()
-            b.record(stream)
-            recs32.append((a, b))
-        torch.cuda.synchronize()
+        t32, t32_iso = time_calls(torch, stream, flush, run_f32, n32, calls=30)
         check(fa.fa_last_status(stream), "f32 forward")
-        t32 = sum(a.elapsed_time(b) for a, b in recs32) / len(recs32) / 1e3
+        del sets32
         tf32 = 4.0 * 4096 * 4096 * 64 / t32 / 1e12
         peak32 = peak_tf / 6.0
         f32 = {"config": "f32 forward, 1 head, M=N=4096, D=64, scale 0.125 through fa_fwd_ws (operands split into three bf16 parts, six products; key blocks of each query tile shared by 4 SMs, merged by the part that finishes last; the split prologue is inside the timed call)", "value": round(tf32, 2),
-               "unit": "TFLOP/s", "us_per_call": round(t32 * 1e6, 1),
+               "unit": "TFLOP/s", "us_per_call": round(t32 * 1e6, 1), "us_isolated": round(t32_iso * 1e6, 1),
+               "l2": f"calls back to back over {n32} copies of the inputs (> 2 x L2); us_isolated: one call, L2 flushed",
                "roofline": {"kernel": "f32_presplit_kernel + fwd_f32ws_kernel<non-causal>", "bound": "tensor",
                             "achieved": round(tf32, 2), "peak": round(peak32, 1), "unit": "TFLOP/s",
                             "frac": round(tf32 / peak32, 4),
@@ -493,7 +520,8 @@ def run_ours(args):
             "heads": FWD["H"],
             "parallelism": f"replicas{world}",
             "l2": "inputs larger than L2: forward and backward rotate over 4 input sets (4 x 63 MB > 129 MB), "
-                  "calls back to back; decode cache 4.29 GB > L2; configs: L2 flushed (512 MB write) before each call",
+                  "calls back to back; decode cache 4.29 GB > L2; configs and f32: calls back to back over copies of their "
+                  "inputs larger than 2 x L2 (us_isolated: one call with L2 flushed)",
         },
         "roofline": {
             "kernel": "fwd_d64_kernel<f16,non-causal>",
@@ -554,35 +582,24 @@ def run_ours(args):
 
 
 def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_src, calls=20):
-    """Every configuration of the workload list, each timed on its own: one call between a pair of
-    CUDA events with L2 flushed before it (decode: its 4.29 GB cache is larger than L2, calls back to
-    back), averaged over `calls` calls after 3 untimed ones."""
-    import numpy as np
+    """Every configuration of the workload list, each timed on its own. `value` and `us_per_call`:
+    calls back to back over enough copies of the inputs (with their outputs and workspace) that
+    together they exceed twice L2, between one pair of CUDA events, as the headline is timed.
+    `us_isolated`: one call between two events with L2 flushed before it (the event pair's own
+    ~2 us and a cold L2 included). Decode: its 4.29 GB cache is larger than L2, calls back to back."""
     import torch
 
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     out = {}
 
-    def timed(fn, flushed=True):
-        for _ in range(3):
-            fn()
-        recs = []
-        for _ in range(calls):
-            if flushed:
-                flush.zero_()
-            a, b = ev(), ev()
-            a.record(stream)
-            fn()
-            b.record(stream)
-            recs.append((a, b))
-        torch.cuda.synchronize()
-        check(fa.fa_last_status(stream), "configuration sweep")
-        return sum(a.elapsed_time(b) for a, b in recs) / len(recs) / 1e3
+    def nbytes(*ts):
+        return sum(t.numel() * t.element_size() for t in ts)
 
-    def tensor_entry(desc, flops, t, kernel, peak=peak_tf, peak_note=None):
+    def tensor_entry(desc, flops, t, t_iso, n_sets, kernel, peak=peak_tf, peak_note=None):
         tf = flops / t / 1e12
         return {"config": desc, "value": round(tf, 2), "unit": "TFLOP/s", "us_per_call": round(t * 1e6, 2),
-                "l2": "flushed before each call",
+                "us_isolated": round(t_iso * 1e6, 2),
+                "l2": f"calls back to back over {n_sets} copies of the inputs (> 2 x L2); us_isolated: one call, "
+                      f"L2 flushed",
                 "roofline": {"kernel": kernel, "bound": "tensor", "achieved": round(tf, 2), "peak": round(peak, 1),
                              "unit": "TFLOP/s", "frac": round(tf / peak, 4),
                              "peak_source": peak_note or f"{peaks_src} bf16 burst (fp16 dense rate equals bf16)",
@@ -596,18 +613,25 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
 
     def forward_entry(name, B, H, M, N, D, dtype, causal, scale, desc, kernel):
         q, k, v = attn(B, H, M, N, D, dtype, seed=M + N)
-        o = torch.empty_like(q)
-        lse = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
         nb = fa.fa_fwd_workspace_bytes(B, H, M, N, D, causal, code[dtype])
-        ws = torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")
-        t = timed(lambda: check(fa.fa_fwd_ws(q, k, v, o, lse, ws if nb else None, nb, B, H, M, N, D, scale, causal,
-                                             code[dtype], stream), name))
+        n = rotation(2 * nbytes(q) + nbytes(k, v) + B * H * M * 4 + nb)
+        sets = [dict(q=q.clone(), k=k.clone(), v=v.clone(), o=torch.empty_like(q),
+                     lse=torch.empty((B, H, M), dtype=torch.float32, device="cuda"),
+                     ws=torch.zeros(max(nb, 16), dtype=torch.uint8, device="cuda")) for _ in range(n)]
+
+        def run(i):
+            t = sets[i]
+            check(fa.fa_fwd_ws(t["q"], t["k"], t["v"], t["o"], t["lse"], t["ws"] if nb else None, nb, B, H, M, N, D,
+                               scale, causal, code[dtype], stream), name)
+
+        t, t_iso = time_calls(torch, stream, flush, run, n, calls)
+        check(fa.fa_last_status(stream), name)
         flops = 4.0 * B * H * M * N * D / (2 if causal else 1)
         peak, note = peak_tf, None
         if dtype == "f32":
             peak = peak_tf / 6.0
             note = f"{peaks_src} bf16 burst / 6 products (each f32 product is six bf16 ones)"
-        out[name] = tensor_entry(desc, flops, t, kernel, peak, note)
+        out[name] = tensor_entry(desc, flops, t, t_iso, n, kernel, peak, note)
 
     # fp16 forward, B4 H12 D64, M = N over {512, 1024, 2048}; bf16 and causal at 2048
     for n in (512, 1024, 2048):
@@ -620,22 +644,30 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
                   "fp16 forward B4 H12 M=N=2048 D64 scale 0.125 causal (FLOP halved)", "fwd_d64_kernel<f16,causal>")
     # FP8 forward (E4M3 operands, fp16 I/O) at the fp16 workload's largest shape: the whole call
     # (three quantisation launches, then the attention kernel), against the fp8 tensor peak
+    q, k, v = attn(4, 12, 2048, 2048, 64, "f16", seed=2048)
+    signs = torch.from_numpy(synth.hadamard_signs(64, 0)).cuda()
+    nb = fa.fa_fwd_fp8_workspace_bytes(4, 12, 2048, 2048, 64)
+    n = rotation(2 * nbytes(q) + nbytes(k, v) + nb)
+    sets = [dict(q=q.clone(), k=k.clone(), v=v.clone(), o=torch.empty_like(q),
+                 lse=torch.empty((4, 12, 2048), dtype=torch.float32, device="cuda"),
+                 ws=torch.empty(nb, dtype=torch.uint8, device="cuda")) for _ in range(n)]
     for causal in (False, True):
-        q, k, v = attn(4, 12, 2048, 2048, 64, "f16", seed=2048)
-        o = torch.empty_like(q)
-        lse = torch.empty((4, 12, 2048), dtype=torch.float32, device="cuda")
-        signs = torch.from_numpy(synth.hadamard_signs(64, 0)).cuda()
-        nb = fa.fa_fwd_fp8_workspace_bytes(4, 12, 2048, 2048, 64)
-        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-        t = timed(lambda: check(fa.fa_fwd_fp8(q, k, v, o, lse, signs, ws, nb, 4, 12, 2048, 2048, 64, 0.125, causal,
-                                              fa.FA_F16, stream), "fa_fwd_fp8"))
+        def run(i):
+            t = sets[i]
+            check(fa.fa_fwd_fp8(t["q"], t["k"], t["v"], t["o"], t["lse"], signs, t["ws"], nb, 4, 12, 2048, 2048, 64,
+                                0.125, causal, fa.FA_F16, stream), "fa_fwd_fp8")
+
+        t, t_iso = time_calls(torch, stream, flush, run, n, calls)
+        check(fa.fa_last_status(stream), "fa_fwd_fp8")
         tag = "causal" if causal else "noncausal"
         out[f"fwd_fp8_N2048_{tag}"] = tensor_entry(
             f"FP8 forward (E4M3 operands after the Hadamard-times-sign transform, per-block scales; fp16 I/O) "
             f"B4 H12 M=N=2048 D64 scale 0.125 {tag}: quantisation + attention per call",
-            4.0 * 4 * 12 * 2048 * 2048 * 64 / (2 if causal else 1), t, f"fwd_fp8_kernel<f16,{tag}> (+ fp8 quantisation)",
+            4.0 * 4 * 12 * 2048 * 2048 * 64 / (2 if causal else 1), t, t_iso, n,
+            f"fwd_fp8_kernel<f16,{tag}> (+ fp8 quantisation)",
             peak_tf * 2.0, f"{peaks_src} bf16 burst x nominal fp8/bf16 (4.5/2.25)")
-    # f32, one head, 256^2 and 4096^2 (3xTF32)
+    del sets
+    # f32, one head, 256^2 (the 4096^2 case is the main line's `f32` object)
     forward_entry("fwd_f32_N256", 1, 1, 256, 256, 64, "f32", False, 0.125,
                   "f32 forward 1 head Nq=Nk=256 D64 scale 0.125 (fa_fwd_ws: three bf16 parts, six products)",
                   "f32_presplit_kernel + fwd_f32ws_kernel<non-causal>")
@@ -652,31 +684,43 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
             o = torch.empty_like(q)
             lse = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
             check(fa.fa_fwd(q, k, v, o, lse, B, H, M, M, 64, 0.5, causal, fa.FA_F16, stream), "fa_fwd")
-            dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+            nb = fa.fa_bwd_ws_workspace_bytes(B, H, M, 64)
+            n = rotation(8 * nbytes(q) + nbytes(lse) + nb)
+            sets = [dict(q=q.clone(), k=k.clone(), v=v.clone(), o=o.clone(), do=do.clone(), lse=lse.clone(),
+                         dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                         ws=torch.empty(nb, dtype=torch.uint8, device="cuda"),
+                         dws=torch.empty((B, H, M), dtype=torch.float32, device="cuda")) for _ in range(n)]
             flops = 2.5 * 4.0 * B * H * M * M * 64 / (2 if causal else 1)
             tag = "causal" if causal else "noncausal"
-            nb = fa.fa_bwd_ws_workspace_bytes(B, H, M, 64)
-            ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
-            t = timed(lambda: check(fa.fa_bwd_ws(q, k, v, o, do, lse, dq, dk, dv, ws, nb, B, H, M, M, 64, 0.5, causal,
-                                                 fa.FA_F16, stream), "fa_bwd_ws"))
+
+            def run_ws(i):
+                t = sets[i]
+                check(fa.fa_bwd_ws(t["q"], t["k"], t["v"], t["o"], t["do"], t["lse"], t["dq"], t["dk"], t["dv"],
+                                   t["ws"], nb, B, H, M, M, 64, 0.5, causal, fa.FA_F16, stream), "fa_bwd_ws")
+
+            def run3(i):
+                t = sets[i]
+                check(fa.fa_bwd(t["q"], t["k"], t["v"], t["o"], t["do"], t["lse"], t["dq"], t["dk"], t["dv"],
+                                t["dws"], B, H, M, M, 64, 0.5, causal, fa.FA_F16, stream), "fa_bwd")
+
+            t, t_iso = time_calls(torch, stream, flush, run_ws, n, calls)
             desc = f"fp16 backward B{B} H{H} N{M} D64 scale 0.5 {tag}"
             out[f"{name0}_bwd_fused_{tag}"] = tensor_entry(
                 desc + " through fa_bwd_ws (delta, fused dK/dV/dQ, dQ conversion; FLOP = 2.5 x forward)", flops, t,
-                f"bwd_fused64_kernel<f16,{tag}>")
-            dws = torch.empty((B, H, M), dtype=torch.float32, device="cuda")
-            run3 = lambda: check(fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, dws, B, H, M, M, 64, 0.5, causal,
-                                           fa.FA_F16, stream), "fa_bwd")
-            t = timed(run3)  # automatic schedule: dK/dV and dQ on CTA pairs when not causal
+                t_iso, n, f"bwd_fused64_kernel<f16,{tag}>")
+            t, t_iso = time_calls(torch, stream, flush, run3, n, calls)  # dK/dV and dQ on CTA pairs when not causal
             kern3 = "bwd_dkdv64_kernel + bwd_dq_kernel" if causal else "bwd_dkdv64_pair_kernel + bwd_dq64_pair_kernel"
             out[f"{name0}_bwd_3kernels_{tag}"] = tensor_entry(
-                desc + " through fa_bwd (delta, dK/dV, dQ kernels; FLOP = 2.5 x forward)", flops, t,
+                desc + " through fa_bwd (delta, dK/dV, dQ kernels; FLOP = 2.5 x forward)", flops, t, t_iso, n,
                 f"{kern3}<f16,{tag}>")
             if not causal:
                 with fa.schedule(fa.FA_SCHED_BWD_PAIR, 0):
-                    t = timed(run3)
+                    t, t_iso = time_calls(torch, stream, flush, run3, n, calls)
                 out[f"{name0}_bwd_3kernels_single_cta_{tag}"] = tensor_entry(
                     desc + " through fa_bwd with single-CTA dK/dV and dQ kernels (FLOP = 2.5 x forward)", flops, t,
-                    f"bwd_dkdv64_kernel + bwd_dq_kernel<f16,{tag}>")
+                    t_iso, n, f"bwd_dkdv64_kernel + bwd_dq_kernel<f16,{tag}>")
+            check(fa.fa_last_status(stream), "backward configurations")
+            del sets
     # bf16 decode B8 H32 N32768 D128 at n_splits 16 and 256 (64 is the main line's)
     d = DEC
     qdec = dev(synth.decode_query(d["B"], d["H"], d["D"], d["dtype"], 0), "bf16")
@@ -689,9 +733,12 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
     for ns in (16, 256):
         ws = torch.empty(fa.fa_decode_workspace_bytes(d["B"], d["H"], d["D"], ns) // 4, dtype=torch.float32,
                          device="cuda")
-        t = timed(lambda: check(fa.fa_decode(qdec, kc, vc, odec, ws, d["B"], d["H"], d["N"], d["D"],
-                                             1 / math.sqrt(d["D"]), ns, fa.FA_BF16, stream), "fa_decode"),
-                  flushed=False)
+
+        def run(i):
+            check(fa.fa_decode(qdec, kc, vc, odec, ws, d["B"], d["H"], d["N"], d["D"], 1 / math.sqrt(d["D"]), ns,
+                               fa.FA_BF16, stream), "fa_decode")
+
+        t, _ = time_calls(torch, stream, flush, run, 1, calls, isolated=1)
         gbs = dec_bytes() / t / 1e9
         out[f"decode_splits{ns}"] = {
             "config": f"bf16 decode B8 H32 N32768 D128 n_splits {ns} (cache 4.29 GB > L2, calls back to back)",
@@ -699,6 +746,7 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
             "roofline": {"kernel": "decode_split_kernel<128,bf16> + decode_combine_kernel", "bound": "hbm",
                          "achieved": round(gbs, 1), "peak": peak_bw, "unit": "GB/s", "frac": round(gbs / peak_bw, 4),
                          "peak_source": f"{peaks_src} copy bandwidth", "traffic": None}}
+    check(fa.fa_last_status(stream), "decode configurations")
     del kc, vc
     torch.cuda.empty_cache()
     return out

@@ -22,6 +22,11 @@
 // buffers at 128 + 64 b (64 f32 columns each; P's parts 0 and 1 written over S, part 2 in 32 columns
 // of its own), so the score products can run up to three blocks ahead of P V; two block partials of
 // O at 384 + 64 o.
+// With few query tiles each tile's keys are split over `parts` CTAs. When every CTA holds one such
+// part and the parts of a tile can run as one thread-block cluster (parts 2, 4 or 8, all clusters
+// resident at once), each part leaves its partial in its own shared memory and, after a cluster
+// barrier, each CTA merges 128 / parts rows of the tile from all the parts' shared memory;
+// otherwise the partials go through the workspace and the part that counts in last merges them.
 #include "fa_internal.cuh"
 #include "ptx.cuh"
 
@@ -38,6 +43,7 @@ constexpr int kThreadsW = 352;            // softmax 0-7, producer 8, MMA issuer
 constexpr int kWarpProdW = 8, kWarpMmaW = 9, kWarpPvW = 10;
 constexpr float kLog2eW = 1.4426950408889634f;
 constexpr float kLn2W = 0.6931471805599453f;
+constexpr int kPartPitch = kDw + 4;       // cluster merge: a partial's rows in shared memory (floats)
 // Tensor memory: Q part p at 32 p; S buffer b (0..2) at 128 + 64 b, P's parts 0 and 1 written over it,
 // part 2 at p2_col(b) (96, 320, 352); O partial buffer o (0..1) at 384 + 64 o
 constexpr uint32_t cQ = 0, cS = 128, cO = 384;
@@ -47,7 +53,7 @@ struct F32wHdr {
   unsigned long long kv_full[kStagesW], kv_empty[kStagesW];
   unsigned long long q_full;      // the unit's Q rows are in tensor memory (8 softmax warps)
   unsigned long long s_full[3];   // S of buffer b computed
-  unsigned long long p_full[3];   // P of buffer b stored, the previous block's partial read (8 warps)
+  unsigned long long p_full[3];   // P of buffer b stored (8 warps)
   unsigned long long s_free[3];   // P V has read P of buffer b: S may be computed there again
   unsigned long long pv_done[2];  // P V into O partial buffer o computed
   unsigned long long mma_done[2];
@@ -92,13 +98,72 @@ __global__ void __launch_bounds__(256) f32_presplit_kernel(const float4* __restr
   }
 }
 
+// Cluster merge by the 256 softmax threads of rank r: rows [r R, r R + R) of the tile, R = 128 / P,
+// tpr threads a row and cpt columns each, from the partials that the P parts of the tile left in
+// their shared memory at `data` (row-major [128][kPartPitch], then m [128] and l [128]; parts
+// without keys left none). Every shared::cluster load of a thread is issued before any is used:
+// one at a time they cost a round trip each (about 180 ns, measured).
+template <int P>
+__device__ __forceinline__ void cluster_merge(uint32_t data, int nbt, int q0, int bh, int M, float* __restrict__ O,
+                                              float* __restrict__ LSE) {
+  constexpr int R = kBMw / P, tpr = 256 / R, cpt = kDw / tpr, nv = cpt / 4;
+  const int tid = static_cast<int>(threadIdx.x);
+  const int r = static_cast<int>(ptx::cluster_rank()) * R + tid / tpr;
+  const int cg = (tid % tpr) * cpt;
+  bool has[P];
+  uint32_t base[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    has[p] = (p + 1) * nbt / P > p * nbt / P;
+    base[p] = ptx::peer_addr(data, static_cast<uint32_t>(p));
+  }
+  float mp[P], lp[P];
+  float4 x[P][nv];
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    mp[p] = -INFINITY;
+    lp[p] = 0.f;
+    if (has[p]) {
+      mp[p] = ptx::ld_cluster_f32(base[p] + (kBMw * kPartPitch + r) * 4);
+      lp[p] = ptx::ld_cluster_f32(base[p] + (kBMw * kPartPitch + kBMw + r) * 4);
+#pragma unroll
+      for (int v = 0; v < nv; ++v) x[p][v] = ptx::ld_cluster_v4(base[p] + (r * kPartPitch + cg + 4 * v) * 4);
+    }
+  }
+  float mm = -INFINITY;
+#pragma unroll
+  for (int p = 0; p < P; ++p) mm = fmaxf(mm, mp[p]);
+  float L = 0.f;
+  float4 acc[nv];
+#pragma unroll
+  for (int v = 0; v < nv; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int p = 0; p < P; ++p) {
+    if (!has[p] || mp[p] == -INFINITY) continue;
+    const float w = ptx::ex2(mp[p] - mm);
+    L = fmaf(w, lp[p], L);
+#pragma unroll
+    for (int v = 0; v < nv; ++v)
+      acc[v] = make_float4(fmaf(w, x[p][v].x, acc[v].x), fmaf(w, x[p][v].y, acc[v].y), fmaf(w, x[p][v].z, acc[v].z),
+                           fmaf(w, x[p][v].w, acc[v].w));
+  }
+  const int row = q0 + r;
+  if (row < M) {
+    const float inv = 1.f / L;
+    float4* dst = reinterpret_cast<float4*>(O + (static_cast<size_t>(bh) * M + row) * kDw + cg);
+#pragma unroll
+    for (int v = 0; v < nv; ++v) dst[v] = make_float4(acc[v].x * inv, acc[v].y * inv, acc[v].z * inv, acc[v].w * inv);
+    if (tid % tpr == 0 && LSE != nullptr) LSE[static_cast<size_t>(bh) * M + row] = (mm + __log2f(L)) * kLn2W;
+  }
+}
+
 template <bool CAUSAL>
 __global__ void __launch_bounds__(kThreadsW, 1)
     fwd_f32ws_kernel(const __grid_constant__ CUtensorMap tmK0, const __grid_constant__ CUtensorMap tmK1,
                      const __grid_constant__ CUtensorMap tmK2, const __grid_constant__ CUtensorMap tmV0,
                      const __grid_constant__ CUtensorMap tmV1, const __grid_constant__ CUtensorMap tmV2,
                      const float* __restrict__ Q, float* __restrict__ O, float* __restrict__ LSE, int BH, int M, int N,
-                     float scale_log2_signed, int parts, float* __restrict__ ws,
+                     float scale_log2_signed, int parts, int cl, float* __restrict__ ws,
                      unsigned long long* __restrict__ counters, uint32_t epoch, DevStatus* status,
                      unsigned long long budget_ns) {
   extern __shared__ uint8_t smem_raw[];
@@ -250,8 +315,8 @@ __global__ void __launch_bounds__(kThreadsW, 1)
           for (int j = 0; j < nb && ok; ++j) {
             const uint32_t gg = g + j, b = gg % 3u, ob = gg & 1u;
             const int st = gg % kStagesW;
-            // P(gg) stored (and the partial two blocks back, which O_ob held, read); its S was
-            // computed from this stage, so V of block gg has landed too
+            // P(gg) stored (the partial two blocks back, which O_ob held, was read before); its S
+            // was computed from this stage, so V of block gg has landed too
             ok = wait(&hdr->p_full[b], (gg / 3u) & 1u, 22);
             if (!ok) break;
             // O_ob = sum of P_x V_y for block gg, from zero (V MN-major); then P's buffer and the
@@ -387,6 +452,13 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         ptx::tmem_st16(tB + c0 / 2, w0);
         ptx::tmem_st16(tB + 32 + c0 / 2, w1);
         ptx::tmem_st16(tmem + lane_sel + p2_col(b) + c0 / 2, w2);
+        // P(gg) stored: its P V may run at once. The O partial buffer it writes held block gg - 2's
+        // partial, which this warp read during the previous block, so the hand-over does not wait
+        // for block gg - 1's P V, read next.
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->p_full[b]));
         const float2 sum2 = ptx::fadd2(sum_a, sum_b);
         // the previous block's partial joins the accumulator; both go to the new maximum
         if (j > 0) {
@@ -406,10 +478,6 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         }
         l = fmaf(l, corr, sum2.x + sum2.y);
         m2 = m_new;
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(ptx::smem_u32(&hdr->p_full[b]));
       }
       if (!ok) break;
       {
@@ -433,6 +501,21 @@ __global__ void __launch_bounds__(kThreadsW, 1)
         ok = exchange(2, l, lo);
         if (!ok) break;
         l += lo;
+      }
+      if (cl) {
+        // this part's partial into this CTA's shared memory, row-major [128][kPartPitch], then m
+        // and l; merged after the cluster barrier below. The K/V stages are free: every block's
+        // copies have landed and the products that read them have completed.
+        float* sp = reinterpret_cast<float*>(smem_raw + (data - ptx::smem_u32(smem_raw)));
+        float4* dst = reinterpret_cast<float4*>(sp + rr * kPartPitch + c0);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) dst[v] = make_float4(oacc[4 * v], oacc[4 * v + 1], oacc[4 * v + 2], oacc[4 * v + 3]);
+        if (half == 0) {
+          sp[kBMw * kPartPitch + rr] = m2;
+          sp[kBMw * kPartPitch + kBMw + rr] = l;
+        }
+        ptx::tc_fence_before();
+        continue;
       }
       if (parts > 1) {
         // unnormalised partial of this part, column-major (a warp's 32 rows of a column are one
@@ -515,6 +598,23 @@ __global__ void __launch_bounds__(kThreadsW, 1)
     }
   }
 
+  if (cl) {
+    __syncthreads();      // every warp converged (the .aligned cluster barrier)
+    ptx::cluster_sync();  // every part's partial is in its CTA's shared memory
+    if (warp < 8) {
+      int bh, q0, jb, nb;
+      tile_of(blockIdx.x, bh, q0, jb, nb);
+      const int nbt = CAUSAL ? min(nkb, (q0 + kBMw - 1) / kBNw + 1) : nkb;
+      if (parts == 2)
+        cluster_merge<2>(data, nbt, q0, bh, M, O, LSE);
+      else if (parts == 4)
+        cluster_merge<4>(data, nbt, q0, bh, M, O, LSE);
+      else
+        cluster_merge<8>(data, nbt, q0, bh, M, O, LSE);
+    }
+    __syncwarp();
+    ptx::cluster_sync();  // the other CTAs have read this one's shared memory
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == kWarpMmaW) {
@@ -567,12 +667,39 @@ cudaError_t launch_fwd_f32_presplit(const void* Q, const void* K, const void* V,
   cfg.gridDim = dim3(static_cast<unsigned>(units < ctx.num_sms ? units : ctx.num_sms));
   cfg.blockDim = dim3(kThreadsW);
   cfg.dynamicSmemBytes = kSmemW;
+  // The parts of a tile as one cluster when every CTA holds one part and all the clusters can be
+  // resident at once (the hardware places a cluster's CTAs together; a cluster waits only for its
+  // own CTAs).
+  int cl = 0;
+  cudaLaunchAttribute cattr[2];
+  cattr[0] = attr[0];
+  if ((parts == 2 || parts == 4 || parts == 8) && units <= ctx.num_sms) {
+    static int fits[2][9] = {{-1, -1, -1, -1, -1, -1, -1, -1, -1}, {-1, -1, -1, -1, -1, -1, -1, -1, -1}};
+    cattr[1].id = cudaLaunchAttributeClusterDimension;
+    cattr[1].val.clusterDim.x = static_cast<unsigned>(parts);
+    cattr[1].val.clusterDim.y = 1;
+    cattr[1].val.clusterDim.z = 1;
+    int& f = fits[causal ? 1 : 0][parts];
+    if (f < 0) {
+      cudaLaunchConfig_t q = cfg;
+      q.attrs = cattr;
+      q.numAttrs = 2;
+      int n = 0;
+      f = cudaOccupancyMaxActiveClusters(&n, kern, &q) == cudaSuccess ? n : 0;
+      cudaGetLastError();  // a refused query leaves the split through the workspace
+    }
+    cl = static_cast<long long>(f) * parts >= units ? 1 : 0;
+  }
+  if (cl) {
+    cfg.attrs = cattr;
+    cfg.numAttrs = 2;
+  }
   unsigned long long* counters =
       parts > 1 ? reinterpret_cast<unsigned long long*>(split_ws + static_cast<size_t>(units) * kF32SlotFloats)
                 : nullptr;
   return cudaLaunchKernelEx(&cfg, kern, mk[0], mk[1], mk[2], mv[0], mv[1], mv[2], static_cast<const float*>(Q),
                             static_cast<float*>(O),
-                            LSE, BH, M, N, scale * kLog2eW, parts, split_ws, counters, epoch, ctx.status,
+                            LSE, BH, M, N, scale * kLog2eW, parts, cl, split_ws, counters, epoch, ctx.status,
                             ctx.wait_budget_ns);
 }
 

@@ -113,15 +113,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow(bar, parity, w, site);
 }
 
-// ------------------------------------------------------- CTA pairs (clusters of two)
-// The kernels that run as CTA pairs (tcgen05 cta_group::2) use these. A pair is a cluster of two
-// CTAs; rank 0 issues the MMAs for both.
+// ------------------------------------------------------- clusters
+// The kernels that run as CTA pairs (tcgen05 cta_group::2; a pair is a cluster of two CTAs, rank 0
+// issues the MMAs for both) and the f32 forward's cluster merge use these.
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return r;
 }
-// Every thread of both CTAs: all memory operations before it are visible to both CTAs after it.
+// Every thread of every CTA of the cluster: all memory operations before it are visible to all of
+// them after it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -130,6 +131,18 @@ __device__ __forceinline__ uint32_t peer_addr(uint32_t bar, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(bar), "r"(rank));
   return r;
+}
+// Loads from another CTA's shared memory (a shared::cluster address from peer_addr).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_v4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
+               : "memory");
+  return v;
 }
 // Arrive on a barrier given by its shared::cluster address (this CTA's or the peer's). Default
 // (CTA-scope) semantics: what an arrival hands over across the pair is tensor memory the arriving

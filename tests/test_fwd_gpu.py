@@ -125,6 +125,14 @@ F32_SHAPES = [
     (2, 3, 300, 200),
     (1, 1, 1, 1),
     (1, 2, 129, 777),
+    # few tiles, long key ranges: each tile's keys split over many CTAs (19, 12 and 30 parts),
+    # merged by the part that counts in last
+    (1, 1, 1000, 3000),
+    (1, 2, 700, 2500),
+    (1, 1, 640, 3900),
+    # parts of a tile as one cluster, merged through shared memory: 2 parts (256^2 and 300 x 200
+    # above), 4 (4096^2 above) and 8 here (19 tiles, the last ragged; causal: empty parts)
+    (1, 1, 2400, 1000),
 ]
 
 
