@@ -249,11 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::prefetch_tmap(&tmQ);
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
-    // whole pairs (the schedule of small problems, where the start weighs most): the first
-    // pair's Q tiles and first key blocks start towards L2 while the CTA sets up
+    // where the start weighs most (whole pairs, or split shares of at most 128 units), the first
+    // piece's Q tiles and first key blocks start towards L2 while the CTA sets up: a dependent
+    // launch's set-up runs on the SMs the previous kernel has left, during that kernel's tail.
+    // (A prefetch only warms L2, where the previous kernel's writes land too.) At B4 H12 N2048
+    // (40 units a CTA) 63.2 -> 62.0 us back to back.
     Schedule<CAUSAL> first(split, BH, num_pairs, nkb);
     Piece p0;
-    if (!split && first.next(p0, split, BH, num_pairs, nkb)) {
+    if ((!split || first.e - first.u <= 128u) && first.next(p0, split, BH, num_pairs, nkb)) {
       for (int t = 0; t < 2; ++t) ptx::tma_prefetch_l2_3d(&tmQ, 0, p0.q0 + t * kBM, p0.bh);
       const int nb = p0.nb1 < kStages ? p0.nb1 : kStages;
       for (int j = 0; j < nb; ++j) {
