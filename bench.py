@@ -708,17 +708,22 @@ def bench_configs(fa, synth, dev, stream, flush, check, peak_tf, peak_bw, peaks_
             out[f"{name0}_bwd_fused_{tag}"] = tensor_entry(
                 desc + " through fa_bwd_ws (delta, fused dK/dV/dQ, dQ conversion; FLOP = 2.5 x forward)", flops, t,
                 t_iso, n, f"bwd_fused64_kernel<f16,{tag}>")
-            t, t_iso = time_calls(torch, stream, flush, run3, n, calls)  # dK/dV and dQ on CTA pairs when not causal
-            kern3 = "bwd_dkdv64_kernel + bwd_dq_kernel" if causal else "bwd_dkdv64_pair_kernel + bwd_dq64_pair_kernel"
+            # automatic schedule: dK/dV and dQ on CTA pairs for non-causal calls with fewer key
+            # tiles than SMs (the Z1 H2 case), single CTAs otherwise
+            t, t_iso = time_calls(torch, stream, flush, run3, n, calls)
+            paired = not causal and B * H * (M // 128) < 152
+            kern3 = "bwd_dkdv64_pair_kernel + bwd_dq64_pair_kernel" if paired else "bwd_dkdv64_kernel + bwd_dq_kernel"
             out[f"{name0}_bwd_3kernels_{tag}"] = tensor_entry(
                 desc + " through fa_bwd (delta, dK/dV, dQ kernels; FLOP = 2.5 x forward)", flops, t, t_iso, n,
                 f"{kern3}<f16,{tag}>")
-            if not causal:
-                with fa.schedule(fa.FA_SCHED_BWD_PAIR, 0):
+            if not causal:  # the other form, forced
+                with fa.schedule(fa.FA_SCHED_BWD_PAIR, 0 if paired else 1):
                     t, t_iso = time_calls(torch, stream, flush, run3, n, calls)
-                out[f"{name0}_bwd_3kernels_single_cta_{tag}"] = tensor_entry(
-                    desc + " through fa_bwd with single-CTA dK/dV and dQ kernels (FLOP = 2.5 x forward)", flops, t,
-                    t_iso, n, f"bwd_dkdv64_kernel + bwd_dq_kernel<f16,{tag}>")
+                other = "single_cta" if paired else "pair"
+                kern_o = "bwd_dkdv64_kernel + bwd_dq_kernel" if paired else "bwd_dkdv64_pair_kernel + bwd_dq64_pair_kernel"
+                out[f"{name0}_bwd_3kernels_{other}_{tag}"] = tensor_entry(
+                    desc + f" through fa_bwd with the dK/dV and dQ kernels forced to {other.replace('_', ' ')} "
+                    f"(FLOP = 2.5 x forward)", flops, t, t_iso, n, f"{kern_o}<f16,{tag}>")
             check(fa.fa_last_status(stream), "backward configurations")
             del sets
     # bf16 decode B8 H32 N32768 D128 at n_splits 16 and 256 (64 is the main line's)

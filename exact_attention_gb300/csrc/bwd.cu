@@ -398,6 +398,7 @@ struct OvHdr {
   unsigned long long full[kStagesMax], empty[kStagesMax];
   unsigned long long s_full, dp_full;      // MMA -> compute
   unsigned long long sig1, sig2;           // compute -> MMA (8 warps each)
+  unsigned long long s_read;               // compute -> MMA: S^T(i) is in registers (dK/dV, fused)
   unsigned long long free1, free2;         // MMA -> compute: packed operand regions read
   unsigned long long acc_full, mma_done[2];
   // fused dK/dV/dQ only: dQ_i computed, dQ_i read from TMEM, dQ_i staged, staging read by the reduce
@@ -441,6 +442,7 @@ __device__ __forceinline__ void ov_init(OvHdr* hdr, int stages, uint32_t full_co
   ptx::mbar_init(ptx::smem_u32(&hdr->dp_full), 1);
   ptx::mbar_init(ptx::smem_u32(&hdr->sig1), 8);
   ptx::mbar_init(ptx::smem_u32(&hdr->sig2), 8);
+  ptx::mbar_init(ptx::smem_u32(&hdr->s_read), 8);
   ptx::mbar_init(ptx::smem_u32(&hdr->free1), 1);
   ptx::mbar_init(ptx::smem_u32(&hdr->free2), 1);
   ptx::mbar_init(ptx::smem_u32(&hdr->acc_full), 1);
@@ -633,8 +635,9 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           const int st = it_s % C::kStages;
           const bool more = i + 1 < itm.hi;
           const bool acc = i > itm.lo;
-          // S^T(i) read and P^T(i) stored
-          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+          // scores issuer: S^T(i) read (its columns free for S^T(i+1) while the compute warps form
+          // P); gradient issuer: P^T(i) stored
+          ok = scores ? wait(&hdr->s_read, (n1++) & 1u, 27) : wait(&hdr->sig1, (n1++) & 1u, 22);
           if (!ok) break;
           ptx::tc_fence_after();
           if (scores) {
@@ -714,6 +717,7 @@ __global__ void __launch_bounds__(kThreadsO, 1)
           ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
           ptx::tmem_wait_ld32(s);
           ptx::tmem_wait_ld32(s + 32);
+          signal(&hdr->s_read);  // S^T(i+1) may be computed while P is formed
           const float2 c2 = make_float2(sl2, sl2);
 #pragma unroll
           for (int q = 0; q < 64; q += 2) {
@@ -936,6 +940,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
     ptx::mbar_init(ptx::smem_u32(&hdr->dq_full), 1);
     ptx::mbar_init(ptx::smem_u32(&hdr->sig1), kCwF);
     ptx::mbar_init(ptx::smem_u32(&hdr->sig2), kCwF);
+    ptx::mbar_init(ptx::smem_u32(&hdr->s_read), kCwF);
     ptx::mbar_init(ptx::smem_u32(&hdr->dq_free), kCwF);
     ptx::mbar_init(ptx::smem_u32(&hdr->dq_staged), kCwF);
     ptx::mbar_init(ptx::smem_u32(&hdr->stg_free), 1);
@@ -1088,8 +1093,9 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           const int st = it_s % C::kStages;
           const bool more = i + 1 < itm.hi;
           const bool acc = i > itm.lo;
-          // S^T(i) read and P^T(i) stored
-          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+          // scores issuer: S^T(i) read (its columns free for S^T(i+1) while the compute warps form
+          // P); gradient issuer: P^T(i) stored
+          ok = scores ? wait(&hdr->s_read, (n1++) & 1u, 27) : wait(&hdr->sig1, (n1++) & 1u, 22);
           if (!ok) break;
           ptx::tc_fence_after();
           if (scores) {
@@ -1264,6 +1270,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
           for (int c = 0; c < kQcF; c += 32) ptx::tmem_ld32(tmem + lane_sel + cS + c0 + c, s + c);
 #pragma unroll
           for (int c = 0; c < kQcF; c += 32) ptx::tmem_wait_ld32(s + c);
+          signal(&hdr->s_read);  // S^T(i+1) may be computed while P is formed
           const float2 c2 = make_float2(sl2, sl2);
           // the block's -LSE values are read four at a time: every lane reads the same 16 bytes
 #pragma unroll

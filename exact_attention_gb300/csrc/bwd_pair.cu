@@ -45,6 +45,7 @@ struct PairHdr {
   unsigned long long peer_fixed, peer_full[kPStages];  // rank 0: rank 1's loads have landed
   unsigned long long s_full, dp_full, free1, free2, acc_full;  // MMA -> compute, committed to both CTAs
   unsigned long long sig1, sig2;  // rank 0: compute warps of both CTAs -> MMA (16 arrivals)
+  unsigned long long s_read;      // rank 0: both CTAs' S^T(i) in registers (16 arrivals)
   unsigned long long mma_done[2];
   uint32_t tmem_base;
   int abort_flag;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     ptx::mbar_init(ptx::smem_u32(&hdr->free2), 1);
     ptx::mbar_init(ptx::smem_u32(&hdr->acc_full), 1);
     ptx::mbar_init(ptx::smem_u32(&hdr->sig1), 16);
+    ptx::mbar_init(ptx::smem_u32(&hdr->s_read), 16);
     ptx::mbar_init(ptx::smem_u32(&hdr->sig2), 16);
     ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[0]), 1);
     ptx::mbar_init(ptx::smem_u32(&hdr->mma_done[1]), 1);
@@ -289,8 +291,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
           const int st = it_s % kPStages;
           const bool more = i + 1 < itm.hi;
           const bool acc = i > itm.lo;
-          // S^T(i) read and P^T(i) stored, in both CTAs
-          ok = wait(&hdr->sig1, (n1++) & 1u, 22);
+          // scores issuer: S^T(i) read in both CTAs (its columns free for S^T(i+1) while the
+          // compute warps form P); gradient issuer: P^T(i) stored in both CTAs
+          ok = scores ? wait(&hdr->s_read, (n1++) & 1u, 27) : wait(&hdr->sig1, (n1++) & 1u, 22);
           if (!ok) break;
           ptx::tc_fence_after();
           if (scores) {
@@ -357,6 +360,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t lane_sel = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t c0 = static_cast<uint32_t>(half * 64);  // this warp's query columns [c0, c0 + 64)
     const uint32_t sig1 = ptx::peer_addr(ptx::smem_u32(&hdr->sig1), 0);
+    const uint32_t s_read = ptx::peer_addr(ptx::smem_u32(&hdr->s_read), 0);
     const uint32_t sig2 = ptx::peer_addr(ptx::smem_u32(&hdr->sig2), 0);
     uint32_t it_s = 0, nb = 0, n_acc = 0;  // n_acc: items with a query block (acc_full phases)
     int n_item = 0;
@@ -390,6 +394,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
           ptx::tmem_ld32(tmem + lane_sel + cS + c0 + 32, s + 32);
           ptx::tmem_wait_ld32(s);
           ptx::tmem_wait_ld32(s + 32);
+          signal(s_read);  // S^T(i+1) may be computed while P is formed
           const float2 c2 = make_float2(sl2, sl2);
 #pragma unroll
           for (int q = 0; q < 64; q += 2) {

@@ -391,12 +391,16 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   FA_TRY(make_ctx(&ctx, stream));
   BwdSplit sp{};
   if (dQacc != nullptr && split_ws != nullptr && use_bwd_split(B * H, M, N, D, causal, ctx.num_sms)) sp.ws = split_ws;
-  // fa_bwd's dK/dV and dQ kernels at D = 64 on CTA pairs: by default for non-causal calls (where
-  // they measured as fast or faster); causal calls keep single CTAs (a pair's 256 rows walk the
-  // blocks of its later half, so the earlier CTA gets one wholly masked block per item, and the
-  // items are coarser to balance)
+  // fa_bwd's dK/dV and dQ kernels at D = 64 on CTA pairs: by default only for non-causal calls
+  // with fewer key tiles than SMs, where they measured 4-7 % faster (Z1 H2 N1024: 30.7 against
+  // 32.8 us). With a wave or more of key tiles the single-CTA kernels are 2-3 % faster (B4 H12
+  // N2048: 251 against 257 us); causal calls keep single CTAs (a pair's 256 rows walk the blocks
+  // of its later half, so the earlier CTA gets one wholly masked block per item, and the items are
+  // coarser to balance).
   const int pair_forced = g_sched_bwd_pair.load();
-  sp.pair = dQacc == nullptr && D == 64 && (pair_forced == 1 || (pair_forced == -1 && causal == 0));
+  const long long key_tiles = static_cast<long long>(B) * H * ((N + 127) / 128);
+  sp.pair = dQacc == nullptr && D == 64 &&
+            (pair_forced == 1 || (pair_forced == -1 && causal == 0 && key_tiles < ctx.num_sms));
   cudaError_t e =
       launch_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, delta_ws, dQacc, B * H, M, N, D, scale, causal != 0, dtype, sp, ctx);
   if (e == cudaErrorNotSupported) return fail(FA_ERR_UNSUPPORTED, "%s: configuration not supported", name);

@@ -163,12 +163,13 @@ size_t fa_fwd_host_workspace_bytes(int B, int H, int M, int N, int D, int causal
  * and the identity D_i = rowsum(dO o O), dS = P o (dP - D) from the "Flash
  * Attention" notes ("IO complexity"). Three launches on `stream`: delta, then
  * dK/dV (one CTA per key block walking the query blocks), then dQ (one CTA per
- * query block walking the key blocks). With D = 64 and no causal mask the dK/dV
- * and dQ launches run on CTA pairs ("Flash Attention" notes, "FlashAttention 4":
- * a 256-row tile split across two CTAs with tcgen05 cta_group::2): each cluster
- * of two CTAs owns 256 keys (dK/dV) or 256 queries (dQ), and one MMA covers both
- * CTAs' rows with each CTA holding half of the other operand (fa_set_schedule,
- * FA_SCHED_BWD_PAIR). dK and dV are bit-identical either way.
+ * query block walking the key blocks). With D = 64, no causal mask and fewer
+ * key tiles (B*H*ceil(N/128)) than SMs, the dK/dV and dQ launches run on CTA
+ * pairs ("Flash Attention" notes, "FlashAttention 4": a 256-row tile split
+ * across two CTAs with tcgen05 cta_group::2): each cluster of two CTAs owns 256
+ * keys (dK/dV) or 256 queries (dQ), and one MMA covers both CTAs' rows with each
+ * CTA holding half of the other operand (fa_set_schedule, FA_SCHED_BWD_PAIR).
+ * dK and dV are bit-identical either way.
  *
  *   Q, K, V, O, dO   inputs (O from fa_fwd with the same arguments)
  *   LSE              input, [B,H,M] float32 written by fa_fwd
@@ -382,7 +383,8 @@ fa_status fa_set_wait_budget_ns(unsigned long long ns);
  *                         (fa_fwd_host_workspace_bytes depends on it)
  *   FA_SCHED_BWD_PAIR     0 / 1: fa_bwd's dK/dV and dQ kernels (D = 64) on CTA
  *                         pairs (tcgen05 cta_group::2, 256 rows per pair) off / on;
- *                         automatic: on for non-causal calls
+ *                         automatic: on for non-causal calls with fewer key
+ *                         tiles than SMs
  * Other keys or values: FA_ERR_INVALID.
  */
 typedef enum fa_sched_key {
