@@ -1382,7 +1382,8 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         using S = FusedSched<CAUSAL>;
         const uint32_t u0 = static_cast<uint32_t>(pc.w) * static_cast<uint32_t>(nqb);  // the item's units
         const uint32_t u1 = u0 + static_cast<uint32_t>(nqb);
-        uint32_t ca = static_cast<uint32_t>(static_cast<uint64_t>(u0) * gridDim.x / units);  // holder of u0
+        // holder of u0 (this branch runs only on the split schedule, where units > 0)
+        uint32_t ca = units > 0u ? static_cast<uint32_t>(static_cast<uint64_t>(u0) * gridDim.x / units) : 0u;
         while (ca + 1u < gridDim.x && S::start(ca + 1u, units) <= u0) ++ca;
         while (ca > 0u && S::start(ca, units) > u0) --ca;
         // CTA c's slot for this item: its second (last) one if its range starts before the item
