@@ -603,7 +603,7 @@ fa_status fa_fwd_fp8(const void* Q, const void* K, const void* V, void* O, float
   FA_TRY(check_ptr(K, "K"));
   FA_TRY(check_ptr(V, "V"));
   FA_TRY(check_ptr(O, "O"));
-  if (signs == nullptr) return fail(FA_ERR_INVALID, "signs is NULL");
+  FA_TRY(check_ptr(signs, "signs"));  // read 16 bytes at a time
   if (LSE != nullptr && (reinterpret_cast<uintptr_t>(LSE) & 3u)) return fail(FA_ERR_INVALID, "LSE misaligned");
   FA_TRY(check_ptr(workspace, "workspace"));
   const Fp8Layout L = fp8_layout(B, H, M, N);

@@ -32,18 +32,59 @@ __device__ __forceinline__ float block_max128(float v, float* red) {
   return v;
 }
 
+// Largest |V| of one 128-key block of one head into vmax (16-byte loads contiguous across
+// each warp).
+template <bool BF16>
+__device__ __forceinline__ void v_block_amax(const uint16_t* __restrict__ V, float* __restrict__ vmax, int N,
+                                             float* red) {
+  const int nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (static_cast<int>(blockIdx.x) >= nkb) return;  // the grid covers the longest of Q, K, V
+  const size_t bh = blockIdx.y;
+  const int k0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
+  const int nrows = min(kRowsPerBlock, N - k0);
+  const uint4* src = reinterpret_cast<const uint4*>(V + (bh * N + k0) * kD8);
+  float am = 0.f;
+  uint4 ld[kRowsPerBlock * kD8 / 8 / 128];
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const int c = static_cast<int>(threadIdx.x) + 128 * i;
+    ld[i] = c < nrows * kD8 / 8 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
+    const uint4 v = ld[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      am = fmaxf(am, fmaxf(fabsf(half_to_f32<BF16>(static_cast<uint16_t>(w[j] & 0xFFFFu))),
+                           fabsf(half_to_f32<BF16>(static_cast<uint16_t>(w[j] >> 16)))));
+  }
+  am = block_max128(am, red);
+  if (threadIdx.x == 0) vmax[bh * nkb + blockIdx.x] = am;
+}
+
 // Q (blockIdx.z = 0) or K (1): one CTA per 128-row block of one head, one row per thread.
 // x -> x diag(signs) H / 8 by a fast Walsh-Hadamard transform in registers, then the block's
 // scale = amax / 448 and the E4M3 row. The block moves through shared memory in 16-byte
-// pieces, so that its global loads and stores are contiguous across each warp.
+// pieces, so that its global loads and stores are contiguous across each warp. z = 2: V's
+// per-block maxima (same launch: all three only read the inputs).
 template <bool BF16>
 __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __restrict__ Q,
                                                            const uint16_t* __restrict__ K,
+                                                           const uint16_t* __restrict__ V,
                                                            const int8_t* __restrict__ signs, uint8_t* __restrict__ Q8,
                                                            uint8_t* __restrict__ K8, float* __restrict__ sq,
-                                                           float* __restrict__ sk, int M, int N) {
+                                                           float* __restrict__ sk, float* __restrict__ vmax, int M,
+                                                           int N) {
   __shared__ uint32_t tile[kRowsPerBlock][kD8 / 2 + 1];  // 32 words of halves a row (+1: no bank conflicts)
   __shared__ float red[4];
+  // launched as a programmatic dependent: the inputs may come from the kernel before it
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
+  if (blockIdx.z == 2) {
+    v_block_amax<BF16>(V, vmax, N, red);
+    return;
+  }
   const bool isk = blockIdx.z == 1;
   const int rows = isk ? N : M;
   const int nblk = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
@@ -78,9 +119,21 @@ __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __res
     x[2 * w] = half_to_f32<BF16>(static_cast<uint16_t>(v & 0xFFFFu));
     x[2 * w + 1] = half_to_f32<BF16>(static_cast<uint16_t>(v >> 16));
   }
+  {  // the signs as one bit each (an int8 is negative when its top bit is set)
+    const uint4* s4 = reinterpret_cast<const uint4*>(signs);
+    uint32_t sw[16];
 #pragma unroll
-  for (int d = 0; d < kD8; ++d)
-    if (__ldg(signs + d) < 0) x[d] = -x[d];
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = __ldg(s4 + i);
+      sw[4 * i] = v.x;
+      sw[4 * i + 1] = v.y;
+      sw[4 * i + 2] = v.z;
+      sw[4 * i + 3] = v.w;
+    }
+#pragma unroll
+    for (int d = 0; d < kD8; ++d)
+      x[d] = __uint_as_float(__float_as_uint(x[d]) ^ (((sw[d / 4] >> (8 * (d % 4) + 7)) & 1u) << 31));
+  }
 #pragma unroll
   for (int h = 1; h < kD8; h <<= 1) {
 #pragma unroll
@@ -117,36 +170,6 @@ __global__ void __launch_bounds__(128) fp8_qk_quant_kernel(const uint16_t* __res
   }
 }
 
-// Largest |V| of each 128-key block of each head (16-byte loads contiguous across each warp).
-template <bool BF16>
-__global__ void __launch_bounds__(128) fp8_v_amax_kernel(const uint16_t* __restrict__ V, float* __restrict__ vmax,
-                                                         int N) {
-  __shared__ float red[4];
-  const int nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
-  const size_t bh = blockIdx.y;
-  const int k0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
-  const int nrows = min(kRowsPerBlock, N - k0);
-  const uint4* src = reinterpret_cast<const uint4*>(V + (bh * N + k0) * kD8);
-  float am = 0.f;
-  uint4 ld[kRowsPerBlock * kD8 / 8 / 128];
-#pragma unroll
-  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
-    const int c = static_cast<int>(threadIdx.x) + 128 * i;
-    ld[i] = c < nrows * kD8 / 8 ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int i = 0; i < kRowsPerBlock * kD8 / 8 / 128; ++i) {
-    const uint4 v = ld[i];
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      am = fmaxf(am, fmaxf(fabsf(half_to_f32<BF16>(static_cast<uint16_t>(w[i] & 0xFFFFu))),
-                           fabsf(half_to_f32<BF16>(static_cast<uint16_t>(w[i] >> 16)))));
-  }
-  am = block_max128(am, red);
-  if (threadIdx.x == 0) vmax[bh * nkb + blockIdx.x] = am;
-}
-
 // V of one 128-key block quantised with its head's scale and written transposed:
 // Vt8[bh][d][key], rows of Npad bytes (keys past N are zero).
 template <bool BF16>
@@ -158,6 +181,9 @@ __global__ void __launch_bounds__(128) fp8_v_quant_kernel(const uint16_t* __rest
   const int nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
   const size_t bh = blockIdx.y;
   const int k0 = static_cast<int>(blockIdx.x) * kRowsPerBlock;
+  // launched as a programmatic dependent of the launch that wrote vmax
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
   float am = 0.f;
   for (int i = threadIdx.x; i < nkb; i += blockDim.x) am = fmaxf(am, vmax[bh * nkb + i]);
   am = block_max128(am, red);
@@ -207,21 +233,31 @@ __global__ void __launch_bounds__(128) fp8_v_quant_kernel(const uint16_t* __rest
 cudaError_t launch_fp8_quant(const void* Q, const void* K, const void* V, const int8_t* signs, const Fp8Ws& w, int BH,
                              int M, int N, int dtype, cudaStream_t stream) {
   const int nqb = (M + kRowsPerBlock - 1) / kRowsPerBlock, nkb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
-  const dim3 gqk(static_cast<unsigned>(nqb > nkb ? nqb : nkb), static_cast<unsigned>(BH), 2u);
-  const dim3 gv(static_cast<unsigned>(nkb), static_cast<unsigned>(BH));
   const auto* q = static_cast<const uint16_t*>(Q);
   const auto* k = static_cast<const uint16_t*>(K);
   const auto* v = static_cast<const uint16_t*>(V);
-  if (dtype == kBF16) {
-    fp8_qk_quant_kernel<true><<<gqk, 128, 0, stream>>>(q, k, signs, w.q8, w.k8, w.sq, w.sk, M, N);
-    fp8_v_amax_kernel<true><<<gv, 128, 0, stream>>>(v, w.vmax, N);
-    fp8_v_quant_kernel<true><<<gv, 128, 0, stream>>>(v, w.vmax, w.vt8, w.sv, N, w.npad);
-  } else {
-    fp8_qk_quant_kernel<false><<<gqk, 128, 0, stream>>>(q, k, signs, w.q8, w.k8, w.sq, w.sk, M, N);
-    fp8_v_amax_kernel<false><<<gv, 128, 0, stream>>>(v, w.vmax, N);
-    fp8_v_quant_kernel<false><<<gv, 128, 0, stream>>>(v, w.vmax, w.vt8, w.sv, N, w.npad);
-  }
-  return cudaGetLastError();
+  // both launches are programmatic dependents of the kernel before them on the stream
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // Q, K (blocks of 128 rows) and V's block maxima in one launch, then V
+  cfg.gridDim = dim3(static_cast<unsigned>(nqb > nkb ? nqb : nkb), static_cast<unsigned>(BH), 3u);
+  cudaError_t e = dtype == kBF16 ? cudaLaunchKernelEx(&cfg, fp8_qk_quant_kernel<true>, q, k, v, signs, w.q8, w.k8, w.sq,
+                                                      w.sk, w.vmax, M, N)
+                                 : cudaLaunchKernelEx(&cfg, fp8_qk_quant_kernel<false>, q, k, v, signs, w.q8, w.k8, w.sq,
+                                                      w.sk, w.vmax, M, N);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(static_cast<unsigned>(nkb), static_cast<unsigned>(BH));
+  return dtype == kBF16
+             ? cudaLaunchKernelEx(&cfg, fp8_v_quant_kernel<true>, v, static_cast<const float*>(w.vmax), w.vt8, w.sv, N,
+                                  w.npad)
+             : cudaLaunchKernelEx(&cfg, fp8_v_quant_kernel<false>, v, static_cast<const float*>(w.vmax), w.vt8, w.sv,
+                                  N, w.npad);
 }
 
 }  // namespace fa

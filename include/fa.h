@@ -241,8 +241,9 @@ size_t fa_bwd_ws_workspace_bytes(int B, int H, int M, int D);
  *   Q, K, V, O, LSE, B, H, M, N, scale, causal   as for fa_fwd
  *   D                  64 (other values: FA_ERR_UNSUPPORTED)
  *   dtype              FA_F16 or FA_BF16 (storage of Q, K, V, O)
- *   signs              device pointer to D signed bytes, each +1 or -1 (a
- *                      negative byte counts as -1), drawn by the caller
+ *   signs              device pointer, 16-byte aligned, to D signed bytes, each
+ *                      +1 or -1 (a negative byte counts as -1), drawn by the
+ *                      caller
  *   workspace          device pointer, 16-byte aligned, at least
  *                      fa_fwd_fp8_workspace_bytes(B,H,M,N,D) bytes: the E4M3
  *                      copies of Q M [B*H][M][64] and K M [B*H][N][64], V

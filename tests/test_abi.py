@@ -101,6 +101,11 @@ def test_invalid_arguments_rejected_before_launch(lib):
         fa.FA_ERR_UNSUPPORTED
     assert fa.fa_fwd_host(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1 << 20, 1, 1, 8, 8, 64, float("inf"), 0, fa.FA_F16,
                           0) == fa.FA_ERR_INVALID
+    # FP8 forward: the signs are read 16 bytes at a time, so a misaligned or NULL pointer is refused
+    assert fa.fa_fwd_fp8(FAKE, FAKE, FAKE, FAKE, None, FAKE + 1, FAKE, 1 << 24, 1, 1, 8, 8, 64, 0.1, 0, fa.FA_F16,
+                         0) == fa.FA_ERR_INVALID
+    assert fa.fa_fwd_fp8(FAKE, FAKE, FAKE, FAKE, None, None, FAKE, 1 << 24, 1, 1, 8, 8, 64, 0.1, 0, fa.FA_F16,
+                         0) == fa.FA_ERR_INVALID
     # decode with rows: R = 0 invalid, R = 5 unsupported
     assert fa.fa_decode_ex(FAKE, FAKE, FAKE, FAKE, None, FAKE, 1, 1, 0, 100, 128, 0.1, 4, fa.FA_BF16, 0) == \
         fa.FA_ERR_INVALID
