@@ -7,8 +7,9 @@ device memory:
   * backward at the same shape, when the library provides it;
   * flash decoding, bf16, B=8, H=32, N=32768, D=128, n_splits=64 (the K/V cache,
     4.29 GB, is far larger than L2).
-Step i runs the forward and the backward on input set i % 4 of four seeded sets
-(4 x 63 MB, larger than L2, so every call reads its inputs from HBM). The K
+Step i runs the forward and the backward on input set i % 12 of twelve seeded
+sets (the forward alone touches 12 x 25 MB, the backward 12 x 51 MB: both more
+than twice the 129 MB L2, so every call reads its inputs from HBM). The K
 calls of each part run back to back on one stream between one pair of CUDA
 events. `value` is the forward's TFLOP/s (4*B*H*M*N*D per call); the decode
 GB/s (K+V bytes read per call) is reported in the `decode` object. `configs`
@@ -43,7 +44,7 @@ METRIC = "attn fwd TFLOP/s & % tensor peak (B4 H12 N2048 D64); decode KV GB/s & 
 FWD = dict(B=4, H=12, M=2048, N=2048, D=64, scale=0.125, causal=False, dtype="f16")
 DEC = dict(B=8, H=32, N=32768, D=128, n_splits=64, dtype="bf16")
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB of L2
-ROTATE = 4  # input sets of the forward/backward workload used in turn: 4 x 63 MB > 129 MB of L2
+ROTATE = 12  # input sets of the forward/backward workload used in turn: the forward's 12 x 25 MB > 2 x L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 ROT_BYTES = 300 << 20  # rotated input copies of a configuration: more than twice L2 (129 MB)
 
@@ -519,7 +520,8 @@ def run_ours(args):
             "head_dim": FWD["D"],
             "heads": FWD["H"],
             "parallelism": f"replicas{world}",
-            "l2": "inputs larger than L2: forward and backward rotate over 4 input sets (4 x 63 MB > 129 MB), "
+            "l2": "inputs larger than L2: forward and backward rotate over 12 input sets (forward 12 x 25 MB, backward "
+                  "12 x 51 MB, both > 2 x 129 MB), "
                   "calls back to back; decode cache 4.29 GB > L2; configs and f32: calls back to back over copies of their "
                   "inputs larger than 2 x L2 (us_isolated: one call with L2 flushed)",
         },
