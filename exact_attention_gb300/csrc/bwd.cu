@@ -176,6 +176,10 @@ __global__ void __launch_bounds__(kThreadsB, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDkDv};
+  // launched as a programmatic dependent: the set-up above overlapped the previous kernel's tail;
+  // no global memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
 
   if (warp == kWarpProdB) {
     // ------------------------------------------------------------ producer (whole warp)
@@ -505,6 +509,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDkDv};
+  // launched as a programmatic dependent: the set-up above overlapped the previous kernel's tail;
+  // no global memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
 
   if (warp == kWarpProdO) {
     // ------------------------------------------------------------ producer (whole warp)
@@ -1508,6 +1516,10 @@ __global__ void __launch_bounds__(kThreadsO, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernBwdDq};
+  // launched as a programmatic dependent: the set-up above overlapped the previous kernel's tail;
+  // no global memory is touched before that kernel has completed
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ptx::grid_dep_wait();
 
   if (warp == kWarpProdO) {
     if (lane == 0) {
@@ -1737,6 +1749,23 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(const float4* __res
   }
 }
 
+// A launch as a programmatic dependent of the kernel before it on the stream (the kernel waits
+// with griddepcontrol.wait before touching global memory).
+template <class Kern, class... Args>
+cudaError_t launch_dependent(Kern kern, int grid, int threads, int smem, cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 template <int D, bool BF16, bool CAUSAL>
 cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
                          void* dQ, void* dK, void* dV, float* delta, float* dQacc, int BH, int M, int N, float scale,
@@ -1827,16 +1856,18 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       auto kern = bwd_dkdv64_kernel<BF16, CAUSAL>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, OvCfg<64>::kSmem);
       if (e != cudaSuccess) return e;
-      kern<<<grid, kThreadsO, OvCfg<64>::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta,
-                                                               static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV),
-                                                               BH, M, N, scale, ctx.status, ctx.wait_budget_ns);
+      e = launch_dependent(kern, grid, kThreadsO, OvCfg<64>::kSmem, ctx.stream, mq, mk, mv, mdo, LSE, delta,
+                           static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), BH, M, N, scale, ctx.status,
+                           ctx.wait_budget_ns);
+      if (e != cudaSuccess) return e;
     } else {
       auto kern = bwd_dkdv_kernel<D, BF16, CAUSAL>;
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
       if (e != cudaSuccess) return e;
-      kern<<<grid, kThreadsB, C::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dK),
-                                                     static_cast<uint16_t*>(dV), BH, M, N, scale, ctx.status,
-                                                     ctx.wait_budget_ns);
+      e = launch_dependent(kern, grid, kThreadsB, C::kSmem, ctx.stream, mq, mk, mv, mdo, LSE, delta,
+                           static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), BH, M, N, scale, ctx.status,
+                           ctx.wait_budget_ns);
+      if (e != cudaSuccess) return e;
     }
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1848,8 +1879,9 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
     if (e != cudaSuccess) return e;
     const long long items = static_cast<long long>(BH) * nqb;
     const int grid = static_cast<int>(items < ctx.num_sms ? items : ctx.num_sms);
-    kern<<<grid, kThreadsO, OvCfg<D>::kSmem, ctx.stream>>>(mq, mk, mv, mdo, LSE, delta, static_cast<uint16_t*>(dQ),
-                                                            BH, M, N, scale, ctx.status, ctx.wait_budget_ns);
+    e = launch_dependent(kern, grid, kThreadsO, OvCfg<D>::kSmem, ctx.stream, mq, mk, mv, mdo, LSE, delta,
+                         static_cast<uint16_t*>(dQ), BH, M, N, scale, ctx.status, ctx.wait_budget_ns);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
 }
