@@ -33,6 +33,10 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "fa_internal.cuh"
 #include "fwd_common.cuh"
 #include "ptx.cuh"
@@ -114,26 +118,33 @@ __device__ __forceinline__ void unit_pair(uint32_t uh, int nkb, int& p, int& jb)
   jb = static_cast<int>(uh - base - q * n);
 }
 
+// Share boundaries of the split schedule chosen by the host (non-causal): CTA c takes units
+// [s[c], s[c+1]). s[gridDim.x] = 0 when the host gave none.
+constexpr int kMaxSplitCtas = 256;
+struct SplitBounds {
+  uint32_t s[kMaxSplitCtas + 1];
+};
+
 // Which pieces a CTA takes. Classic: whole pairs blockIdx.x, +gridDim.x, ... (tile_info
-// order). Split: the contiguous range [c U / G, (c+1) U / G) of the U units of all heads
-// (U < 2^31, checked by the host), so every CTA does the same number of blocks and no
-// partial last wave is left; a pair cut by a range boundary is finished by the CTA that
-// holds its first block, which processes that piece last, while the CTAs holding the rest
-// process theirs first.
+// order). Split: a contiguous range of the U units of all heads (U < 2^31, checked by the
+// host), [c U / G, (c+1) U / G) or the host's boundaries `bnd` (the same number of blocks
+// each, give or take what a CTA's piece boundaries and merges cost), so no partial last wave
+// is left; a pair cut by a range boundary is finished by the CTA that holds its first block,
+// which processes that piece last, while the CTAs holding the rest process theirs first.
 template <bool CAUSAL>
 struct Schedule {
   uint32_t u, e;  // split: the remaining unit range; classic: u = next round, e = pair count
-  __device__ static uint32_t start(uint32_t c, uint32_t units) {
-    return static_cast<uint32_t>(static_cast<uint64_t>(c) * units / gridDim.x);
+  __device__ static uint32_t start(const uint32_t* bnd, uint32_t c, uint32_t units) {
+    return bnd != nullptr ? bnd[c] : static_cast<uint32_t>(static_cast<uint64_t>(c) * units / gridDim.x);
   }
   __device__ static uint32_t total_units(int BH, int num_pairs, int nkb) {
     return static_cast<uint32_t>(BH) * units_before<CAUSAL>(num_pairs, nkb);
   }
-  __device__ Schedule(bool split, int BH, int num_pairs, int nkb) {
+  __device__ Schedule(bool split, int BH, int num_pairs, int nkb, const uint32_t* bnd) {
     if (split) {
       const uint32_t units = total_units(BH, num_pairs, nkb);
-      u = start(blockIdx.x, units);
-      e = start(blockIdx.x + 1, units);
+      u = start(bnd, blockIdx.x, units);
+      e = start(bnd, blockIdx.x + 1, units);
     } else {
       u = 0;
       e = static_cast<uint32_t>(BH * num_pairs);
@@ -198,7 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fwd_d64_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO, float* __restrict__ LSE, int BH,
                    int M, int N, float scale_log2_signed, float* __restrict__ ws, uint32_t* __restrict__ flags, uint32_t epoch,
-                   DevStatus* status, unsigned long long budget_ns, int inject) {
+                   DevStatus* status, unsigned long long budget_ns, int inject,
+                   const __grid_constant__ SplitBounds bounds) {
   extern __shared__ uint8_t smem_raw[];
   Hdr* hdr = reinterpret_cast<Hdr*>(smem_raw);
   const uint32_t raw_u32 = ptx::smem_u32(smem_raw);
@@ -212,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM);
   const int nkb = (N + kBN - 1) / kBN;
   const bool split = ws != nullptr;
+  const uint32_t* bnd = split && bounds.s[gridDim.x] != 0u ? bounds.s : nullptr;
   // scale < 0: the score product is negated in the tensor core and the softmax scales by |scale|.
   // |scale| is kept above 1e-30 so that a masked score (-inf) times it stays -inf when scale = 0
   // (every visible weight is then exp2 of about 0, i.e. 1).
@@ -254,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // launch's set-up runs on the SMs the previous kernel has left, during that kernel's tail.
     // (A prefetch only warms L2, where the previous kernel's writes land too.) At B4 H12 N2048
     // (40 units a CTA) 63.2 -> 62.0 us back to back.
-    Schedule<CAUSAL> first(split, BH, num_pairs, nkb);
+    Schedule<CAUSAL> first(split, BH, num_pairs, nkb, bnd);
     Piece p0;
     if ((!split || first.e - first.u <= 128u) && first.next(p0, split, BH, num_pairs, nkb)) {
       for (int t = 0; t < 2; ++t) ptx::tma_prefetch_l2_3d(&tmQ, 0, p0.q0 + t * kBM, p0.bh);
@@ -283,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool skip_first = inject == kInjectFwdStage && blockIdx.x == 0;
       int it = 0;
       bool ok = true;
-      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb, bnd);
       Piece ti;
       for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
         const int qb = it % kQBuf;
@@ -336,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t dS = tmem + kColS + t * kBN;
       const uint32_t dO = tmem + kColO + t * kD;
       const uint32_t aP = tmem + kColP + t * (kBN / 2);
-      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb, bnd);
       Piece ti;
       for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
         const int qb = it % kQBuf;
@@ -411,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // warps wrote; then, both tiles done, the Q buffer's release. None of this waits on the
     // softmax warps' critical path.
     if (lane == 0) {
-      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+      Schedule<CAUSAL> sch(split, BH, num_pairs, nkb, bnd);
       Piece ti;
       for (int it = 0; sch.next(ti, split, BH, num_pairs, nkb); ++it) {
         const int qb = it % kQBuf;
@@ -457,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t nblk = 0u;  // blocks processed by this tile slot (all pairs)
     uint32_t o_ph = 0u;
     bool ok = true;
-    Schedule<CAUSAL> sch(split, BH, num_pairs, nkb);
+    Schedule<CAUSAL> sch(split, BH, num_pairs, nkb, bnd);
     Piece ti;
     int it = 0;          // pieces taken (Q buffer = it % kQBuf)
     for (; ok && sch.next(ti, split, BH, num_pairs, nkb); ++it) {
@@ -615,9 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t units = Schedule<CAUSAL>::total_units(BH, num_pairs, nkb);
         const uint32_t end_u = static_cast<uint32_t>(ti.bh) * units_before<CAUSAL>(num_pairs, nkb) +
                                units_before<CAUSAL>(ti.q0 / (2 * kBM) + 1, nkb);  // the pair's last unit + 1
-        for (uint32_t c2 = blockIdx.x + 1; c2 < gridDim.x && Schedule<CAUSAL>::start(c2, units) < end_u && ok; ++c2) {
-          // a CTA with an empty range (more CTAs than units) writes no partial
-          if (Schedule<CAUSAL>::start(c2 + 1, units) == Schedule<CAUSAL>::start(c2, units)) continue;
+        for (uint32_t c2 = blockIdx.x + 1; c2 < gridDim.x && Schedule<CAUSAL>::start(bnd, c2, units) < end_u && ok;
+             ++c2) {
+          // a CTA with an empty range writes no partial
+          if (Schedule<CAUSAL>::start(bnd, c2 + 1, units) == Schedule<CAUSAL>::start(bnd, c2, units)) continue;
           uint32_t* f = flags + static_cast<size_t>(c2) * 8 + warp;
           bool got = true;
           if (lane == 0) {
@@ -684,6 +698,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Share boundaries of the non-causal split schedule over G CTAs: contiguous ranges of the U
+// (pair, key block) units, each pair nkb units, balanced by an estimated cost instead of the
+// unit count. A range's cost, in tenths of a block: 10 per unit, 12 per further pair it
+// touches (a piece boundary), 16 when it ends inside a pair whose first block it holds (it
+// merges that pair's partials last), 4 when it starts inside a pair (it writes a partial).
+// Weights from a per-CTA timeline at B4 H12 N2048: a block 1.3 us, a piece boundary 1.5 us, a
+// merge 2 us, a partial's write about 0.5 us. The smallest target cost that a greedy fill
+// (each range as long as it stays within the target) stretches over all U units.
+void balance_split(uint32_t U, uint32_t nkb, int G, uint32_t* out) {
+  auto cost = [&](uint32_t s, uint32_t e) -> uint64_t {  // range [s, e), e > s
+    const uint32_t p0 = s / nkb, p1 = (e - 1u) / nkb;
+    uint64_t c = 10ull * (e - s) + 12ull * (p1 - p0);
+    if (e % nkb != 0u && s <= p1 * nkb) c += 16u;
+    if (s % nkb != 0u) c += 4u;
+    return c;
+  };
+  auto fill = [&](uint64_t target, uint32_t* b) {
+    uint32_t s = 0;
+    b[0] = 0;
+    for (int c = 0; c < G; ++c) {
+      uint32_t best = s;
+      const uint64_t reach = target / 10u + 2u * nkb + 2u;  // no range is longer than this
+      for (uint64_t e = s + 1ull; e <= U && e <= s + reach; ++e)
+        if (cost(s, static_cast<uint32_t>(e)) <= target) best = static_cast<uint32_t>(e);
+      b[c + 1] = best;
+      s = best;
+    }
+    return s >= U;
+  };
+  uint64_t lo = 10ull * U / static_cast<uint64_t>(G), hi = 2ull * lo + 64ull;
+  while (!fill(hi, out)) hi *= 2;
+  while (lo < hi) {
+    const uint64_t mid = (lo + hi) / 2;
+    if (fill(mid, out)) hi = mid;
+    else lo = mid + 1;
+  }
+  fill(hi, out);
+  out[G] = U;
+}
+
 template <bool BF16, bool CAUSAL>
 cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo, float* LSE,
                      int BH, int M, int N, float scale, const FwdSplit& sp, const LaunchCtx& ctx) {
@@ -696,6 +750,23 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   // (A cooperative launch, which would guarantee the split schedule's CTAs are resident at once,
   // measured to serialise with the previous kernel, 65.5 against 62.9 us back to back at
   // B4 H12 N2048; the split schedule's one CTA per SM becomes resident as the SMs free up.)
+  SplitBounds bounds{};  // all zero: the kernel divides the units evenly
+  if (sp.ws != nullptr && !CAUSAL && ctx.num_sms <= kMaxSplitCtas) {
+    // computed once per shape (about a millisecond), then reused
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int, int>, SplitBounds> cache;
+    const int num_pairs = (M + 2 * kBM - 1) / (2 * kBM), nkb = (N + kBN - 1) / kBN;
+    const auto key = std::make_tuple(BH, num_pairs, nkb, ctx.num_sms);
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+      SplitBounds b{};
+      balance_split(static_cast<uint32_t>(BH) * static_cast<uint32_t>(num_pairs) * static_cast<uint32_t>(nkb),
+                    static_cast<uint32_t>(nkb), ctx.num_sms, b.s);
+      it = cache.emplace(key, b).first;
+    }
+    bounds = it->second;
+  }
   if (sp.ws != nullptr) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(ctx.num_sms);
@@ -708,7 +779,7 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, BH, M, N, scale * kLog2e, sp.ws, sp.flags, sp.epoch,
-                              ctx.status, ctx.wait_budget_ns, ctx.inject);
+                              ctx.status, ctx.wait_budget_ns, ctx.inject, bounds);
   }
   const int grid = static_cast<int>(tiles < ctx.num_sms ? tiles : ctx.num_sms);
   cudaLaunchConfig_t cfg{};
@@ -722,7 +793,8 @@ cudaError_t launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mo, LSE, BH, M, N, scale * kLog2e, static_cast<float*>(nullptr),
-                            static_cast<uint32_t*>(nullptr), 0u, ctx.status, ctx.wait_budget_ns, ctx.inject);
+                            static_cast<uint32_t*>(nullptr), 0u, ctx.status, ctx.wait_budget_ns, ctx.inject,
+                            bounds);
 }
 
 }  // namespace
