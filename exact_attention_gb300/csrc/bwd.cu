@@ -1181,7 +1181,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             ptx::tma_reduce_add_3d(&tmQacc, sStg, 0, i * kT, itm.bh);
             ptx::tma_reduce_add_3d(&tmQacc, sStg + kT * 128, 32, i * kT, itm.bh);
           });
-        if (ok && pc.kind == 0)
+        if (ok && pc.kind != 2)  // whole items and the first blocks of cut ones store dV / dK
           ok = drain([&] {
             ptx::tma_store_3d(&tmdV, sStg, 0, itm.r0, itm.bh);
             ptx::tma_store_3d(&tmdK, sStg + kChunkB, 0, itm.r0, itm.bh);
@@ -1382,11 +1382,11 @@ __global__ void __launch_bounds__(kThreadsF, 1)
       }
       ptx::tc_fence_before();
       if (pc.kind != 0) {
-        // A piece of a split item. Every CTA holding one adds it up the same way: it writes its
-        // raw sums into its slot for that piece and counts itself in on the item's counter (one
-        // per compute warp, kept by the CTA holding the item's first block); the warp that
-        // counts in last adds the others' slots to its own sums and writes that part of dV and
-        // dK. No CTA waits for another.
+        // A piece of a split item. The CTAs holding its later blocks took those pieces first:
+        // each writes its raw sums into its slot and counts itself in on the item's counter (one
+        // per compute warp, kept for the CTA holding the item's first block). That CTA took its
+        // piece last: it waits (bounded) until every other holder has counted in, adds their
+        // slots to its own sums and stores dV and dK as a whole item does.
         using S = FusedSched<CAUSAL>;
         const uint32_t u0 = static_cast<uint32_t>(pc.w) * static_cast<uint32_t>(nqb);  // the item's units
         const uint32_t u1 = u0 + static_cast<uint32_t>(nqb);
@@ -1400,46 +1400,47 @@ __global__ void __launch_bounds__(kThreadsF, 1)
         auto slot_at = [&](uint32_t sl, int part, int k) {
           return part_ws + static_cast<size_t>(sl) * kFusedSlotFloats + (part * 64 + d0 + k) * kT + rr;
         };
-        uint32_t holders = 0;
-        for (uint32_t c = ca; c < gridDim.x && S::start(c, units) < u1; ++c)
-          if (S::start(c + 1u, units) > S::start(c, units)) ++holders;
-        const uint32_t mine = slot_of(blockIdx.x);
+        uint32_t* cnt = counters + static_cast<size_t>(ca) * kCwF + warp;
+        if (pc.kind == 2) {
+          const uint32_t mine = slot_of(blockIdx.x);
 #pragma unroll
-        for (int part = 0; part < 2; ++part)
+          for (int part = 0; part < 2; ++part)
 #pragma unroll
-          for (int k = 0; k < kDcF; ++k) __stcg(slot_at(mine, part, k), g2[part][k]);
-        __threadfence();  // every lane's slot writes, at gpu scope, before the count
-        __syncwarp();
-        uint32_t before = 0;
-        if (lane == 0) before = atomicAdd(counters + static_cast<size_t>(ca) * kCwF + warp, 1u);
-        __syncwarp();  // the other lanes' reads below follow lane 0's count
-        before = __shfl_sync(0xFFFFFFFFu, before, 0);
-        if (before + 1u < holders) continue;  // a later holder finishes this part of the item
-        __threadfence();  // the other holders' slot writes, counted in before this warp, are visible
-        for (uint32_t c = ca; c < gridDim.x && S::start(c, units) < u1; ++c) {
-          if (c == blockIdx.x || S::start(c + 1u, units) == S::start(c, units)) continue;
+            for (int k = 0; k < kDcF; ++k) __stcg(slot_at(mine, part, k), g2[part][k]);
+          __threadfence();  // every lane's slot writes, at gpu scope, before the count
+          __syncwarp();
+          if (lane == 0) atomicAdd(cnt, 1u);
+          continue;
+        }
+        // the item's first blocks: the other holders' counts, then their slots
+        uint32_t others = 0;
+        for (uint32_t c = ca + 1u; c < gridDim.x && S::start(c, units) < u1; ++c)
+          if (S::start(c + 1u, units) > S::start(c, units)) ++others;
+        bool got = true;
+        if (lane == 0) {
+          const uint64_t t0 = ptx::globaltimer_ns();
+          got = false;
+          for (uint32_t k = 0; k < (1u << 30); ++k) {
+            if (ptx::ld_acquire_u32(cnt) >= others) {
+              got = true;
+              break;
+            }
+            if ((k & 255u) == 255u && (*wc.abort_flag || ptx::globaltimer_ns() - t0 > wc.budget_ns)) break;
+          }
+          if (!got) ptx::raise_error(wc, kStatusTimeout, 39);
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, got, 0);
+        if (!ok) break;
+        __syncwarp();     // lane 0's acquire, then this barrier, order every lane's slot reads after the writes
+        __threadfence();
+        for (uint32_t c = ca + 1u; c < gridDim.x && S::start(c, units) < u1; ++c) {
+          if (S::start(c + 1u, units) == S::start(c, units)) continue;
           const uint32_t sl = slot_of(c);
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int k = 0; k < kDcF; ++k) g2[part][k] += __ldcg(slot_at(sl, part, k));
         }
-        // this thread's row of dV and scale * dK, columns [d0, d0 + kDcF)
-        const int key_row = itm.r0 + rr;
-        if (key_row < N) {
-          const size_t g = (static_cast<size_t>(itm.bh) * N + key_row) * D + d0;
-#pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const float f = part == 0 ? 1.f : scale;
-            uint32_t h[kDcF / 2];
-#pragma unroll
-            for (int k = 0; k < kDcF / 2; ++k) h[k] = pack2<BF16>(g2[part][2 * k] * f, g2[part][2 * k + 1] * f);
-            uint4* d4 = reinterpret_cast<uint4*>((part == 0 ? dV : dK) + g);
-#pragma unroll
-            for (int v = 0; v < kDcF / 8; ++v) d4[v] = make_uint4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
-          }
-        }
-        continue;
       }
       // dV and scale * dK in the I/O type, as the two 128 x 64 output tiles (128-byte swizzled
       // rows, the tensor maps' layout; rows past N are clipped by the maps), stored by TMA
@@ -1817,8 +1818,10 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       if (e != cudaSuccess) return e;
       // The later kernels are launched as programmatic dependents: each starts its set-up while
       // the kernel before it drains and waits (griddepcontrol.wait) before touching that
-      // kernel's results. No CTA waits for another (the split schedule's partials are added by
-      // whichever holder of a cut key tile finishes last), so none has to be resident at once.
+      // kernel's results. On the split schedule the CTA holding a cut key tile's first blocks
+      // waits (bounded) for the partials of the CTAs holding the rest, which take those pieces
+      // first; the launch has one CTA per SM, resident as the SMs free up (as the forward's
+      // split schedule relies on).
       cudaLaunchAttribute pdl[1];
       pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       pdl[0].val.programmaticStreamSerializationAllowed = 1;
