@@ -103,7 +103,8 @@ def load_peaks():
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    """nvidia-smi samples (50 ms) of SM clock and throttle reasons while running, each stamped with
+    the host clock so that they can be binned by phase."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -117,7 +118,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -128,7 +129,7 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
 
     def __exit__(self, *a):
         time.sleep(0.3)
@@ -139,15 +140,17 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, phases=None):
+        """Median and minimum SM clock, the throttle reasons seen, and with `phases` (name -> host
+        perf_counter window) the median and minimum of the samples that fall in each window."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for t, ln in self.lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
+                sm.append((t, float(f[1])))
                 mx = float(f[2])
             except ValueError:
                 continue
@@ -156,7 +159,16 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        mhz = [c for _, c in sm]
+        out = {"sm_mhz": statistics.median(mhz), "sm_min_mhz": min(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+               "samples": len(mhz)}
+        if phases:
+            by = {}
+            for name, (a, b) in phases.items():
+                w = [c for t, c in sm if a <= t <= b]
+                by[name] = {"median": statistics.median(w), "min": min(w), "samples": len(w)} if w else None
+            out["phases"] = by
+        return out
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -367,6 +379,9 @@ def run_ours(args):
     t_bwd = e[2].elapsed_time(e[3]) / 1e3
     t_dec = e[4].elapsed_time(e[5]) / 1e3
     t_step = e[0].elapsed_time(e[5]) / 1e3
+    # the device starts the first forward as soon as it is queued: the phases' windows on the host clock
+    clock_phases = {"fwd": (t0, t0 + t_fwd), "bwd": (t0 + t_fwd, t0 + t_fwd + t_bwd),
+                    "decode": (t0 + t_fwd + t_bwd, t0 + t_step)}
     t_fwd = max_over_ranks(t_fwd, world)
     t_bwd = max_over_ranks(t_bwd, world)
     t_dec = max_over_ranks(t_dec, world)
@@ -568,7 +583,7 @@ def run_ours(args):
         "e2e": {"value": round(e2e_tflops, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": launches_per_step * K,
-        "clocks": clk.summary(),
+        "clocks": clk.summary(clock_phases),
         "wall_s": round(wall, 3),
     }
     if not args.no_cpu_baseline and world == 1:

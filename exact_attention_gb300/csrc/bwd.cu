@@ -899,7 +899,7 @@ __global__ void __launch_bounds__(kThreadsF, 1)
                        const __grid_constant__ CUtensorMap tmQacc, int BH, int M, int N,
                        float scale, float* __restrict__ part_ws, uint32_t* __restrict__ counters,
                        uint16_t* __restrict__ dK, uint16_t* __restrict__ dV,
-                       DevStatus* status, unsigned long long budget_ns) {
+                       DevStatus* status, unsigned long long budget_ns, int inject) {
   constexpr int D = 64;
   using C = FusedCfg;
   constexpr uint32_t cS = 0, cdP = 128, cP = 256, cdQ = 320, cdV = 384, cdK = 448;
@@ -1409,7 +1409,13 @@ __global__ void __launch_bounds__(kThreadsF, 1)
             for (int k = 0; k < kDcF; ++k) __stcg(slot_at(mine, part, k), g2[part][k]);
           __threadfence();  // every lane's slot writes, at gpu scope, before the count
           __syncwarp();
-          if (lane == 0) atomicAdd(cnt, 1u);
+          bool count = true;
+          if (inject == kInjectBwdCount) {  // test-only: the lowest CTA starting inside an item never counts in
+            uint32_t c = 1u;
+            while (c < gridDim.x && S::start(c, units) % static_cast<uint32_t>(nqb) == 0u) ++c;
+            count = blockIdx.x != c;
+          }
+          if (lane == 0 && count) atomicAdd(cnt, 1u);
           continue;
         }
         // the item's first blocks: the other holders' counts, then their slots
@@ -1835,7 +1841,7 @@ cudaError_t launch_bwd_t(const void* Q, const void* K, const void* V, const void
       e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, mdo, LSE, static_cast<const float*>(delta), mdk, mdv, macc, BH,
                              M, N, scale, split ? sp.ws : static_cast<float*>(nullptr), counters,
                              static_cast<uint16_t*>(dK), static_cast<uint16_t*>(dV), ctx.status,
-                             ctx.wait_budget_ns);
+                             ctx.wait_budget_ns, ctx.inject);
       if (e != cudaSuccess) return e;
       const long long n4 = static_cast<long long>(n / 4);
       long long blocks = (n4 + 255) / 256;

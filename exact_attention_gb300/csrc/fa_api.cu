@@ -390,7 +390,10 @@ fa_status bwd_impl(const void* Q, const void* K, const void* V, const void* O, c
   LaunchCtx ctx{};
   FA_TRY(make_ctx(&ctx, stream));
   BwdSplit sp{};
-  if (dQacc != nullptr && split_ws != nullptr && use_bwd_split(B * H, M, N, D, causal, ctx.num_sms)) sp.ws = split_ws;
+  if (dQacc != nullptr && split_ws != nullptr && use_bwd_split(B * H, M, N, D, causal, ctx.num_sms)) {
+    sp.ws = split_ws;
+    ctx.inject = take_inject(kInjectBwdCount, 0);
+  }
   // fa_bwd's dK/dV and dQ kernels at D = 64 on CTA pairs: by default only for non-causal calls
   // with fewer key tiles than SMs, where they measured 4-7 % faster (Z1 H2 N1024: 30.7 against
   // 32.8 us). With a wave or more of key tiles the single-CTA kernels are 2-3 % faster (B4 H12
@@ -464,7 +467,7 @@ fa_status fa_set_schedule(fa_sched_key key, int value) {
 }
 
 fa_status fa_debug_inject(int kind) {
-  if (kind < 0 || kind > kInjectFwdFlag) return fail(FA_ERR_INVALID, "unknown fault-injection kind %d", kind);
+  if (kind < 0 || kind > kInjectBwdCount) return fail(FA_ERR_INVALID, "unknown fault-injection kind %d", kind);
   g_inject.store(kind);
   return FA_OK;
 }

@@ -41,6 +41,8 @@ inline size_t dtype_size(int dt) { return dt == kF32 ? 4u : 2u; }
 constexpr int kInjectDecodeStage = 1;  // decode: CTA 0 never loads its first stage of keys
 constexpr int kInjectFwdStage = 2;     // D = 64 forward: CTA 0 never loads its first K/V stage
 constexpr int kInjectFwdFlag = 3;      // D = 64 forward, split schedule: CTA 1 never publishes its partial
+constexpr int kInjectBwdCount = 4;     // fused backward, split schedule: the first CTA holding a later
+                                       // piece of a cut key tile never counts its partial in
 
 // Per-launch context every kernel receives.
 struct LaunchCtx {

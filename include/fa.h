@@ -410,6 +410,10 @@ fa_status fa_set_schedule(fa_sched_key key, int value);
  *   3  next fp16/bf16 D = 64 forward on the split schedule: CTA 1 never
  *      publishes the partial of its first piece, so the CTA that merges it
  *      gives up its wait on CTA 1's flags (a wait between CTAs)
+ *   4  next fa_bwd_ws call on the fused pass's split schedule: the lowest CTA
+ *      whose share starts inside a key tile never counts its partial in, so
+ *      the CTA holding that tile's first query blocks gives up its wait for
+ *      the count (a wait between CTAs)
  */
 fa_status fa_debug_inject(int kind);
 

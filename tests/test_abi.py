@@ -90,6 +90,7 @@ def test_invalid_arguments_rejected_before_launch(lib):
     args[5] = None
     assert fa.fa_bwd(*args, 1, 1, 8, 8, 64, 0.1, 0, fa.FA_F16, 0) == fa.FA_ERR_INVALID
     assert fa.fa_set_wait_budget_ns(10) == fa.FA_ERR_INVALID
+    assert fa.fa_debug_inject(5) == fa.FA_ERR_INVALID
     assert fa.fa_debug_inject(7) == fa.FA_ERR_INVALID
     assert fa.fa_debug_inject(0) == fa.FA_OK  # cancels nothing pending; host-only
     # host-buffer forward: NULL host buffers, a head dimension it cannot run, bad scale

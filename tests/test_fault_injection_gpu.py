@@ -15,7 +15,7 @@ import oracle
 import exact_attention_gb300 as fa
 from exact_attention_gb300 import synth
 
-from helpers import TOL_O, assert_close, f64, to_device, to_f64
+from helpers import TOL_GRAD, TOL_O, assert_close, f64, to_device, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -88,3 +88,47 @@ def test_forward_split_flag_wait_times_out_and_context_survives():
     assert status == fa.FA_ERR_TIMEOUT, (status, msg)
     assert "kernel fwd " in msg and "block 0" in msg, msg
     assert "wait site 36 " in msg or "wait site 37 " in msg, msg
+
+
+def test_backward_split_count_wait_times_out_and_context_survives():
+    """A wait between CTAs in the fused backward: on its split schedule the lowest CTA whose share
+    starts inside a key tile never counts its partial in, so the CTA holding that key tile's first
+    query blocks gives up: its compute warps' wait for the count (wait site 39) or its drain warp's
+    wait for the dV/dK tiles those warps never stage (site 38), which began earlier and so usually
+    runs out first. The next call, whose delta kernel zeroes the counters again, must match the
+    oracle."""
+    import torch
+
+    B, H, M, N = 2, 3, 1024, 1024
+    q, k, v, do = synth.attention_inputs(B, H, M, N, 64, "f16", seed=39, with_dout=True)
+    qd, kd, vd, dod = (to_device(x, "f16") for x in (q, k, v, do))
+    o, lse = fa.forward(qd, kd, vd, 0.125, False)
+    # the CTA expected to report: the holder of the first blocks of the key tile that CTA c cuts
+    G = torch.cuda.get_device_properties(0).multi_processor_count
+    nqb = M // 128
+    units = B * H * (N // 128) * nqb
+    c = next(c for c in range(1, G) if (c * units // G) % nqb != 0)
+    assert fa.fa_set_wait_budget_ns(20_000_000) == fa.FA_OK
+    try:
+        with fa.schedule(fa.FA_SCHED_BWD_SPLIT, 1):
+            assert fa.fa_debug_inject(4) == fa.FA_OK
+            fa.backward(qd, kd, vd, o, dod, lse, 0.125, False, fused=True)
+            status = fa.fa_last_status()
+            msg = fa.fa_last_error_message()
+            assert fa.fa_last_status() == fa.FA_OK
+            fa.fa_debug_inject(0)
+            fa.fa_set_wait_budget_ns(DEFAULT_BUDGET_NS)
+            dq, dk, dv, _ = fa.backward(qd, kd, vd, o, dod, lse, 0.125, False, fused=True)
+            assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    finally:
+        fa.fa_debug_inject(0)
+        fa.fa_set_wait_budget_ns(DEFAULT_BUDGET_NS)
+    assert status == fa.FA_ERR_TIMEOUT, (status, msg)
+    assert "kernel bwd_dkdv " in msg and f"block {c - 1}" in msg, msg
+    assert "wait site 39 " in msg or "wait site 38 " in msg, msg
+    grads = (to_f64(dq), to_f64(dk), to_f64(dv))
+    for b, h in ((0, 0), (B - 1, H - 1)):
+        ref = oracle.backward(f64(q[b, h], "f16"), f64(k[b, h], "f16"), f64(v[b, h], "f16"), f64(do[b, h], "f16"),
+                              0.125, False)
+        for n, (g, r) in enumerate(zip(grads, ref)):
+            assert_close(g[b, h], r, TOL_GRAD["f16"], f"{'dQ dK dV'.split()[n]}[{b},{h}] after the injected timeout")
