@@ -124,7 +124,12 @@ class ClockSampler:
             self.t.start()
         except Exception:
             self.proc = None
-        time.sleep(0.3)
+        # the timed region starts once nvidia-smi is up and sampling (its start-up, slower on a
+        # machine where it has not run yet, then stays out of the region), after 5 s at most
+        t_end = time.perf_counter() + 5.0
+        while self.proc is not None and len(self.lines) < 2 and time.perf_counter() < t_end:
+            time.sleep(0.02)
+        time.sleep(0.1)
         return self
 
     def _read(self):
