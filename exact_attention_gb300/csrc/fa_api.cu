@@ -10,7 +10,9 @@
 #include <cstdlib>
 #include <cstring>
 #include <atomic>
+#include <algorithm>
 #include <chrono>
+#include <cmath>
 #include <mutex>
 #include <vector>
 
@@ -227,18 +229,30 @@ long long split_units(int BH, int M, int N, int causal) {
   return static_cast<long long>(BH) * per_head;
 }
 
+// Whether the D = 64 forward takes the split schedule (fa_fwd_ws). Estimated times in key blocks
+// per SM: whole pairs take rounds * nkb; the split takes its share, units / num_sms, plus about
+// 3.5 blocks for its piece boundaries and merge, plus 1.2 for each further partial the holder of
+// a pair's first blocks merges (a pair spans about nkb / share shares). Fitted to back-to-back
+// times at fourteen non-causal shapes from B1 H2 N1024 to B16 H16 N4096 (a block is about
+// 1.27 us): the split wins when pairs have many key blocks and either fill fewer SMs than there
+// are or leave the last round part-empty (B1 H1 N8192 31.6 against 80.5 us, B1 H4 N2048 18.8
+// against 24.3, B4 H12 N2048 60.5 against 65.1); whole pairs win with few key blocks a pair
+// (B2 H12 N1024 15.4 against 18.1 us, B4 H12 N512 even). Within 3 % the call keeps whole pairs,
+// whose schedule has no waits between CTAs.
 bool use_split(int BH, int M, int N, int causal, int num_sms) {
   const long long pairs = static_cast<long long>(BH) * ((M + 255) / 256);
   const long long units = split_units(BH, M, N, causal);
   if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
   const int forced = g_sched_fwd_split.load();
   if (forced >= 0) return forced == 1;
-  if (units < 4ll * num_sms) return false;
   // causal: whole pairs dealt in a serpentine order (heaviest with lightest) measured faster
   // than the split, whose extra pieces cost more than the balance gains
   if (causal) return false;
-  const long long rounds = (pairs + num_sms - 1) / num_sms;
-  return pairs * 10 < rounds * num_sms * 9;
+  const double nkb = static_cast<double>((N + 127) / 128);
+  const double rounds = static_cast<double>((pairs + num_sms - 1) / num_sms);
+  const double share = static_cast<double>(units) / num_sms;
+  const double partials = std::max(0.0, std::ceil(nkb / share) - 1.0);
+  return share + 3.5 + 1.2 * partials < 0.97 * rounds * nkb;
 }
 
 // Whether the fused backward (fa_bwd_ws, D = 64) runs its split schedule: non-causal calls
@@ -657,18 +671,28 @@ fa_status fa_last_status(void* stream) {
 // ---------------------------------------------------------------------------
 // Forward on host buffers, with the copies overlapped with the kernels.
 //
-// The (batch, head) heads are cut into kHostDefaultChunks chunks (fa_set_schedule with
-// FA_SCHED_HOST_CHUNKS fixes another count, 1..8). Three internal
-// streams of the device carry the copies in, the kernels and the copies out, so
-// chunk c's inputs travel while chunk c-1 is computed and chunk c-2's output
-// travels back; events order each chunk's three steps, and the caller's stream
-// is joined at entry and at exit, so the call is ordered on it like any other.
+// The (batch, head) heads are cut into chunks: by default three, of about 4/7, 2/7 and 1/7 of
+// the heads (fa_set_schedule with FA_SCHED_HOST_CHUNKS fixes a count of equal chunks instead,
+// 1..8). Three internal streams of the device carry the copies in, the kernels and the copies
+// out, so chunk c's inputs travel while chunk c-1 is computed and earlier chunks' outputs travel
+// back; events order each chunk's three steps, and the caller's stream is joined at entry and at
+// exit, so the call is ordered on it like any other.
 
 namespace {
 
-constexpr int kHostDefaultChunks = 4;  // measured best at B4 H12 N2048 D64: the copies in and out share
-                                       // the host link (about 220-260 GB/s together), and a chunk's
-                                       // kernel has a fixed cost of about 15 us, so more chunks lose
+// The copies in and out share the host link (about 245 GB/s together, 200 one way), and a
+// chunk's outputs can only leave after its kernel: the time after the last input lands is that
+// chunk's kernel and its copy out, so the last chunk is the smallest. At B4 H12 N2048 D64 (a
+// per-chunk event timeline) chunks of 28, 14 and 6 heads took 281-285 us a call against 298-307
+// for three equal chunks and 306-315 for four; more chunks add per-copy and per-launch costs.
+constexpr int kHostDefaultChunks = 3;
+
+// First head of chunk c of n over BH heads (c = n gives BH).
+long long host_chunk_start(long long BH, int n, int c, bool equal) {
+  if (equal || n != kHostDefaultChunks) return static_cast<long long>(c) * BH / n;
+  static const int kSevenths[kHostDefaultChunks + 1] = {0, 4, 6, 7};  // 4:2:1
+  return (BH * kSevenths[c] + 3) / 7;
+}
 
 struct HostPipe {
   bool ready = false;
@@ -710,6 +734,7 @@ fa_status host_pipe(HostPipe** out) {
 // Q, K, V, O and LSE of the whole problem, each 256-byte aligned.
 struct HostLayout {
   int chunks = 0;
+  bool equal = true;  // equal chunks, or the default 4:2:1 cut
   size_t split = 0, q = 0, k = 0, v = 0, o = 0, lse = 0, total = 0;
 };
 
@@ -719,13 +744,17 @@ HostLayout host_layout(int B, int H, int M, int N, int D, int causal, fa_dtype d
   const int forced = g_sched_host_chunks.load();
   const int want = forced >= 1 ? forced : kHostDefaultChunks;
   L.chunks = static_cast<int>(BH < want ? BH : want);
-  const int hi = static_cast<int>((BH + L.chunks - 1) / L.chunks), lo = static_cast<int>(BH / L.chunks);
-  const size_t w1 = fa_fwd_workspace_bytes(1, hi, M, N, D, causal, dtype);
-  const size_t w2 = lo > 0 ? fa_fwd_workspace_bytes(1, lo, M, N, D, causal, dtype) : 0;
+  L.equal = forced >= 1 || BH < 7;  // the 4:2:1 cut needs a head in its smallest chunk
+  size_t w = 0;  // the forward's own workspace, for the largest chunk
+  for (int c = 0; c < L.chunks; ++c) {
+    const long long nh = host_chunk_start(BH, L.chunks, c + 1, L.equal) - host_chunk_start(BH, L.chunks, c, L.equal);
+    const size_t wc = nh > 0 ? fa_fwd_workspace_bytes(1, static_cast<int>(nh), M, N, D, causal, dtype) : 0;
+    w = wc > w ? wc : w;
+  }
   const size_t es = dtype == FA_F32 ? 4 : 2;
   const size_t qb = static_cast<size_t>(BH) * M * D * es, kb = static_cast<size_t>(BH) * N * D * es;
   L.split = 0;
-  L.q = align256(w1 > w2 ? w1 : w2);
+  L.q = align256(w);
   L.k = L.q + align256(qb);
   L.v = L.k + align256(kb);
   L.o = L.v + align256(kb);
@@ -774,8 +803,8 @@ fa_status fa_fwd_host(const void* hQ, const void* hK, const void* hV, void* hO, 
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->start, 0);
   if (e != cudaSuccess) return cuda_fail(e, "fa_fwd_host: joining the caller's stream");
   for (int c = 0; c < L.chunks; ++c) {
-    const int h0 = static_cast<int>(static_cast<long long>(c) * BH / L.chunks);
-    const int h1 = static_cast<int>(static_cast<long long>(c + 1) * BH / L.chunks);
+    const int h0 = static_cast<int>(host_chunk_start(BH, L.chunks, c, L.equal));
+    const int h1 = static_cast<int>(host_chunk_start(BH, L.chunks, c + 1, L.equal));
     const int nh = h1 - h0;
     char* dq = ws + L.q + h0 * qrow;
     char* dk = ws + L.k + h0 * krow;

@@ -440,12 +440,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (ti.kind == 2) {
           // the softmax warps' partial writes were ordered before their epi arrivals, which this
-          // thread has observed: a gpu-scope release from here publishes them (cumulativity)
+          // thread has observed: a gpu-scope fence from here, then the flag stores, publishes them
+          // (cumulativity). One fence serves all eight flags: a release store each would fence
+          // again, eight round trips in a row (several us per partial on small shares).
           __threadfence();
           // (test-only fault injection: CTA 1 never publishes, so the CTA merging its partial
           // gives up its bounded wait on the flags and the launch reports a timeout)
           if (!(inject == kInjectFwdFlag && blockIdx.x == 1))
-            for (int w = 0; w < 8; ++w) ptx::st_release_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + w, epoch);
+            for (int w = 0; w < 8; ++w) ptx::st_relaxed_u32(flags + static_cast<size_t>(blockIdx.x) * 8 + w, epoch);
         } else {
           ptx::bulk_wait_read();  // both stores have read the buffer
         }

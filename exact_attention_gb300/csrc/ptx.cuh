@@ -510,6 +510,11 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
 __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// A relaxed gpu-scope store: after a fence it completes a release pattern, so one fence can
+// publish several flags (each st.release would fence again).
+__device__ __forceinline__ void st_relaxed_u32(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // ------------------------------------------------------------- packed f32 (f32x2)
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {

@@ -122,11 +122,12 @@ fa_status fa_fwd_ws(const void* Q, const void* K, const void* V, void* O, float*
  * The forward on HOST buffers: copies in, computes and copies out, overlapped.
  *
  * For callers whose Q, K, V live in host memory and who want O (and LSE) back
- * there. The (batch, head) heads are cut into 4 chunks (fa_set_schedule with
- * FA_SCHED_HOST_CHUNKS fixes another count, 1..8); the library's
- * own copy and compute streams for the device move chunk c in while chunk c-1
- * is computed (same kernels and results as fa_fwd_ws) and chunk c-2's output
- * travels back. The call is asynchronous and ordered on `stream`: work queued
+ * there. The (batch, head) heads are cut into three chunks of about 4/7, 2/7
+ * and 1/7 of them (equal chunks below seven heads; fa_set_schedule with
+ * FA_SCHED_HOST_CHUNKS fixes a count of equal chunks instead, 1..8); the
+ * library's own copy and compute streams for the device move chunk c in while
+ * chunk c-1 is computed (same kernels and results as fa_fwd_ws) and earlier
+ * chunks' outputs travel back. The call is asynchronous and ordered on `stream`: work queued
  * on `stream` before it happens first, and `stream` waits for the last copy
  * out before anything queued after it. Not for stream capture (the internal
  * streams and events are not part of a capture).
@@ -380,8 +381,9 @@ fa_status fa_set_wait_budget_ns(unsigned long long ns);
  *                         fa_fwd_host) off / on
  *   FA_SCHED_BWD_SPLIT    0 / 1: the fused backward's split schedule (fa_bwd_ws,
  *                         non-causal, D = 64) off / on
- *   FA_SCHED_HOST_CHUNKS  1..8: number of head chunks fa_fwd_host pipelines
- *                         (fa_fwd_host_workspace_bytes depends on it)
+ *   FA_SCHED_HOST_CHUNKS  1..8: number of equal head chunks fa_fwd_host
+ *                         pipelines (default -1: three chunks, 4:2:1;
+ *                         fa_fwd_host_workspace_bytes depends on it)
  *   FA_SCHED_BWD_PAIR     0 / 1: fa_bwd's dK/dV and dQ kernels (D = 64) on CTA
  *                         pairs (tcgen05 cta_group::2, 256 rows per pair) off / on;
  *                         automatic: on for non-causal calls with fewer key

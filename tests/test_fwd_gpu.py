@@ -207,12 +207,13 @@ def test_forward_f32_without_workspace(causal):
 
 
 HOST_CASES = [
-    # B, H, M, N, D, dtype, causal
+    # B, H, M, N, D, dtype, causal (default chunks: three, 4:2:1 from seven heads up)
     (1, 1, 256, 300, 64, "f16", False),    # one head: one chunk
-    (2, 3, 300, 200, 64, "bf16", True),    # six heads: six chunks, ragged M and N
-    (3, 5, 700, 1500, 64, "f16", False),   # 15 heads over 8 chunks (two sizes)
+    (2, 3, 300, 200, 64, "bf16", True),    # six heads: three equal chunks, ragged M and N
+    (3, 5, 700, 1500, 64, "f16", False),   # 15 heads in chunks of 9, 4 and 2
     (2, 2, 512, 512, 128, "f16", True),    # D = 128
     (1, 3, 256, 384, 64, "f32", False),    # f32 (3xTF32 path)
+    (1, 7, 256, 640, 64, "f32", False),    # f32, seven heads: 4, 2 and 1
 ]
 
 
@@ -238,6 +239,23 @@ def test_forward_host_buffers(B, H, M, N, D, dtype, causal, pinned):
         assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
         check_heads((q, k, v), to_f64(ho), to_f64(hl), dtype, causal, scale,
                     rel_l2=REL_L2_F32 if dtype == "f32" else None)
+
+
+@pytest.mark.parametrize("chunks", [2, 5, 8])
+def test_forward_host_buffers_forced_chunks(chunks):
+    """fa_set_schedule(FA_SCHED_HOST_CHUNKS, n): n equal chunks (15 heads: two sizes each)."""
+    import torch
+    B, H, M, N, D = 3, 5, 384, 700, 64
+    q, k, v = synth.attention_inputs(B, H, M, N, D, "bf16", seed=chunks)
+    hq, hk, hv = (to_device(x, "bf16").cpu().pin_memory() for x in (q, k, v))
+    ho, hl = torch.empty_like(hq).pin_memory(), torch.empty((B, H, M), dtype=torch.float32).pin_memory()
+    with fa.schedule(fa.FA_SCHED_HOST_CHUNKS, chunks):
+        nbytes = fa.fa_fwd_host_workspace_bytes(B, H, M, N, D, 0, fa.FA_BF16)
+        ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+        assert fa.fa_fwd_host(hq, hk, hv, ho, hl, ws, nbytes, B, H, M, N, D, 0.125, 0, fa.FA_BF16) == fa.FA_OK
+        torch.cuda.synchronize()
+    assert fa.fa_last_status() == fa.FA_OK, fa.fa_last_error_message()
+    check_heads((q, k, v), to_f64(ho), to_f64(hl), "bf16", False, 0.125)
 
 
 def test_forward_host_buffers_without_lse_and_checks():
