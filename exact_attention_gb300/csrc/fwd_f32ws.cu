@@ -80,6 +80,14 @@ __global__ void __launch_bounds__(256) f32_presplit_kernel(const float4* __restr
                                                            uint2* __restrict__ kp, uint2* __restrict__ vp,
                                                            long long quads) {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // this thread's lines of K and V into L2 while the kernel before finishes (one thread a line;
+  // up to 32 MB of them, a quarter of L2)
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < quads && quads <= (1ll << 20);
+       i += static_cast<long long>(gridDim.x) * blockDim.x)
+    if ((i & 7) == 0) {
+      ptx::prefetch_l2(K + i);
+      ptx::prefetch_l2(V + i);
+    }
   ptx::grid_dep_wait();  // K and V may come from the kernel before this one
   for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < quads;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -230,8 +238,16 @@ __global__ void __launch_bounds__(kThreadsW, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = hdr->tmem_base;
   ptx::WaitCtx wc{&hdr->abort_flag, status, budget_ns, kKernFwdF32};
-  // launched as a programmatic dependent of the prologue: global memory only after it completed
+  // launched as a programmatic dependent of the prologue: global memory only after it completed,
+  // but the softmax warps' first rows of Q (this thread's 128-byte half row) are brought into L2
+  // before, while the prologue runs
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (warp < 8 && static_cast<int>(blockIdx.x) < tiles * parts) {
+    int bh, q0, jb, nb;
+    tile_of(static_cast<int>(blockIdx.x), bh, q0, jb, nb);
+    const int row = q0 + (warp & 3) * 32 + lane;
+    if (nb > 0 && row < M) ptx::prefetch_l2(Q + (static_cast<size_t>(bh) * M + row) * kDw + (warp >> 2) * 32);
+  }
   ptx::grid_dep_wait();
 
   if (warp == kWarpProdW) {

@@ -165,6 +165,11 @@ static __device__ __noinline__ void mbar_wait_drain(uint32_t bar, uint32_t parit
 }
 
 // ---------------------------------------------------------------------- TMA
+// Brings the 128-byte line holding p into L2 (a hint: L2 stays coherent with later writes, so
+// it may run before griddepcontrol.wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
