@@ -174,6 +174,16 @@ def test_forward_split_schedule_matches_oracle(dtype, B, H, M, N, causal):
     check_heads(inputs, out, lse, dtype, causal, scale)
 
 
+@pytest.mark.parametrize("B,H,M,N,dtype", [(1, 4, 2048, 2048, "bf16"), (1, 2, 1024, 8192, "f16")])
+def test_forward_split_automatic_choice(B, H, M, N, dtype):
+    """Shapes whose pairs have many key blocks and fill few SMs take the split schedule without
+    forcing (32 pairs of 16 blocks; 8 pairs of 64 blocks, each cut into about 19 pieces, so the
+    holder of a pair's first blocks merges about 18 partials)."""
+    scale = 0.125
+    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, False, scale, seed=N + H)
+    check_heads(inputs, out, lse, dtype, False, scale)
+
+
 def test_forward_split_schedule_repeated_calls():
     """Back-to-back calls reuse one workspace; each launch's flags carry a new epoch, and the
     merging CTAs put the flags they consumed back to zero."""
@@ -295,7 +305,7 @@ NEG_CASES = [
     # B, H, M, N, D, dtype, causal, scale
     (1, 2, 300, 200, 64, "f16", False, -0.125),
     (1, 2, 300, 700, 64, "bf16", True, -0.2),
-    (2, 3, 1000, 900, 64, "f16", False, -0.125),  # split schedule at automatic choice
+    (1, 4, 2048, 2048, 64, "f16", False, -0.125),  # split schedule at automatic choice
     (1, 2, 384, 256, 128, "f16", True, -1 / math.sqrt(128)),
     (1, 1, 256, 300, 64, "f32", False, -0.125),
     (1, 1, 5, 700, 64, "f32", True, -0.3),
