@@ -245,14 +245,22 @@ bool use_split(int BH, int M, int N, int causal, int num_sms) {
   if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
   const int forced = g_sched_fwd_split.load();
   if (forced >= 0) return forced == 1;
-  // causal: whole pairs dealt in a serpentine order (heaviest with lightest) measured faster
-  // than the split, whose extra pieces cost more than the balance gains
-  if (causal) return false;
   const double nkb = static_cast<double>((N + 127) / 128);
-  const double rounds = static_cast<double>((pairs + num_sms - 1) / num_sms);
   const double share = static_cast<double>(units) / num_sms;
   const double partials = std::max(0.0, std::ceil(nkb / share) - 1.0);
-  return share + 3.5 + 1.2 * partials < 0.97 * rounds * nkb;
+  const double split = share + 3.5 + 1.2 * partials;
+  if (causal) {
+    // whole pairs dealt in a serpentine order (heaviest with lightest) measured faster than the
+    // split from a round of pairs up (B4 H12 N2048 44.1 against 50.9 us, B1 H16 N8192 151 against
+    // 167): the split's extra pieces cost more than the balance gains. With fewer pairs than SMs
+    // each pair has an SM and the call takes as long as the heaviest, tile 0 of a head's last pair
+    // (B1 H4 N4096: 44.0 us whole, 25.4 split; B4 H12 N512 and N1024 stay whole).
+    if (pairs >= num_sms) return false;
+    const double pph = static_cast<double>((M + 255) / 256);
+    return split < 0.97 * std::min(nkb, 2.0 * pph - 1.0);
+  }
+  const double rounds = static_cast<double>((pairs + num_sms - 1) / num_sms);
+  return split < 0.97 * rounds * nkb;
 }
 
 // Whether the fused backward (fa_bwd_ws, D = 64) runs its split schedule: non-causal calls

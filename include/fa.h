@@ -106,10 +106,13 @@ size_t fa_fwd_workspace_bytes(int B, int H, int M, int N, int D, int causal, fa_
  *                    workspace at the same time.
  *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
  *
- * The split is used when the call is not causal, every SM gets at least four key
- * blocks and the last wave would be less than 90 % full (causal pairs, whose key
- * ranges differ in length, are dealt whole in a serpentine order, which measured
- * faster); fa_set_schedule(FA_SCHED_FWD_SPLIT, 0 or 1) turns it off or on regardless.
+ * The split is used when an estimate of its time in key blocks per SM (its
+ * share, plus 3.5 for piece boundaries and the merge, plus 1.2 for each further
+ * partial the holder of a pair's first blocks merges) is below 0.97 of whole
+ * pairs' (non-causal: rounds x key blocks a pair; causal: the heaviest pair,
+ * and only with fewer pairs than SMs, since from a round of pairs up causal
+ * pairs dealt whole in a serpentine order measured faster);
+ * fa_set_schedule(FA_SCHED_FWD_SPLIT, 0 or 1) turns it off or on regardless.
  * For f32 with few query tiles, several CTAs share each tile's keys: each writes
  * an unnormalised partial and counts itself in on the tile, and the one that
  * counts in last merges the partials the same way and writes O and LSE.

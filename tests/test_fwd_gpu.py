@@ -174,14 +174,15 @@ def test_forward_split_schedule_matches_oracle(dtype, B, H, M, N, causal):
     check_heads(inputs, out, lse, dtype, causal, scale)
 
 
-@pytest.mark.parametrize("B,H,M,N,dtype", [(1, 4, 2048, 2048, "bf16"), (1, 2, 1024, 8192, "f16")])
-def test_forward_split_automatic_choice(B, H, M, N, dtype):
+@pytest.mark.parametrize("B,H,M,N,dtype,causal", [(1, 4, 2048, 2048, "bf16", False), (1, 2, 1024, 8192, "f16", False),
+                                                    (1, 2, 4096, 4096, "f16", True)])
+def test_forward_split_automatic_choice(B, H, M, N, dtype, causal):
     """Shapes whose pairs have many key blocks and fill few SMs take the split schedule without
-    forcing (32 pairs of 16 blocks; 8 pairs of 64 blocks, each cut into about 19 pieces, so the
-    holder of a pair's first blocks merges about 18 partials)."""
+    forcing: 32 pairs of 16 blocks; 8 pairs of 64 blocks, each cut into about 19 pieces, so the
+    holder of a pair's first blocks merges about 18 partials; causal, 32 pairs of 1 to 31 blocks."""
     scale = 0.125
-    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, False, scale, seed=N + H)
-    check_heads(inputs, out, lse, dtype, False, scale)
+    inputs, out, lse = run_fwd(B, H, M, N, 64, dtype, causal, scale, seed=N + H)
+    check_heads(inputs, out, lse, dtype, causal, scale)
 
 
 def test_forward_split_schedule_repeated_calls():
