@@ -211,9 +211,8 @@ std::atomic<int> g_sched_host_chunks{-1};
 std::atomic<int> g_sched_bwd_pair{-1};
 constexpr int kHostChunks = 8;  // most head chunks of fa_fwd_host (events kept per device)
 
-// Whether a forward call with a workspace runs the split schedule (D = 64 halves).
-// fa_set_schedule(FA_SCHED_FWD_SPLIT, 0 / 1) forces it off / on; by default it is used for
-// non-causal calls when whole pairs would leave the last wave of CTAs less than 90 % full.
+// Whether a forward call with a workspace can run the split schedule (D = 64 halves); use_split
+// below decides whether it does.
 bool split_capable(int D, int dtype) { return D == 64 && dtype != FA_F32; }
 
 // Units of the D=64 forward's split schedule: the key blocks of each query-tile pair's tile 0
