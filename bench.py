@@ -102,6 +102,22 @@ def load_peaks():
 
 
 # ------------------------------------------------------------------ clocks
+def other_gpu_processes(device_index: int):
+    """Compute processes on this GPU other than this one (nvidia-smi), or None if unavailable."""
+    try:
+        out = subprocess.run(["nvidia-smi", "-i", str(device_index), "--query-compute-apps=pid,used_memory",
+                              "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20).stdout
+    except Exception:
+        return None
+    me = os.getpid()
+    procs = []
+    for ln in out.splitlines():
+        f = [x.strip() for x in ln.split(",")]
+        if len(f) >= 2 and f[0].isdigit() and int(f[0]) != me:
+            procs.append({"pid": int(f[0]), "mib": f[1]})
+    return procs
+
+
 class ClockSampler:
     """nvidia-smi samples (50 ms) of SM clock and throttle reasons while running, each stamped with
     the host clock so that they can be binned by phase."""
@@ -349,21 +365,33 @@ def run_ours(args):
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
-    def steps(n):
+    NCHUNK = 10  # events inside each part: per-chunk times show whether a slow part was slow throughout
+
+    def steps(n, chunks=None):
         """n steps: step i runs the forward and the backward on input set i % ROTATE and one decode.
-        Each part's n calls run back to back between one pair of CUDA events; returns their times."""
+        Each part's n calls run back to back between one pair of CUDA events; returns their times.
+        With `chunks` (a dict), each part's calls are also cut into NCHUNK chunks between events."""
         e = [ev() for _ in range(6)]
+
+        def part(k, run):
+            marks = []
+            for i in range(n):
+                if chunks is not None and i % max(1, n // NCHUNK) == 0 and len(marks) < NCHUNK:
+                    marks.append((i, ev()))
+                    marks[-1][1].record(stream)
+                run(i)
+            if chunks is not None:
+                end = ev()
+                end.record(stream)
+                chunks[k] = (marks, end)
         e[0].record(stream)
-        for i in range(n):
-            run_fwd(i)
+        part("fwd", run_fwd)
         e[1].record(stream)
         e[2].record(stream)
-        for i in range(n):
-            run_bwd(i)
+        part("bwd", run_bwd)
         e[3].record(stream)
         e[4].record(stream)
-        for _ in range(n):
-            run_dec()
+        part("decode", lambda i: run_dec())
         e[5].record(stream)
         return e
 
@@ -371,11 +399,14 @@ def run_ours(args):
     check(fa.fa_last_status(stream), "warm-up")
     torch.cuda.synchronize()
 
+    load_before = os.getloadavg()[0] if hasattr(os, "getloadavg") else None
+    foreign = other_gpu_processes(local)
+    chunk_ev = {}
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        e = steps(args.steps)
+        e = steps(args.steps, chunk_ev)
         torch.cuda.synchronize()
         barrier(world)
         wall = time.perf_counter() - t0
@@ -590,6 +621,13 @@ def run_ours(args):
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(clock_phases),
         "wall_s": round(wall, 3),
+        # the main step's parts cut into chunks (microseconds per call in each), the host's load
+        # average before the timed region and other processes on this GPU: context for a slow run
+        "chunks_us_per_call": {k: [round(a.elapsed_time(b) * 1e3 / max(1, j - i), 2)
+                                   for (i, a), (j, b) in zip(m, m[1:] + [(args.steps, end)])]
+                               for k, (m, end) in chunk_ev.items()},
+        "host_load": round(load_before, 2) if load_before is not None else None,
+        "other_gpu_processes": foreign,
     }
     if not args.no_cpu_baseline and world == 1:
         tf, heads, secs, thr = oracle_forward_sample(args.cpu_seconds)
