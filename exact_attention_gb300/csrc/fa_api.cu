@@ -262,19 +262,29 @@ bool use_split(int BH, int M, int N, int causal, int num_sms) {
   return split < 0.97 * rounds * nkb;
 }
 
-// Whether the fused backward (fa_bwd_ws, D = 64) runs its split schedule: non-causal calls
-// whose whole key tiles would leave the last round of CTAs less than 90 % full.
-// fa_set_schedule(FA_SCHED_BWD_SPLIT, 0 / 1) forces it off / on (non-causal only).
+// Whether the fused backward (fa_bwd_ws, D = 64) runs its split schedule (non-causal calls only).
+// Estimated times in (key tile, query block) steps per SM: whole key tiles take rounds * nqb;
+// the split takes its share, units / num_sms, plus about 5 steps for its piece boundaries and
+// merge, plus 0.8 for each further partial the holder of a key tile's first blocks adds (a tile
+// spans about nqb / share shares). Fitted to back-to-back times at twelve shapes (a step is
+// 1.2-1.9 us): the split wins where key tiles have many query blocks and fill few SMs or leave
+// the last round part-empty (B1 H1 N4096 34.3 against 58.9 us, B4 H12 N2048 163.4 against 180.3,
+// B1 H4 N2048 31.8 against 35.8); whole tiles win with few query blocks a tile or many tiles
+// (B1 H16 N1024 25.2 against 31.4 us, B4 H12 N1024 59.0 against 61.5, B8 H16 N2048 418 against
+// 454). Within 3 % the call keeps whole tiles. fa_set_schedule(FA_SCHED_BWD_SPLIT, 0 / 1) forces
+// it off / on (non-causal only).
 bool use_bwd_split(int BH, int M, int N, int D, int causal, int num_sms) {
   if (D != 64 || causal) return false;
   const long long items = static_cast<long long>(BH) * ((N + 127) / 128);
-  const long long units = items * ((M + 127) / 128);
+  const long long nqb = (M + 127) / 128;
+  const long long units = items * nqb;
   if (units >= (1ll << 31)) return false;  // the kernel indexes units in 32 bits
   const int forced = g_sched_bwd_split.load();
   if (forced >= 0) return forced == 1;
-  if (units < 4ll * num_sms) return false;
-  const long long rounds = (items + num_sms - 1) / num_sms;
-  return items * 10 < rounds * num_sms * 9;
+  const double share = static_cast<double>(units) / num_sms;
+  const double partials = std::max(0.0, std::ceil(static_cast<double>(nqb) / share) - 1.0);
+  const double rounds = static_cast<double>((items + num_sms - 1) / num_sms);
+  return share + 5.0 + 0.8 * partials < 0.97 * rounds * static_cast<double>(nqb);
 }
 
 // Launch epochs of the split schedules' flags and counters. The sequence starts at a value

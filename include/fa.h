@@ -213,11 +213,16 @@ size_t fa_bwd_workspace_bytes(int B, int H, int M);
  *                    every part it reads (no zero-fill needed); caller-owned,
  *                    one call at a time.
  *   workspace_bytes  its size; smaller than needed is FA_ERR_INVALID.
- * Non-causal calls with D = 64 whose key tiles (B*H*ceil(N/128)) would
- * leave the last round of SMs under 90 % busy run a split schedule: every SM
- * takes an equal share of the (key tile, query block) pairs, and each SM
- * holding part of a cut key tile writes its partial dK/dV; whichever finishes
- * last adds the others' and writes the tile (no SM waits for another).
+ * Non-causal calls with D = 64 may run a split schedule: every SM takes a
+ * contiguous share of the (key tile, query block) pairs. The SMs holding the
+ * later blocks of a cut key tile take those pieces first and write their
+ * partial dK/dV; the SM holding its first blocks takes its piece last, waits
+ * (bounded, fa_set_wait_budget_ns) until they have counted in, adds them and
+ * writes the tile. The split is used when an estimate of its time in (key tile,
+ * query block) steps per SM (its share, plus 5 for piece boundaries and the
+ * merge, plus 0.8 per further partial a tile's first-block holder adds) is below
+ * 0.97 of whole tiles' (rounds x ceil(M/128));
+ * fa_set_schedule(FA_SCHED_BWD_SPLIT, 0 or 1) turns it off or on regardless.
  * The summation order of dQ's key blocks follows the SMs' timing, so dQ can
  * differ between runs in the last bits of the f32 accumulator, and so can dK
  * and dV of a key tile the split schedule cuts (otherwise they do not).
