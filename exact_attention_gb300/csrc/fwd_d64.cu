@@ -46,18 +46,13 @@ using fwdc::ffma2;
 using fwdc::fmax3;
 using fwdc::kBM;
 using fwdc::kBN;
-using fwdc::classic_tile;
 using fwdc::mask32;
-using fwdc::tile_info;
-using fwdc::TileInfo;
-using fwds::kMaxSplitCtas;
 using fwds::kPairRows;
 using fwds::kSlotFloats;
 using fwds::Piece;
 using fwds::Schedule;
 using fwds::split_bounds;
 using fwds::SplitBounds;
-using fwds::unit_pair;
 using fwds::units_before;
 
 constexpr int kD = 64;
