@@ -46,6 +46,7 @@ EXPORTS = (
     "fa_set_wait_budget_ns",
     "fa_set_schedule",
     "fa_debug_inject",
+    "fa_debug_schedule_choice",
 )
 
 _lib = None
@@ -113,6 +114,8 @@ def lib() -> ctypes.CDLL:
     L.fa_set_schedule.restype = st
     L.fa_debug_inject.argtypes = [i]
     L.fa_debug_inject.restype = st
+    L.fa_debug_schedule_choice.argtypes = [i] * 7
+    L.fa_debug_schedule_choice.restype = i
     _lib = L
     return L
 
@@ -249,6 +252,10 @@ class schedule:
 
 def fa_debug_inject(kind: int) -> int:
     return lib().fa_debug_inject(int(kind))
+
+
+def fa_debug_schedule_choice(which: int, B: int, H: int, M: int, N: int, causal: bool, num_sms: int) -> int:
+    return lib().fa_debug_schedule_choice(int(which), B, H, M, N, int(causal), num_sms)
 
 
 

@@ -427,6 +427,16 @@ fa_status fa_set_schedule(fa_sched_key key, int value);
  */
 fa_status fa_debug_inject(int kind);
 
+/*
+ * Test-only: the schedule the library would choose, without launching anything
+ * (no GPU needed). which = 0: the fp16/bf16 D = 64 forward with a workspace
+ * (fa_fwd_ws); which = 1: the fused backward (fa_bwd_ws, D = 64). num_sms is
+ * the device's SM count to assume. Returns 1 for the split schedule, 0 for
+ * whole query pairs / key tiles, -1 for an unknown `which` or a non-positive
+ * size. A setting made with fa_set_schedule applies as it does to the calls.
+ */
+int fa_debug_schedule_choice(int which, int B, int H, int M, int N, int causal, int num_sms);
+
 #ifdef __cplusplus
 }
 #endif
