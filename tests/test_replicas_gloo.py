@@ -45,7 +45,7 @@ def test_two_gloo_replicas():
     import torch.multiprocessing as mp
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork: this process may already hold a CUDA context
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert sorted(out.keys()) == [0, 1]
