@@ -505,6 +505,7 @@ fa_status fa_debug_inject(int kind) {
 
 int fa_debug_schedule_choice(int which, int B, int H, int M, int N, int causal, int num_sms) {
   if (B <= 0 || H <= 0 || M <= 0 || N <= 0 || num_sms <= 0) return -1;
+  if (static_cast<long long>(B) * H > INT_MAX) return -1;
   if (which == 0) return use_split(B * H, M, N, causal, num_sms) ? 1 : 0;
   if (which == 1) return use_bwd_split(B * H, M, N, 64, causal, num_sms) ? 1 : 0;
   return -1;

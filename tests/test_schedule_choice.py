@@ -70,3 +70,4 @@ def test_forced_schedules_and_invalid_queries():
     assert fa.fa_debug_schedule_choice(2, 1, 1, 128, 128, False, SMS) == -1
     assert fa.fa_debug_schedule_choice(0, 0, 1, 128, 128, False, SMS) == -1
     assert fa.fa_debug_schedule_choice(0, 1, 1, 128, 128, False, 0) == -1
+    assert fa.fa_debug_schedule_choice(0, 1 << 16, 1 << 16, 128, 128, False, SMS) == -1  # B*H past int
